@@ -1,0 +1,449 @@
+#!/usr/bin/env python3
+"""Benchmark of one decode step over an FP8-quantised, paged KV cache.
+
+A step is the whole hot path for one batch: append every request's new
+token (absmax scale, FP8 rounding, slot scatter) and run paged decode
+attention over the full cache (plan, split kernel, merge).  The default
+workload is one Llama-3-70B-shaped decode layer: 12 requests x 16384 cached
+tokens, 64 query / 8 KV heads, head_dim 128, E4M3 codes with one scale per
+(token, kv head), block size 16 -- 415 MB of cache read per step, more than
+the 129 MB L2, so no flush is needed between steps.
+
+Output: one JSON line (rank 0).  `value` is the achieved algorithmic HBM
+bandwidth of the step in GB/s; `roofline` is for the split kernel alone,
+timed with CUDA events around its launch; `e2e` is the same metric through
+the public API with pinned host inputs copied in and the output copied back
+inside the timed region; `cpu_baseline` times the CPU oracle on a bounded
+sample of the same workload.
+
+Multi-GPU (torchrun): replicas only -- every rank runs its own copy of the
+workload with no collective on the data path (weak scaling); the step time
+is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from fp8_quantised_paged_gb300 import workloads as W  # noqa: E402
+
+METRIC = "FP8 paged decode attn: achieved HBM GB/s (% of GB300 peak), KV tokens/s"
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["fp8pa", "reference"], default="fp8pa")
+    ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--traffic-json", default=os.path.join(ROOT, "profiles", "traffic.json"),
+                    help="per-launch DRAM bytes of the split kernel from an ncu capture")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------- accounting
+def accounting(w: W.Workload, b_sel=None) -> dict:
+    """Algorithmic bytes of one step (or of the requests in b_sel)."""
+    bs = w.block_size
+    lens = w.seq_lens if b_sel is None else w.seq_lens[list(b_sel)]
+    B = len(lens)
+    ntens = 1 if w.mla else 2
+    kv_tokens = int(lens.sum())
+    codes = w.head_dim * w.n_kv_heads * ntens
+    if w.scale_mode == W.SCALE_TOKEN_HEAD:
+        sc_tok = 4 * w.n_kv_heads * ntens
+    elif w.scale_mode == W.SCALE_TOKEN_GROUP:
+        sc_tok = 4 * w.n_kv_heads * (w.head_dim // w.group_size) * ntens
+    else:
+        sc_tok = 0
+    static_sc = 4 * w.n_kv_heads * w.head_dim * ntens if w.scale_mode == W.SCALE_CHANNEL_STATIC else 0
+    kv = kv_tokens * (codes + sc_tok) + static_sc
+    q = B * w.n_q_heads * w.head_dim * 2
+    out = B * w.n_q_heads * w.head_dim_v * 2
+    pages = int(sum(math.ceil(int(L) / bs) for L in lens))
+    tables = pages * 4 + B * 4
+    split = kv + q + tables
+    decode = split + out
+    append = B * (codes * 2 + codes + sc_tok) + B * 4
+    return {"kv_tokens": kv_tokens, "bytes_per_token": codes + sc_tok, "split": split,
+            "decode": decode, "append": append, "step": decode + append}
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{index}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index),
+                                          f"--query-gpu={self.FIELDS}", "--format=csv,noheader",
+                                          "-lms", "100"], stdout=self.f,
+                                         stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self) -> dict | None:
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        sms, maxs, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sms.append(float(parts[1].split()[0]))
+                maxs.append(float(parts[2].split()[0]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sms:
+            return None
+        return {"sm_mhz": statistics.median(sms), "sm_max_mhz": max(maxs),
+                "reasons": sorted(reasons), "samples": len(sms)}
+
+
+# ---------------------------------------------------------------- helpers
+def peaks() -> dict:
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6800.0, "source": "fallback"}
+
+
+def traffic_per_launch(path, workload_name):
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        e = d.get(workload_name)
+        return None if e is None or e.get("stale") else float(e["dram_bytes_per_launch"])
+    except (OSError, ValueError, KeyError, TypeError):
+        return None
+
+
+def to_bf16_tensor(bits, device):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(device)
+
+
+# ---------------------------------------------------------------- CPU oracle timing
+def oracle_sample(w: W.Workload, b: int, heads=None, threads=None):
+    """Run the oracle (append of request b's tokens into a compact pool, then
+    attention for `heads` of request b).  Returns (seconds, bytes)."""
+    import oracle
+    k, v = W.request_kv(w, b)
+    L = int(w.seq_lens[b])
+    bs, hkv, d = w.block_size, w.n_kv_heads, w.head_dim
+    nbl = (L + bs - 1) // bs
+    ng = d // w.group_size if w.scale_mode == W.SCALE_TOKEN_GROUP else 1
+    kc = np.zeros((nbl, hkv, bs, d), np.uint8)
+    vc = None if w.mla else np.zeros_like(kc)
+    if w.scale_mode == W.SCALE_CHANNEL_STATIC:
+        ks = oracle.kv_channel_scales(k, w.fmt)
+        vs = oracle.kv_channel_scales(v, w.fmt)
+    else:
+        ks = np.zeros((nbl, hkv, bs, ng), np.float32)
+        vs = None if w.mla else np.zeros_like(ks)
+    t = np.arange(L)
+    slots = (t // bs * bs + t % bs).astype(np.int32)
+    bt = np.arange(nbl, dtype=np.int32)[None]
+    sl = np.array([L], np.int32)
+    q = W.queries(w)[b:b + 1]
+    heads = list(range(w.n_q_heads)) if heads is None else list(heads)
+    t0 = time.perf_counter()
+    oracle.kv_append_quant(k, v, slots, w.fmt, w.scale_mode, w.group_size, kc, vc, ks, vs, bs)
+    if w.mla:
+        vc, vs = kc, ks
+    oracle.paged_decode_attention(q, kc, vc, ks, vs, bt, sl, bs, hkv, w.head_dim_v, w.fmt,
+                                  w.scale_mode, w.group_size, w.sm_scale,
+                                  rows=np.array(heads, np.int32), num_threads=threads)
+    dt = time.perf_counter() - t0
+    acc = accounting(w, [b])
+    frac = len(heads) / w.n_q_heads
+    return dt, acc["step"] * frac, acc["kv_tokens"] * frac
+
+
+def run_reference(args, rank):
+    """The CPU oracle as the reference arm: every step is a bounded sample
+    (one request, one KV head's query group) of the same workload."""
+    import oracle
+    if rank != 0:
+        return
+    w = W.make_workload(args.workload, "full")
+    G = w.n_q_heads // w.n_kv_heads
+    threads = oracle.max_threads()
+    times, nbytes, toks = [], 0.0, 0.0
+    for i in range(args.warmup + args.steps):
+        b = i % w.batch
+        kvh = (i // w.batch) % w.n_kv_heads
+        dt, by, tk = oracle_sample(w, b, heads=range(kvh * G, kvh * G + G), threads=threads)
+        if i >= args.warmup:
+            times.append(dt)
+            nbytes += by
+            toks += tk
+    total = sum(times)
+    value = nbytes / total / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "kv_tokens_per_s": toks / total,
+            "config": dict(w.describe(), sample="one request x one KV head group per step"),
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                             "sample": f"request i % {w.batch}, query heads of one KV head, "
+                                       "append of that request + attention"},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- GPU arm
+def run_gpu(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+    import fp8_quantised_paged_gb300 as F
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    w = W.make_workload(args.workload, "full")
+    acc = accounting(w)
+    nb, hkv, bs, d = w.num_blocks, w.n_kv_heads, w.block_size, w.head_dim
+    ntens = 1 if w.mla else 2
+    ng = d // w.group_size if w.scale_mode == W.SCALE_TOKEN_GROUP else 1
+
+    # ---- cache: prefill every request's first L-1 tokens through the library
+    kc = torch.zeros((nb, hkv, bs, d), dtype=torch.uint8, device=dev)
+    vc = None if w.mla else torch.zeros_like(kc)
+    last_k, last_v = [], []
+    if w.scale_mode == W.SCALE_CHANNEL_STATIC:
+        kvs = [W.request_kv(w, b) for b in range(w.batch)]
+        ks = F.kv_channel_scales(to_bf16_tensor(np.concatenate([k for k, _ in kvs]), dev), w.fmt)
+        vs = F.kv_channel_scales(to_bf16_tensor(np.concatenate([v for _, v in kvs]), dev), w.fmt)
+        get = lambda b: kvs[b]
+    else:
+        ks = torch.zeros((nb, hkv, bs, ng), dtype=torch.float32, device=dev)
+        vs = None if w.mla else torch.zeros_like(ks)
+        get = lambda b: W.request_kv(w, b)
+    for b in range(w.batch):
+        k, v = get(b)
+        L = int(w.seq_lens[b])
+        if L > 1:
+            F.kv_append_quant(to_bf16_tensor(k[:L - 1], dev),
+                              None if v is None else to_bf16_tensor(v[:L - 1], dev),
+                              torch.from_numpy(W.token_slots(w, b, 0, L - 1)).to(dev), kc, vc,
+                              ks, vs, fmt=w.fmt, scale_mode=w.scale_mode,
+                              group_size=w.group_size)
+        last_k.append(k[L - 1])
+        if v is not None:
+            last_v.append(v[L - 1])
+    if w.mla:
+        vc_, vs_ = kc, ks
+    else:
+        vc_, vs_ = vc, vs
+
+    # ---- step inputs, resident
+    q_h = W.queries(w)
+    kn_h = np.stack(last_k)
+    vn_h = None if w.mla else np.stack(last_v)
+    slot_h = W.step_slots(w)
+    q = to_bf16_tensor(q_h, dev)
+    kn = to_bf16_tensor(kn_h, dev)
+    vn = None if w.mla else to_bf16_tensor(vn_h, dev)
+    slots = torch.from_numpy(slot_h).to(dev)
+    bt = torch.from_numpy(w.block_tables).to(dev)
+    sl = torch.from_numpy(w.seq_lens).to(dev)
+    out = torch.empty((w.batch, w.n_q_heads, w.head_dim_v), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(F.decode_workspace_bytes(w.batch, w.n_q_heads, hkv, d, w.head_dim_v, bs,
+                                              w.max_blocks, dev), dtype=torch.uint8, device=dev)
+
+    def step(q_, kn_, vn_, slots_, sl_):
+        F.kv_append_quant(kn_, vn_, slots_, kc, vc, ks, vs, fmt=w.fmt, scale_mode=w.scale_mode,
+                          group_size=w.group_size)
+        F.paged_decode_attention(q_, kc, vc_, ks, vs_, bt, sl_, hkv, w.sm_scale, fmt=w.fmt,
+                                 scale_mode=w.scale_mode, group_size=w.group_size,
+                                 head_dim_v=w.head_dim_v, out=out, workspace=ws)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        step(q, kn, vn, slots, sl)
+    torch.cuda.synchronize()
+    assert F.get_device_error() == 0, "device error during warm-up"
+
+    # ---- timed region (device-resident inputs)
+    from fp8_quantised_paged_gb300 import _native as N
+    import ctypes
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    for a, b_ in ev:  # materialise the event handles
+        a.record()
+        b_.record()
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_stop = torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.3)
+    barrier()
+    torch.cuda.synchronize()
+    t_start.record()
+    for i in range(args.steps):
+        N.check(N.lib.fp8pa_set_split_events(ctypes.c_void_p(ev[i][0].cuda_event),
+                                             ctypes.c_void_p(ev[i][1].cuda_event)), "events")
+        step(q, kn, vn, slots, sl)
+    t_stop.record()
+    torch.cuda.synchronize()
+    barrier()
+    N.check(N.lib.fp8pa_set_split_events(None, None), "events")
+    clk = clocks.stop()
+    ms_total = t_start.elapsed_time(t_stop)
+    split_ms = [a.elapsed_time(b_) for a, b_ in ev]
+    if world > 1:
+        t = torch.tensor([ms_total], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / args.steps
+    assert F.get_device_error() == 0, "device error during the timed region"
+
+    # ---- end to end through the public API with pinned host buffers
+    e2e = None
+    if not args.no_e2e:
+        def pin(a):
+            return torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+        q_p = pin(q_h.view(np.int16))
+        kn_p = pin(kn_h.view(np.int16))
+        vn_p = None if w.mla else pin(vn_h.view(np.int16))
+        sl_p = pin(w.seq_lens)
+        slot_p = pin(slot_h)
+        out_p = torch.empty(out.shape, dtype=torch.bfloat16).pin_memory()
+        qd, knd = torch.empty_like(q), torch.empty_like(kn)
+        vnd = None if w.mla else torch.empty_like(vn)
+        sld, slotd = torch.empty_like(sl), torch.empty_like(slots)
+        h2d = q_p.numel() * 2 + kn_p.numel() * 2 + (0 if vn_p is None else vn_p.numel() * 2) \
+            + sl_p.numel() * 4 + slot_p.numel() * 4
+        d2h = out_p.numel() * 2
+
+        def e2e_step():
+            qd.view(torch.int16).copy_(q_p, non_blocking=True)
+            knd.view(torch.int16).copy_(kn_p, non_blocking=True)
+            if vnd is not None:
+                vnd.view(torch.int16).copy_(vn_p, non_blocking=True)
+            sld.copy_(sl_p, non_blocking=True)
+            slotd.copy_(slot_p, non_blocking=True)
+            step(qd, knd, vnd, slotd, sld)
+            out_p.copy_(out, non_blocking=True)
+            torch.cuda.current_stream().synchronize()
+
+        for _ in range(args.warmup):
+            e2e_step()
+        barrier()
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            e2e_step()
+        e2e_s = (time.perf_counter() - t0) / args.steps
+        if world > 1:
+            t = torch.tensor([e2e_s], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_s = float(t.item())
+        e2e = {"value": world * acc["step"] / e2e_s / 1e9, "unit": "GB/s",
+               "ms_per_step": e2e_s * 1e3, "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h)}
+
+    if rank != 0:
+        return
+    pk = peaks()
+    split_avg_ms = statistics.mean(split_ms)
+    achieved = acc["split"] / (split_avg_ms * 1e-3) / 1e9
+    traffic = traffic_per_launch(args.traffic_json, w.name)
+    value = world * acc["step"] / (ms_step * 1e-3) / 1e9
+    line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "pct_of_peak_hbm": 100.0 * value / world / pk["hbm_gbs"],
+            "kv_tokens_per_s": world * acc["kv_tokens"] / (ms_step * 1e-3),
+            "config": dict(w.describe(), parallelism=f"replicas x{world}",
+                           kv_dtype="e4m3" if w.fmt == W.E4M3 else "e5m2",
+                           compute="fp8 codes -> f16 warp MMA, f32 accumulate and softmax",
+                           l2="no flush: every step reads the whole cache, larger than L2",
+                           step="append (1 token/request) + plan + split + merge",
+                           bytes_per_step=acc["step"]),
+            "roofline": {"kernel": "gqa_split_kernel", "bound": "hbm",
+                         "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                         "frac": achieved / pk["hbm_gbs"], "traffic": traffic,
+                         "algorithmic_bytes_per_launch": acc["split"],
+                         "avg_launch_ms": split_avg_ms, "peak_source": pk["source"] +
+                         " (MEASURED_PEAKS.json hbm_gbs, copy bandwidth)"},
+            "gpu_launches": 4 * args.steps,
+            "clocks": clk,
+            "e2e": e2e}
+    if not args.no_cpu_baseline:
+        import oracle
+        threads = oracle.max_threads()
+        G = w.n_q_heads // w.n_kv_heads
+        dt, by, _ = oracle_sample(w, 0, heads=range(0, G), threads=threads)
+        line["cpu_baseline"] = {"value": by / dt / 1e9, "unit": "GB/s", "cores": threads,
+                                "kind": "oracle",
+                                "sample": "request 0: append of its tokens + attention of the "
+                                          f"{G} query heads of KV head 0 ({dt:.2f} s)"}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    try:
+        run_gpu(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

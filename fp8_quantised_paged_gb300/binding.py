@@ -1,0 +1,153 @@
+"""FP8-quantised paged decode attention for GB300 (sm_103a).
+
+Two calls, both hand-written CUDA kernels behind a C ABI (``include/fp8pa.h``):
+
+* :func:`kv_append_quant` -- absmax-scale each new token's K/V rows, round
+  them to E4M3 or E5M2 and scatter codes and scales into the paged cache.
+* :func:`paged_decode_attention` -- grouped-query (or shared-latent MLA)
+  attention of one query token per request over its paged FP8 cache, split
+  across the GPU and merged.
+
+These wrappers only check torch tensors and pass their device pointers and
+the current CUDA stream to the library.  PyTorch provides memory and streams;
+all arithmetic runs in the library's kernels.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _native as N
+from ._native import (E4M3, E5M2, OUT_BF16, OUT_F32, SCALE_CHANNEL_STATIC, SCALE_TOKEN_GROUP,
+                      SCALE_TOKEN_HEAD, Fp8paError)
+
+__all__ = ["kv_append_quant", "kv_channel_scales", "paged_decode_attention",
+           "decode_workspace_bytes", "get_device_error", "set_decode_workers", "version",
+           "E4M3", "E5M2", "SCALE_TOKEN_HEAD", "SCALE_CHANNEL_STATIC", "SCALE_TOKEN_GROUP",
+           "OUT_BF16", "OUT_F32", "Fp8paError"]
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _need(t, dtype, name, device=None):
+    if t is None:
+        return
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def version() -> int:
+    return int(N.lib.fp8pa_version())
+
+
+def set_decode_workers(workers: int) -> None:
+    N.check(N.lib.fp8pa_set_decode_workers(int(workers)), "set_decode_workers")
+
+
+def kv_append_quant(k, v, slot_mapping, k_cache, v_cache, k_scale, v_scale, fmt=E4M3,
+                    scale_mode=SCALE_TOKEN_HEAD, group_size=64, stream=None):
+    """k, v: bf16 [num_tokens, Hkv, D] (v may be None for the MLA latent);
+    slot_mapping: int32 [num_tokens]; caches: uint8 [num_blocks, Hkv, bs, D];
+    scales: float32 per the scale mode (see include/fp8pa.h)."""
+    _need(k, torch.bfloat16, "k")
+    dev = k.device
+    _need(v, torch.bfloat16, "v", dev)
+    _need(slot_mapping, torch.int32, "slot_mapping", dev)
+    _need(k_cache, torch.uint8, "k_cache", dev)
+    _need(v_cache, torch.uint8, "v_cache", dev)
+    _need(k_scale, torch.float32, "k_scale", dev)
+    _need(v_scale, torch.float32, "v_scale", dev)
+    n, hkv, d = k.shape
+    nb, _, bs, _ = k_cache.shape
+    with torch.cuda.device(dev):
+        rc = N.lib.fp8pa_kv_append_quant(_ptr(k), _ptr(v), _ptr(slot_mapping), n, hkv, d, fmt,
+                                         scale_mode, group_size, _ptr(k_cache), _ptr(v_cache),
+                                         _ptr(k_scale), _ptr(v_scale), nb, bs, _stream(stream))
+    N.check(rc, "kv_append_quant")
+
+
+def kv_channel_scales(x, fmt=E5M2, out=None, stream=None):
+    """Static per-channel scales max(absmax over tokens / FMAX, 1e-12) of a
+    bf16 [N, Hkv, D] tensor; returns float32 [Hkv, D]."""
+    _need(x, torch.bfloat16, "x")
+    n, hkv, d = x.shape
+    if out is None:
+        out = torch.empty((hkv, d), dtype=torch.float32, device=x.device)
+    _need(out, torch.float32, "out", x.device)
+    with torch.cuda.device(x.device):
+        rc = N.lib.fp8pa_kv_channel_scales(_ptr(x), n, hkv, d, fmt, _ptr(out), _stream(stream))
+    N.check(rc, "kv_channel_scales")
+    return out
+
+
+def decode_workspace_bytes(batch, n_q_heads, n_kv_heads, head_dim, head_dim_v, block_size,
+                           max_blocks_per_seq, device=None) -> int:
+    with torch.cuda.device(device if device is not None else torch.cuda.current_device()):
+        nbytes = int(N.lib.fp8pa_decode_workspace_bytes(batch, n_q_heads, n_kv_heads, head_dim,
+                                                        head_dim_v, block_size,
+                                                        max_blocks_per_seq))
+    if nbytes == 0:
+        raise Fp8paError(N.ERR_UNSUPPORTED, "decode_workspace_bytes")
+    return nbytes
+
+
+def paged_decode_attention(q, k_cache, v_cache, k_scale, v_scale, block_tables, seq_lens,
+                           n_kv_heads, sm_scale, fmt=E4M3, scale_mode=SCALE_TOKEN_HEAD,
+                           group_size=64, head_dim_v=None, out=None, out_dtype=None,
+                           workspace=None, stream=None):
+    """q: bf16 [B, Hq, Dk]; caches/scales as written by kv_append_quant
+    (v_cache/v_scale may be the same tensors as k_cache/k_scale for MLA);
+    block_tables: int32 [B, max_blocks]; seq_lens: int32 [B].
+    Returns out [B, Hq, Dv] (bf16 unless out_dtype=torch.float32)."""
+    _need(q, torch.bfloat16, "q")
+    dev = q.device
+    for t, dt, name in ((k_cache, torch.uint8, "k_cache"), (v_cache, torch.uint8, "v_cache"),
+                        (k_scale, torch.float32, "k_scale"), (v_scale, torch.float32, "v_scale"),
+                        (block_tables, torch.int32, "block_tables"),
+                        (seq_lens, torch.int32, "seq_lens")):
+        _need(t, dt, name, dev)
+    B, hq, dk = q.shape
+    dv = dk if head_dim_v is None else head_dim_v
+    nb, _, bs, _ = k_cache.shape
+    max_blocks = block_tables.shape[1]
+    if out is None:
+        out = torch.empty((B, hq, dv), dtype=out_dtype or torch.bfloat16, device=dev)
+    odt = OUT_F32 if out.dtype == torch.float32 else OUT_BF16
+    if out.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("out must be bf16 or float32")
+    _need(out, out.dtype, "out", dev)
+    with torch.cuda.device(dev):
+        need = decode_workspace_bytes(B, hq, n_kv_heads, dk, dv, bs, max_blocks, dev)
+        if workspace is None:
+            workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+        _need(workspace, torch.uint8, "workspace", dev)
+        rc = N.lib.fp8pa_paged_decode_attention(
+            _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
+            _ptr(block_tables), max_blocks, _ptr(seq_lens), B, bs, hq, n_kv_heads, dk, dv, fmt,
+            scale_mode, group_size, float(sm_scale), nb, _ptr(out), odt, _ptr(workspace),
+            workspace.numel(), _stream(stream))
+    N.check(rc, "paged_decode_attention")
+    return out
+
+
+def get_device_error(stream=None, device=None) -> int:
+    """Synchronise the stream, then read and clear the device error word."""
+    flags = ctypes.c_uint32(0)
+    with torch.cuda.device(device if device is not None else torch.cuda.current_device()):
+        N.check(N.lib.fp8pa_get_device_error(_stream(stream), ctypes.byref(flags)),
+                "get_device_error")
+    return int(flags.value)

@@ -1,0 +1,284 @@
+// api.cu -- the extern "C" boundary declared in include/fp8pa.h: argument
+// validation, dispatch to the kernels, tensor-map encoding, the per-device
+// error word and status strings.  No call allocates device memory.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace fp8pa {
+
+// The device error word (one per device that loads the library).
+__device__ uint32_t g_device_error;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+uint32_t* g_err_ptr[kMaxDevices] = {nullptr};
+std::mutex g_mu;
+
+uint32_t* device_error_ptr(int* dev_out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  if (dev_out) *dev_out = dev;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_err_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
+    g_err_ptr[dev] = static_cast<uint32_t*>(p);
+  }
+  return g_err_ptr[dev];
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? FP8PA_OK : FP8PA_ERR_CUDA; }
+
+}  // namespace
+
+bool encode_tensor_map_2d_u8(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows,
+                             uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle swz) {
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  if (!encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+      return false;
+    encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {inner};
+  cuuint32_t box[2] = {box_inner, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims,
+                            strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace fp8pa
+
+using namespace fp8pa;
+
+namespace {
+
+struct DecodePath {
+  DecodeShape shape;
+  int status;
+};
+
+// Validate the decode shapes (pointers are checked by the caller) and
+// choose the kernel family.
+DecodePath decode_path(int batch, int hq, int hkv, int d, int dv, int bs, int max_blocks, int fmt,
+                       int mode, int gs, int num_blocks, int out_dtype) {
+  DecodePath r{};
+  r.status = FP8PA_OK;
+  DecodeShape& s = r.shape;
+  s.batch = batch;
+  s.hq = hq;
+  s.hkv = hkv;
+  s.d = d;
+  s.dv = dv;
+  s.bs = bs;
+  s.max_blocks = max_blocks;
+  s.mla = 0;
+  if ((fmt != FP8PA_E4M3 && fmt != FP8PA_E5M2) ||
+      (mode != FP8PA_SCALE_TOKEN_HEAD && mode != FP8PA_SCALE_CHANNEL_STATIC &&
+       mode != FP8PA_SCALE_TOKEN_GROUP) ||
+      (out_dtype != FP8PA_OUT_BF16 && out_dtype != FP8PA_OUT_F32)) {
+    r.status = FP8PA_ERR_BAD_ENUM;
+    return r;
+  }
+  if (batch < 0 || hq <= 0 || hkv <= 0 || hq % hkv != 0 || bs <= 0 || max_blocks <= 0 ||
+      num_blocks <= 0 || d <= 0 || dv <= 0) {
+    r.status = FP8PA_ERR_BAD_SHAPE;
+    return r;
+  }
+  if (static_cast<long long>(num_blocks) * hkv * bs >= (1ll << 31) ||
+      static_cast<long long>(max_blocks) * bs >= (1ll << 31) ||
+      static_cast<long long>(batch) * max_blocks * bs * hkv >= (1ll << 31)) {
+    r.status = FP8PA_ERR_UNSUPPORTED;
+    return r;
+  }
+  if (d == 576) {
+    s.mla = 1;
+    if (hkv != 1 || dv != 512 || mode != FP8PA_SCALE_TOKEN_GROUP || gs != 64 || bs != 64 ||
+        hq % 64 != 0)
+      r.status = FP8PA_ERR_UNSUPPORTED;
+    return r;
+  }
+  if ((d != 64 && d != 128) || dv != d || (bs != 16 && bs != 32 && bs != 64) || hq / hkv > 8 ||
+      mode == FP8PA_SCALE_TOKEN_GROUP)
+    r.status = FP8PA_ERR_UNSUPPORTED;
+  return r;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fp8pa_version(void) { return (1 << 16) | 0; }
+
+const char* fp8pa_error_string(int code) {
+  switch (code) {
+    case FP8PA_OK: return "ok";
+    case FP8PA_ERR_NULL_POINTER: return "a required pointer is NULL";
+    case FP8PA_ERR_BAD_ENUM: return "unknown fmt, scale_mode or out_dtype";
+    case FP8PA_ERR_BAD_SHAPE: return "inconsistent or non-positive sizes";
+    case FP8PA_ERR_UNSUPPORTED: return "shape or mode combination not supported";
+    case FP8PA_ERR_WORKSPACE: return "workspace missing or too small";
+    case FP8PA_ERR_ALIGNMENT: return "a pointer is not 16-byte aligned";
+    case FP8PA_ERR_CUDA: return "CUDA runtime error";
+    default: return "unknown status";
+  }
+}
+
+int fp8pa_set_decode_workers(int workers) {
+  if (workers < 0) return FP8PA_ERR_BAD_SHAPE;
+  g_decode_workers_override = workers;
+  return FP8PA_OK;
+}
+
+int fp8pa_set_split_events(void* start, void* stop) {
+  if ((start == nullptr) != (stop == nullptr)) return FP8PA_ERR_NULL_POINTER;
+  g_split_ev_start = static_cast<cudaEvent_t>(start);
+  g_split_ev_stop = static_cast<cudaEvent_t>(stop);
+  return FP8PA_OK;
+}
+
+int fp8pa_kv_append_quant(const void* k, const void* v, const int32_t* slot_mapping,
+                          int num_tokens, int n_kv_heads, int head_dim, int fmt, int scale_mode,
+                          int group_size, uint8_t* k_cache, uint8_t* v_cache, float* k_scale,
+                          float* v_scale, int num_blocks, int block_size, void* stream) {
+  if (num_tokens < 0 || n_kv_heads <= 0 || head_dim <= 0 || num_blocks <= 0 || block_size <= 0)
+    return FP8PA_ERR_BAD_SHAPE;
+  if ((fmt != FP8PA_E4M3 && fmt != FP8PA_E5M2) ||
+      (scale_mode != FP8PA_SCALE_TOKEN_HEAD && scale_mode != FP8PA_SCALE_CHANNEL_STATIC &&
+       scale_mode != FP8PA_SCALE_TOKEN_GROUP))
+    return FP8PA_ERR_BAD_ENUM;
+  if (head_dim % 16 != 0 || head_dim > 768) return FP8PA_ERR_UNSUPPORTED;
+  if (scale_mode == FP8PA_SCALE_TOKEN_GROUP &&
+      (!pow2(group_size) || group_size < 16 || group_size > 256 || head_dim % group_size != 0))
+    return FP8PA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(num_blocks) * block_size >= (1ll << 31)) return FP8PA_ERR_UNSUPPORTED;
+  if (num_tokens == 0) return FP8PA_OK;
+  if (!k || !slot_mapping || !k_cache || !k_scale) return FP8PA_ERR_NULL_POINTER;
+  if (v && (!v_cache || !v_scale)) return FP8PA_ERR_NULL_POINTER;
+  if (!aligned16(k) || !aligned16(k_cache) || (v && (!aligned16(v) || !aligned16(v_cache))) ||
+      !aligned16(k_scale) || (v && !aligned16(v_scale)))
+    return FP8PA_ERR_ALIGNMENT;
+  AppendArgs a{};
+  a.src[0] = static_cast<const uint16_t*>(k);
+  a.src[1] = static_cast<const uint16_t*>(v);
+  a.cache[0] = k_cache;
+  a.cache[1] = v_cache;
+  a.scale[0] = k_scale;
+  a.scale[1] = v_scale;
+  a.slot_mapping = slot_mapping;
+  a.num_tokens = num_tokens;
+  a.hkv = n_kv_heads;
+  a.d = head_dim;
+  a.ntens = v ? 2 : 1;
+  a.gs = scale_mode == FP8PA_SCALE_TOKEN_GROUP ? group_size : head_dim;
+  a.num_blocks = num_blocks;
+  a.bs = block_size;
+  a.err = device_error_ptr(nullptr);
+  if (!a.err) return FP8PA_ERR_CUDA;
+  return cuda_status(launch_append(a, fmt, scale_mode, static_cast<cudaStream_t>(stream)));
+}
+
+int fp8pa_kv_channel_scales(const void* x, int num_tokens, int n_kv_heads, int head_dim, int fmt,
+                            float* scale_out, void* stream) {
+  if (num_tokens < 0 || n_kv_heads <= 0 || head_dim <= 0) return FP8PA_ERR_BAD_SHAPE;
+  if (fmt != FP8PA_E4M3 && fmt != FP8PA_E5M2) return FP8PA_ERR_BAD_ENUM;
+  if (head_dim % 16 != 0) return FP8PA_ERR_UNSUPPORTED;
+  if (!scale_out || (num_tokens > 0 && !x)) return FP8PA_ERR_NULL_POINTER;
+  if ((num_tokens > 0 && !aligned16(x)) || !aligned16(scale_out)) return FP8PA_ERR_ALIGNMENT;
+  return cuda_status(launch_channel_scales(static_cast<const uint16_t*>(x), num_tokens,
+                                           n_kv_heads * head_dim, fmt, scale_out,
+                                           static_cast<cudaStream_t>(stream)));
+}
+
+size_t fp8pa_decode_workspace_bytes(int batch, int n_q_heads, int n_kv_heads, int head_dim,
+                                    int head_dim_v, int block_size, int max_blocks_per_seq) {
+  const int mode = head_dim == 576 ? FP8PA_SCALE_TOKEN_GROUP : FP8PA_SCALE_TOKEN_HEAD;
+  DecodePath path = decode_path(batch, n_q_heads, n_kv_heads, head_dim, head_dim_v, block_size,
+                                max_blocks_per_seq, FP8PA_E4M3, mode, 64, 1, FP8PA_OUT_BF16);
+  if (path.status != FP8PA_OK) return 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  path.shape.workers = decode_workers(path.shape, FP8PA_E4M3, mode, dev);
+  return decode_workspace_bytes(path.shape);
+}
+
+int fp8pa_paged_decode_attention(const void* q, const uint8_t* k_cache, const uint8_t* v_cache,
+                                 const float* k_scale, const float* v_scale,
+                                 const int32_t* block_tables, int max_blocks_per_seq,
+                                 const int32_t* seq_lens, int batch, int block_size,
+                                 int n_q_heads, int n_kv_heads, int head_dim, int head_dim_v,
+                                 int fmt, int scale_mode, int group_size, float sm_scale,
+                                 int num_blocks, void* out, int out_dtype, void* workspace,
+                                 size_t workspace_bytes, void* stream) {
+  DecodePath path = decode_path(batch, n_q_heads, n_kv_heads, head_dim, head_dim_v, block_size,
+                                max_blocks_per_seq, fmt, scale_mode, group_size, num_blocks,
+                                out_dtype);
+  if (path.status != FP8PA_OK) return path.status;
+  if (batch == 0) return FP8PA_OK;
+  if (!q || !k_cache || !k_scale || !block_tables || !seq_lens || !out || !workspace)
+    return FP8PA_ERR_NULL_POINTER;
+  if (path.shape.mla) {
+    if (v_cache != k_cache || v_scale != k_scale) return FP8PA_ERR_UNSUPPORTED;
+  } else if (!v_cache || !v_scale) {
+    return FP8PA_ERR_NULL_POINTER;
+  }
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k_scale) ||
+      !aligned16(v_scale) || !aligned16(workspace) || !aligned16(out))
+    return FP8PA_ERR_ALIGNMENT;
+  int dev = 0;
+  uint32_t* err = device_error_ptr(&dev);
+  if (!err) return FP8PA_ERR_CUDA;
+  path.shape.workers = decode_workers(path.shape, fmt, scale_mode, dev);
+  if (workspace_bytes < decode_workspace_bytes(path.shape)) return FP8PA_ERR_WORKSPACE;
+  DecodeArgs a{};
+  a.q = static_cast<const uint16_t*>(q);
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.k_scale = k_scale;
+  a.v_scale = v_scale;
+  a.block_tables = block_tables;
+  a.seq_lens = seq_lens;
+  a.num_blocks = num_blocks;
+  a.fmt = fmt;
+  a.mode = scale_mode;
+  a.gs = group_size;
+  a.out_dtype = out_dtype;
+  a.sm_scale = sm_scale;
+  a.out = out;
+  a.workspace = workspace;
+  a.err = err;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const cudaError_t e = path.shape.mla ? launch_decode_mla(path.shape, a, st)
+                                       : launch_decode_gqa(path.shape, a, st);
+  return cuda_status(e);
+}
+
+int fp8pa_get_device_error(void* stream, uint32_t* flags) {
+  if (!flags) return FP8PA_ERR_NULL_POINTER;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return FP8PA_ERR_CUDA;
+  if (!device_error_ptr(nullptr)) return FP8PA_ERR_CUDA;
+  uint32_t v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_device_error, sizeof v) != cudaSuccess) return FP8PA_ERR_CUDA;
+  const uint32_t zero = 0;
+  if (cudaMemcpyToSymbol(g_device_error, &zero, sizeof zero) != cudaSuccess) return FP8PA_ERR_CUDA;
+  *flags = v;
+  return FP8PA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,719 @@
+// decode_gqa.cu -- split-K paged decode attention for grouped-query heads.
+//
+// Method ("Llama 3 70B FP8 deployment", dpshk.com/news/5605006, sec. 1.2:
+// GQA; "DeepSeek V4 950", 2kiu.com/news/4508674, sec. 2.3: softmax and
+// accumulation in FP32; "DeepSeek-V4.1 512K", hotelren.com/news/5711065,
+// sec. 2.2: blockwise attention with an online softmax, sec. 3.3: paged
+// blocks through a per-request block table):
+//   out[b][h] = sum_t softmax_t(sm_scale * q[b][h] . k^_t) v^_t,
+//   k^ = decode(code) * scale, query head h reading KV head h / G.
+//
+// GB300 design.
+//  * Work is the flat list of units (request b, kv head, page j).  A planner
+//    kernel cuts it into equal contiguous ranges, one per warp of a grid that
+//    fills every SM; a range that crosses a (b, kv head) boundary yields one
+//    partial per piece.  A merge kernel folds the partials of each output
+//    row with the log-sum-exp rule.  Balance is exact for ragged batches and
+//    a 128K-token request spreads over the whole GPU.
+//  * Each warp streams its pages through a private ring of shared-memory
+//    stages filled by the tensor-copy engine (TMA, 2-D boxes of
+//    block_size x head_dim bytes with the 128/64-byte swizzle) plus 1-D bulk
+//    copies of the per-token scales, completion tracked by mbarriers.  One
+//    lane issues; no thread waits on another CTA.  Every wait is bounded.
+//  * The G <= 8 heads sharing a KV head form a tiny dense contraction
+//    (16 tokens x 8 heads x head_dim per tile).  GB300's FP32 pipe cannot
+//    keep up with HBM on it (about 8 FMA per cached byte), so QK^T and PV
+//    run on warp MMA (m16n8k16, f16 in, f32 accumulate) over codes converted
+//    exactly to f16 in registers.  Scales stay outside the contraction: the
+//    per-token K scale multiplies the score, the per-token V scale folds
+//    into P, per-channel K scales fold into q, per-channel V scales multiply
+//    the output.  Power-of-two normalisers keep q and P inside f16's range.
+//  * Softmax runs in FP32 in the log2 domain with warp-shuffle maxima.
+#include <float.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace fp8pa {
+
+namespace {
+
+constexpr int kWarps = 4;  // warps (= workers) per CTA
+
+__device__ __forceinline__ int ld_i32(const int* p) { return *reinterpret_cast<const volatile int*>(p); }
+
+// ---------------------------------------------------------------- planner
+// Workspace header: [0] U = total units, [1] units per worker, [4..] unit
+// prefix per request (B+1 ints), then segment base per (b, kv head)
+// (B*Hkv+1 ints).  Partial buffers follow at 256-byte aligned offsets.
+constexpr int kPlanHeader = 4;
+
+__device__ int block_scan_excl(int v, int* s, int* total) {
+  const int tid = threadIdx.x;
+  s[tid] = v;
+  __syncthreads();
+  for (int off = 1; off < 1024; off <<= 1) {
+    const int t = tid >= off ? s[tid - off] : 0;
+    __syncthreads();
+    s[tid] += t;
+    __syncthreads();
+  }
+  const int incl = s[tid];
+  *total = s[1023];
+  __syncthreads();
+  return incl - v;
+}
+
+__device__ __forceinline__ int clamp_len(int L, int cap) { return L < 0 ? 0 : (L > cap ? cap : L); }
+
+__global__ void __launch_bounds__(1024) plan_kernel(const int32_t* seq_lens, int B, int hkv, int bs,
+                                                    int max_blocks, int workers, int* ws,
+                                                    uint32_t* err) {
+  __shared__ int s[1024];
+  const int tid = threadIdx.x;
+  const int cap = max_blocks * bs;
+  int* uprefix = ws + kPlanHeader;
+  int* segbase = uprefix + B + 1;
+  int carry = 0;
+  for (int base = 0; base < B; base += 1024) {
+    const int b = base + tid;
+    int n = 0;
+    if (b < B) {
+      const int L = seq_lens[b];
+      if (L < 0 || L > cap) raise_error(err, FP8PA_DEVERR_SEQ_LEN);
+      n = (clamp_len(L, cap) + bs - 1) / bs;
+    }
+    int tot;
+    const int ex = block_scan_excl(n, s, &tot);
+    if (b < B) uprefix[b] = (carry + ex) * hkv;
+    carry += tot;
+  }
+  const int U = carry * hkv;
+  const int upw = max(1, (U + workers - 1) / workers);
+  if (tid == 0) {
+    uprefix[B] = U;
+    ws[0] = U;
+    ws[1] = upw;
+  }
+  __syncthreads();
+  carry = 0;
+  const int E = B * hkv;
+  for (int base = 0; base < E; base += 1024) {
+    const int e = base + tid;
+    int segs = 0;
+    if (e < E) {
+      const int b = e / hkv, kvh = e % hkv;
+      const int nb = (uprefix[b + 1] - uprefix[b]) / hkv;
+      if (nb > 0) {
+        const int fu = uprefix[b] + kvh * nb;
+        segs = (fu + nb - 1) / upw - fu / upw + 1;
+      }
+    }
+    int tot;
+    const int ex = block_scan_excl(segs, s, &tot);
+    if (e < E) segbase[e] = carry + ex;
+    carry += tot;
+  }
+  if (tid == 0) segbase[E] = carry;
+}
+
+// ---------------------------------------------------------------- split kernel
+struct GqaParams {
+  const uint16_t* q;
+  const float* k_scale;
+  const float* v_scale;
+  const int32_t* block_tables;
+  const int32_t* seq_lens;
+  const int* plan;
+  float* part_ml;
+  float* part_o;
+  uint32_t* err;
+  int B, hq, hkv, G, max_blocks, num_blocks;
+  float qk_scale_log2;
+};
+
+template <int D, int BS, int NST>
+struct GqaSmem {
+  static constexpr int kPage = BS * D;
+  static constexpr int kPages = kWarps * NST * 2 * kPage;
+  static constexpr int kScales = kWarps * NST * 2 * BS * 4;
+  static constexpr int kPs = kWarps * 256;
+  static constexpr int kBars = kWarps * NST * 8;
+  static constexpr int kOk = kWarps * NST * 4;
+  static constexpr int kBytes = kPages + kScales + kPs + kBars + kOk + 1024;
+};
+
+// Byte offset of 16-byte chunk `ch` of row `r` in a TMA box written with the
+// 128-byte (128-byte rows) or 64-byte (64-byte rows) swizzle.
+template <int D>
+__device__ __forceinline__ uint32_t swz(int r, int ch) {
+  if constexpr (D == 128) {
+    return static_cast<uint32_t>(r * 128 + ((ch ^ (r & 7)) << 4));
+  } else {
+    return static_cast<uint32_t>(r * 64 + ((ch ^ ((r >> 1) & 3)) << 4));
+  }
+}
+
+struct Cursor {
+  int b, kvh, j, nb;
+};
+
+template <int D, int BS, int FMT, int MODE, int NST>
+__global__ void __launch_bounds__(kWarps * 32)
+    gqa_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+                     const GqaParams p) {
+  using SM = GqaSmem<D, BS, NST>;
+  constexpr int PAGE = SM::kPage;
+  constexpr int TILES = BS / 16;
+  constexpr int KW = D / 16;   // K words per row per thread = k-steps
+  constexpr int KCH = D / 64;  // 16-byte K chunks per row per thread
+  constexpr int VW = D / 32;   // V words per token per thread
+  constexpr int MT = D / 16;   // dv tiles of 16
+  constexpr bool TOKSC = (MODE == FP8PA_SCALE_TOKEN_HEAD);
+  constexpr uint32_t TX = 2 * PAGE + (TOKSC ? 2 * BS * 4 : 0);
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, c = lane & 3;
+  uint8_t* pages = smem + warp * (NST * 2 * PAGE);
+  float* scl = reinterpret_cast<float*>(smem + SM::kPages) + warp * (NST * 2 * BS);
+  uint16_t* ps = reinterpret_cast<uint16_t*>(smem + SM::kPages + SM::kScales) + warp * 128;
+  uint64_t* bars =
+      reinterpret_cast<uint64_t*>(smem + SM::kPages + SM::kScales + SM::kPs) + warp * NST;
+  int* okf =
+      reinterpret_cast<int*>(smem + SM::kPages + SM::kScales + SM::kPs + SM::kBars) + warp * NST;
+
+  const int* uprefix = p.plan + kPlanHeader;
+  const int* segbase = uprefix + p.B + 1;
+  const int U = ld_i32(p.plan), upw = ld_i32(p.plan + 1);
+  const long wid = static_cast<long>(blockIdx.x) * kWarps + warp;
+  const long u0 = wid * upw;
+  if (u0 >= U) return;
+  const int n_units = static_cast<int>(min(static_cast<long>(upw), U - u0));
+
+  if (lane == 0) {
+    for (int s = 0; s < NST; ++s) mbar_init(&bars[s], 1);
+    fence_barrier_init();
+    prefetch_tensormap(&tmk);
+    prefetch_tensormap(&tmv);
+  }
+  __syncwarp();
+
+  // ---- unit cursor: (request, kv head, page) of a flat unit index
+  auto locate = [&](long u) {
+    int lo = 0, hi = p.B;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (uprefix[mid] <= u) lo = mid; else hi = mid;
+    }
+    Cursor cu;
+    cu.b = lo;
+    cu.nb = (uprefix[lo + 1] - uprefix[lo]) / p.hkv;
+    const int local = static_cast<int>(u - uprefix[lo]);
+    cu.kvh = local / cu.nb;
+    cu.j = local % cu.nb;
+    return cu;
+  };
+  auto advance = [&](Cursor& cu) {
+    if (++cu.j < cu.nb) return;
+    cu.j = 0;
+    if (++cu.kvh < p.hkv) return;
+    cu.kvh = 0;
+    do {
+      ++cu.b;
+    } while (cu.b < p.B && uprefix[cu.b + 1] == uprefix[cu.b]);
+    if (cu.b < p.B) cu.nb = (uprefix[cu.b + 1] - uprefix[cu.b]) / p.hkv;
+  };
+  auto block_of = [&](const Cursor& cu) {
+    return __ldg(p.block_tables + static_cast<long>(cu.b) * p.max_blocks + cu.j);
+  };
+  // Issue the copies of one page into stage s (lane 0 only acts).
+  auto issue = [&](const Cursor& cu, int blk, int s) {
+    if (lane == 0) {
+      const bool ok = blk >= 0 && blk < p.num_blocks;
+      okf[s] = ok ? 1 : 0;
+      if (ok) {
+        const int row = (blk * p.hkv + cu.kvh) * BS;
+        mbar_arrive_expect_tx(&bars[s], TX);
+        tma_load_2d(pages + s * 2 * PAGE, &tmk, 0, row, &bars[s]);
+        tma_load_2d(pages + s * 2 * PAGE + PAGE, &tmv, 0, row, &bars[s]);
+        if constexpr (TOKSC) {
+          bulk_load(scl + s * 2 * BS, p.k_scale + row, BS * 4, &bars[s]);
+          bulk_load(scl + s * 2 * BS + BS, p.v_scale + row, BS * 4, &bars[s]);
+        }
+      } else {
+        raise_error(p.err, FP8PA_DEVERR_BLOCK_RANGE);
+        mbar_arrive(&bars[s]);
+      }
+    }
+  };
+
+  Cursor cc = locate(u0);
+  Cursor pc = cc;
+  int ip = 0;  // units issued
+  int pblk = block_of(pc);
+  {
+    const int npro = min(NST, n_units);
+    for (; ip < npro; ++ip) {
+      issue(pc, pblk, ip);
+      advance(pc);
+      if (ip + 1 < n_units) pblk = block_of(pc);
+    }
+  }
+
+  // ---- per-segment state
+  uint32_t qb[KW][2];
+  float O[MT][4];
+  float m0 = -FLT_MAX, m1 = -FLT_MAX, l0 = 0.f, l1 = 0.f, zs = 0.f;
+  int erun = -127, Lb = 0;
+  const float NEG_INF = __int_as_float(0xff800000);
+  bool abandoned = false;
+  int i = 0;
+
+  for (; i < n_units; ++i) {
+    const int s = i % NST;
+    const uint32_t par = static_cast<uint32_t>((i / NST) & 1);
+    if (i == 0 || cc.j == 0) {
+      // ---- new segment: load q for the G heads of (b, kv head)
+      Lb = clamp_len(__ldg(p.seq_lens + cc.b), p.max_blocks * BS);
+      const int h = cc.kvh * p.G + g;
+      float qv[D / 4];
+      if (g < p.G) {
+        const uint4* src = reinterpret_cast<const uint4*>(
+            p.q + (static_cast<long>(cc.b) * p.hq + h) * D + c * (D / 4));
+#pragma unroll
+        for (int x = 0; x < D / 32; ++x) {
+          const uint4 u = __ldg(src + x);
+          const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            qv[8 * x + 2 * e] = __uint_as_float(w[e] << 16);
+            qv[8 * x + 2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
+          }
+        }
+        if constexpr (!TOKSC) {
+          const float* ksc = p.k_scale + cc.kvh * D + c * (D / 4);
+#pragma unroll
+          for (int e = 0; e < D / 4; ++e) qv[e] *= __ldg(ksc + e);
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < D / 4; ++e) qv[e] = 0.f;
+      }
+      float amax = 0.f;
+#pragma unroll
+      for (int e = 0; e < D / 4; ++e) amax = fmaxf(amax, fabsf(qv[e]));
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+      const int eq = amax > 0.f ? exp_above(amax) : 0;
+      const float fq = exp2i(14 - eq);
+#pragma unroll
+      for (int j = 0; j < KW; ++j) {
+        qb[j][0] = pack_half2(qv[4 * j] * fq, qv[4 * j + 1] * fq);
+        qb[j][1] = pack_half2(qv[4 * j + 2] * fq, qv[4 * j + 3] * fq);
+      }
+      zs = p.qk_scale_log2 * exp2i(eq - 14);
+      m0 = m1 = NEG_INF;
+      l0 = l1 = 0.f;
+      erun = TOKSC ? -127 : 1;
+#pragma unroll
+      for (int t = 0; t < MT; ++t) O[t][0] = O[t][1] = O[t][2] = O[t][3] = 0.f;
+    }
+
+    const bool landed = mbar_wait_bounded(&bars[s], par, kWaitLimitCycles);
+    if (!__all_sync(0xffffffffu, landed)) {
+      if (lane == 0) raise_error(p.err, FP8PA_DEVERR_TIMEOUT);
+      abandoned = true;
+      break;
+    }
+    const int valid = okf[s] ? min(BS, Lb - cc.j * BS) : 0;
+    const uint32_t kbase = smem_u32(pages + s * 2 * PAGE);
+    const uint32_t vbase = kbase + PAGE;
+    const float* sks = scl + s * 2 * BS;
+    const float* svs = sks + BS;
+
+#pragma unroll
+    for (int tt = 0; tt < TILES; ++tt) {
+      const int r0 = tt * 16;
+      if (r0 >= valid) break;
+      const int tv = valid - r0;
+      // ---- S^T = K . Q^T : rows = tokens (g, g+8), cols = heads (2c, 2c+1)
+      uint32_t kw[2][KW];
+#pragma unroll
+      for (int rr = 0; rr < 2; ++rr) {
+        const int R = r0 + g + 8 * rr;
+#pragma unroll
+        for (int qq = 0; qq < KCH; ++qq) {
+          const uint4 x = lds128(kbase + swz<D>(R, c * KCH + qq));
+          kw[rr][4 * qq] = x.x;
+          kw[rr][4 * qq + 1] = x.y;
+          kw[rr][4 * qq + 2] = x.z;
+          kw[rr][4 * qq + 3] = x.w;
+        }
+      }
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int j = 0; j < KW; ++j) {
+        mma_16816(acc, fp8x2_to_f16x2<FMT>(kw[0][j]), fp8x2_to_f16x2<FMT>(kw[1][j]),
+                  fp8x2_to_f16x2<FMT>(kw[0][j] >> 16), fp8x2_to_f16x2<FMT>(kw[1][j] >> 16),
+                  qb[j][0], qb[j][1]);
+      }
+      const bool v0 = g < tv, v1 = g + 8 < tv;
+      float sk0 = 1.f, sk1 = 1.f;
+      if constexpr (TOKSC) {
+        sk0 = sks[r0 + g];
+        sk1 = sks[r0 + g + 8];
+      }
+      const float z00 = v0 ? acc[0] * (zs * sk0) : NEG_INF;
+      const float z01 = v0 ? acc[1] * (zs * sk0) : NEG_INF;
+      const float z10 = v1 ? acc[2] * (zs * sk1) : NEG_INF;
+      const float z11 = v1 ? acc[3] * (zs * sk1) : NEG_INF;
+      float mx0 = fmaxf(z00, z10), mx1 = fmaxf(z01, z11);
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+      }
+      const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+      const bool live0 = mn0 != NEG_INF, live1 = mn1 != NEG_INF;
+      const float al0 = live0 ? ex2(m0 - mn0) : 1.f;
+      const float al1 = live1 ? ex2(m1 - mn1) : 1.f;
+      const float p00 = live0 ? ex2(z00 - mn0) : 0.f;
+      const float p10 = live0 ? ex2(z10 - mn0) : 0.f;
+      const float p01 = live1 ? ex2(z01 - mn1) : 0.f;
+      const float p11 = live1 ? ex2(z11 - mn1) : 0.f;
+      l0 = l0 * al0 + p00 + p10;
+      l1 = l1 * al1 + p01 + p11;
+      m0 = mn0;
+      m1 = mn1;
+      // ---- fold the V scale into P, normalised by a running power of two
+      float rs = 1.f, q00, q01, q10, q11;
+      if constexpr (TOKSC) {
+        const float sv0 = v0 ? svs[r0 + g] : 0.f;
+        const float sv1 = v1 ? svs[r0 + g + 8] : 0.f;
+        float svm = fmaxf(sv0, sv1);
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) svm = fmaxf(svm, __shfl_xor_sync(0xffffffffu, svm, o));
+        const int et = svm > 0.f ? exp_above(svm) : erun;
+        if (et > erun) {
+          rs = exp2i(erun - et);
+          erun = et;
+        }
+        const float pf = exp2i(15 - erun);
+        q00 = p00 * sv0 * pf;
+        q01 = p01 * sv0 * pf;
+        q10 = p10 * sv1 * pf;
+        q11 = p11 * sv1 * pf;
+      } else {
+        q00 = p00 * 16384.f;
+        q01 = p01 * 16384.f;
+        q10 = p10 * 16384.f;
+        q11 = p11 * 16384.f;
+      }
+      const float f0 = al0 * rs, f1 = al1 * rs;
+#pragma unroll
+      for (int t = 0; t < MT; ++t) {
+        O[t][0] *= f0;
+        O[t][2] *= f0;
+        O[t][1] *= f1;
+        O[t][3] *= f1;
+      }
+      // ---- P^T through shared memory into the B layout of the PV MMA.
+      // Position 4c'+u of a head row holds token 4c' + ((u + c') & 3).
+      __syncwarp();
+      {
+        const int pos0 = 4 * (g >> 2) + (((g & 3) - (g >> 2)) & 3);
+        const int t1 = g + 8;
+        const int pos1 = 4 * (t1 >> 2) + (((t1 & 3) - (t1 >> 2)) & 3);
+        ps[(2 * c) * 16 + pos0] = __half_as_ushort(__float2half_rn(q00));
+        ps[(2 * c + 1) * 16 + pos0] = __half_as_ushort(__float2half_rn(q01));
+        ps[(2 * c) * 16 + pos1] = __half_as_ushort(__float2half_rn(q10));
+        ps[(2 * c + 1) * 16 + pos1] = __half_as_ushort(__float2half_rn(q11));
+      }
+      __syncwarp();
+      const uint2 pb = lds64(smem_u32(ps + g * 16 + 4 * c));
+      // ---- O^T += V^T . P^T : rows = dv, cols = heads
+      uint32_t vw[4][VW];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int tau = 4 * c + ((u + c) & 3);
+        const int R = r0 + tau;
+        if constexpr (D == 128) {
+          const uint4 x = lds128(vbase + swz<D>(R, g));
+          vw[u][0] = x.x;
+          vw[u][1] = x.y;
+          vw[u][2] = x.z;
+          vw[u][3] = x.w;
+        } else {
+          const uint2 x = lds64(vbase + swz<D>(R, g >> 1) + 8 * (g & 1));
+          vw[u][0] = x.x;
+          vw[u][1] = x.y;
+        }
+        if (tau >= tv) {
+#pragma unroll
+          for (int e = 0; e < VW; ++e) vw[u][e] = 0u;
+        }
+      }
+#pragma unroll
+      for (int t = 0; t < MT; ++t) {
+        const uint32_t sel = (t & 1) ? 0x7362u : 0x5140u;
+        const uint32_t x01 = prmt(vw[0][t >> 1], vw[1][t >> 1], sel);
+        const uint32_t x23 = prmt(vw[2][t >> 1], vw[3][t >> 1], sel);
+        mma_16816(O[t], fp8x2_to_f16x2<FMT>(x01), fp8x2_to_f16x2<FMT>(x01 >> 16),
+                  fp8x2_to_f16x2<FMT>(x23), fp8x2_to_f16x2<FMT>(x23 >> 16), pb.x, pb.y);
+      }
+    }
+    __syncwarp();
+
+    // ---- refill this stage with the next page of the range
+    if (ip < n_units) {
+      issue(pc, pblk, ip % NST);
+      ++ip;
+      advance(pc);
+      if (ip < n_units) pblk = block_of(pc);
+    }
+
+    // ---- segment end: write the partial (m, l, o) of this warp's piece
+    if (i == n_units - 1 || cc.j == cc.nb - 1) {
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        l0 += __shfl_xor_sync(0xffffffffu, l0, o);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, o);
+      }
+      const int fu = uprefix[cc.b] + cc.kvh * cc.nb;
+      const long seg = segbase[cc.b * p.hkv + cc.kvh] + (wid - fu / upw);
+      const float fin = TOKSC ? exp2i(erun - 15) : (1.0f / 16384.f);
+#pragma unroll
+      for (int hsel = 0; hsel < 2; ++hsel) {
+        const int hh = 2 * c + hsel;
+        if (hh >= p.G) continue;
+        float vals[D / 8];
+#pragma unroll
+        for (int t = 0; t < MT; ++t) {
+          vals[2 * t] = O[t][hsel] * fin;
+          vals[2 * t + 1] = O[t][2 + hsel] * fin;
+        }
+        const int dv0 = (D / 8) * g;
+        if constexpr (!TOKSC) {
+          const float* vsc = p.v_scale + cc.kvh * D + dv0;
+#pragma unroll
+          for (int e = 0; e < D / 8; ++e) vals[e] *= __ldg(vsc + e);
+        }
+        float4* po = reinterpret_cast<float4*>(p.part_o + (seg * p.G + hh) * D + dv0);
+#pragma unroll
+        for (int e = 0; e < D / 32; ++e)
+          po[e] = make_float4(vals[4 * e], vals[4 * e + 1], vals[4 * e + 2], vals[4 * e + 3]);
+        if (g == 0) {
+          p.part_ml[(seg * p.G + hh) * 2] = hsel ? m1 : m0;
+          p.part_ml[(seg * p.G + hh) * 2 + 1] = hsel ? l1 : l0;
+        }
+      }
+    }
+    advance(cc);
+  }
+
+  if (abandoned) {
+    // Drain the copies still in flight into this warp's stages before the
+    // CTA may exit (bounded again).
+    for (int k = i; k < ip; ++k)
+      (void)mbar_wait_bounded(&bars[k % NST], static_cast<uint32_t>((k / NST) & 1),
+                              kWaitLimitCycles);
+  }
+}
+
+// ---------------------------------------------------------------- merge
+struct MergeParams {
+  const int* plan;
+  const float* part_ml;
+  const float* part_o;
+  void* out;
+  int B, hq, hkv, G, dv, out_f32;
+};
+
+template <int DV>
+__global__ void __launch_bounds__(256) merge_kernel(const MergeParams p) {
+  constexpr int PER = DV / 32;
+  const int gw = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (gw >= p.B * p.hq) return;
+  const int b = gw / p.hq, h = gw % p.hq;
+  const int kvh = h / p.G, hh = h % p.G;
+  const int* segbase = p.plan + kPlanHeader + p.B + 1;
+  const int sb = segbase[b * p.hkv + kvh], se = segbase[b * p.hkv + kvh + 1];
+  const float NEG_INF = __int_as_float(0xff800000);
+  float M = NEG_INF;
+  for (int s = sb + lane; s < se; s += 32) M = fmaxf(M, p.part_ml[(static_cast<long>(s) * p.G + hh) * 2]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  float acc[PER];
+#pragma unroll
+  for (int e = 0; e < PER; ++e) acc[e] = 0.f;
+  float L = 0.f;
+  if (M != NEG_INF) {
+    for (int s = sb; s < se; ++s) {
+      const long r = static_cast<long>(s) * p.G + hh;
+      const float w = ex2(p.part_ml[r * 2] - M);
+      L += w * p.part_ml[r * 2 + 1];
+      const float* po = p.part_o + r * DV + lane * PER;
+#pragma unroll
+      for (int e = 0; e < PER; e += 2) {
+        const float2 v = *reinterpret_cast<const float2*>(po + e);
+        acc[e] += w * v.x;
+        acc[e + 1] += w * v.y;
+      }
+    }
+  }
+  const float inv = L > 0.f ? 1.0f / L : 0.f;
+  const long ob = (static_cast<long>(b) * p.hq + h) * DV + lane * PER;
+  if (p.out_f32) {
+    float* o = reinterpret_cast<float*>(p.out) + ob;
+#pragma unroll
+    for (int e = 0; e < PER; ++e) o[e] = acc[e] * inv;
+  } else {
+    __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(p.out) + ob;
+#pragma unroll
+    for (int e = 0; e < PER; e += 2)
+      *reinterpret_cast<__nv_bfloat162*>(o + e) =
+          __floats2bfloat162_rn(acc[e] * inv, acc[e + 1] * inv);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+template <int D, int BS>
+constexpr int stages_for() {
+  constexpr int stage = 2 * BS * D;
+  constexpr int n = 16384 / stage;
+  return n < 2 ? 2 : (n > 8 ? 8 : n);
+}
+
+using SplitFn = void (*)(const CUtensorMap, const CUtensorMap, const GqaParams);
+
+struct SplitKernel {
+  SplitFn fn;
+  int smem;
+};
+
+template <int D, int BS, int FMT, int MODE>
+SplitKernel pick4() {
+  constexpr int NST = stages_for<D, BS>();
+  return {gqa_split_kernel<D, BS, FMT, MODE, NST>, GqaSmem<D, BS, NST>::kBytes};
+}
+
+template <int D, int BS, int FMT>
+SplitKernel pick3(int mode) {
+  return mode == FP8PA_SCALE_TOKEN_HEAD ? pick4<D, BS, FMT, FP8PA_SCALE_TOKEN_HEAD>()
+                                        : pick4<D, BS, FMT, FP8PA_SCALE_CHANNEL_STATIC>();
+}
+
+template <int D, int BS>
+SplitKernel pick2(int fmt, int mode) {
+  return fmt == FP8PA_E4M3 ? pick3<D, BS, FP8PA_E4M3>(mode) : pick3<D, BS, FP8PA_E5M2>(mode);
+}
+
+template <int D>
+SplitKernel pick1(int bs, int fmt, int mode) {
+  switch (bs) {
+    case 16: return pick2<D, 16>(fmt, mode);
+    case 32: return pick2<D, 32>(fmt, mode);
+    default: return pick2<D, 64>(fmt, mode);
+  }
+}
+
+SplitKernel pick(int d, int bs, int fmt, int mode) {
+  return d == 128 ? pick1<128>(bs, fmt, mode) : pick1<64>(bs, fmt, mode);
+}
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+}  // namespace
+
+int g_decode_workers_override = 0;
+cudaEvent_t g_split_ev_start = nullptr, g_split_ev_stop = nullptr;
+
+// Split workers for the GQA kernel: one per resident warp slot.
+int decode_workers(const DecodeShape& s, int fmt, int mode, int device) {
+  if (g_decode_workers_override > 0) return g_decode_workers_override;
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess || sms <= 0)
+    sms = 1;
+  if (s.mla) return sms;  // the shared-latent kernel decides per CTA
+  const SplitKernel k = pick(s.d, s.bs, fmt, mode);
+  cudaFuncSetAttribute(reinterpret_cast<const void*>(k.fn),
+                       cudaFuncAttributeMaxDynamicSharedMemorySize, k.smem);
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, reinterpret_cast<const void*>(k.fn),
+                                                    kWarps * 32, k.smem) != cudaSuccess ||
+      per_sm <= 0)
+    per_sm = 1;
+  return sms * per_sm * kWarps;
+}
+
+size_t decode_workspace_bytes(const DecodeShape& s) {
+  const int G = s.hq / s.hkv;
+  const size_t plan = align256(sizeof(int) * (kPlanHeader + (s.batch + 1) +
+                                               static_cast<size_t>(s.batch) * s.hkv + 1));
+  const size_t segs = static_cast<size_t>(s.workers) + static_cast<size_t>(s.batch) * s.hkv;
+  const size_t ml = align256(segs * G * 2 * sizeof(float));
+  const size_t o = align256(segs * G * static_cast<size_t>(s.dv) * sizeof(float));
+  return plan + ml + o;
+}
+
+cudaError_t launch_decode_gqa(const DecodeShape& s, const DecodeArgs& a, cudaStream_t stream) {
+  const int G = s.hq / s.hkv;
+  const SplitKernel k = pick(s.d, s.bs, a.fmt, a.mode);
+  cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(k.fn),
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, k.smem);
+  if (e != cudaSuccess) return e;
+
+  CUtensorMap tmk, tmv;
+  const uint64_t rows = static_cast<uint64_t>(a.num_blocks) * s.hkv * s.bs;
+  const CUtensorMapSwizzle swz =
+      s.d == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  if (!encode_tensor_map_2d_u8(&tmk, a.k_cache, s.d, rows, s.d, s.bs, swz) ||
+      !encode_tensor_map_2d_u8(&tmv, a.v_cache, s.d, rows, s.d, s.bs, swz))
+    return cudaErrorInvalidValue;
+
+  char* ws = static_cast<char*>(a.workspace);
+  int* plan = reinterpret_cast<int*>(ws);
+  const size_t plan_bytes = align256(sizeof(int) * (kPlanHeader + (s.batch + 1) +
+                                                     static_cast<size_t>(s.batch) * s.hkv + 1));
+  const size_t segs = static_cast<size_t>(s.workers) + static_cast<size_t>(s.batch) * s.hkv;
+  float* part_ml = reinterpret_cast<float*>(ws + plan_bytes);
+  float* part_o = reinterpret_cast<float*>(ws + plan_bytes + align256(segs * G * 2 * sizeof(float)));
+
+  plan_kernel<<<1, 1024, 0, stream>>>(a.seq_lens, s.batch, s.hkv, s.bs, s.max_blocks, s.workers,
+                                      plan, a.err);
+  GqaParams p;
+  p.q = a.q;
+  p.k_scale = a.k_scale;
+  p.v_scale = a.v_scale;
+  p.block_tables = a.block_tables;
+  p.seq_lens = a.seq_lens;
+  p.plan = plan;
+  p.part_ml = part_ml;
+  p.part_o = part_o;
+  p.err = a.err;
+  p.B = s.batch;
+  p.hq = s.hq;
+  p.hkv = s.hkv;
+  p.G = G;
+  p.max_blocks = s.max_blocks;
+  p.num_blocks = a.num_blocks;
+  p.qk_scale_log2 = a.sm_scale * 1.4426950408889634f;
+  const int ctas = (s.workers + kWarps - 1) / kWarps;
+  if (g_split_ev_start) cudaEventRecord(g_split_ev_start, stream);
+  k.fn<<<ctas, kWarps * 32, k.smem, stream>>>(tmk, tmv, p);
+  if (g_split_ev_stop) cudaEventRecord(g_split_ev_stop, stream);
+
+  MergeParams mp{plan, part_ml, part_o, a.out, s.batch, s.hq, s.hkv, G, s.dv, a.out_dtype};
+  const int mblocks = (s.batch * s.hq + 7) / 8;
+  if (s.dv == 128)
+    merge_kernel<128><<<mblocks, 256, 0, stream>>>(mp);
+  else
+    merge_kernel<64><<<mblocks, 256, 0, stream>>>(mp);
+  return cudaGetLastError();
+}
+
+}  // namespace fp8pa

@@ -1,0 +1,60 @@
+// internal.h -- host-side declarations shared by the library's translation
+// units (not part of the public ABI; the ABI is include/fp8pa.h).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace fp8pa {
+
+struct AppendArgs {
+  const uint16_t* src[2];   // k, v rows (bf16 bits), [num_tokens][hkv][d]
+  uint8_t* cache[2];        // k, v codes
+  float* scale[2];          // k, v scales (written, or read in CHANNEL_STATIC)
+  const int32_t* slot_mapping;
+  int num_tokens, hkv, d, ntens, gs, num_blocks, bs;
+  uint32_t* err;
+};
+
+cudaError_t launch_append(const AppendArgs& a, int fmt, int mode, cudaStream_t stream);
+cudaError_t launch_channel_scales(const uint16_t* x, int num_tokens, int hd, int fmt, float* out,
+                                  cudaStream_t stream);
+
+// Workspace layout of the split-K decode, shared by planner, split and merge.
+struct DecodeShape {
+  int batch, hq, hkv, d, dv, bs, max_blocks;
+  int workers;        // split workers (warps or CTAs, per kernel family)
+  int mla;            // 1 for the shared-latent kernel
+};
+
+size_t decode_workspace_bytes(const DecodeShape& s);
+
+struct DecodeArgs {
+  const uint16_t* q;
+  const uint8_t* k_cache;
+  const uint8_t* v_cache;
+  const float* k_scale;
+  const float* v_scale;
+  const int32_t* block_tables;
+  const int32_t* seq_lens;
+  int num_blocks, fmt, mode, gs, out_dtype;
+  float sm_scale;
+  void* out;
+  void* workspace;
+  uint32_t* err;
+};
+
+int decode_workers(const DecodeShape& s, int fmt, int mode, int device);
+cudaError_t launch_decode_gqa(const DecodeShape& s, const DecodeArgs& a, cudaStream_t stream);
+cudaError_t launch_decode_mla(const DecodeShape& s, const DecodeArgs& a, cudaStream_t stream);
+
+// Tensor-map encoder from the driver (resolved once through the runtime).
+bool encode_tensor_map_2d_u8(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows,
+                             uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle swz);
+
+extern int g_decode_workers_override;
+extern cudaEvent_t g_split_ev_start, g_split_ev_stop;
+
+}  // namespace fp8pa

@@ -1,0 +1,213 @@
+/*
+ * fp8pa.h -- C ABI of the GB300 (sm_103a) library for decode-step attention
+ * over an FP8-quantised, paged KV cache.
+ *
+ * The method (as the source pages state it):
+ *  - KV rows are stored as FP8 codes with an fp32 scale.  E4M3 has 4 exponent
+ *    and 3 mantissa bits (range +-448, smallest non-zero 2^-9); E5M2 has 5 and
+ *    2 (range +-57344) and is the format recommended for the KV cache for its
+ *    range ("DeepSeek V4 950: whole-network FP8 dataflow",
+ *    2kiu.com/news/4508674, sec. 2.1; "FP8混合精度推理全链路部署实战",
+ *    ybb.press/ai-applications/14145.html, sec. 1.1 and sec. 2.2).
+ *  - The scale of a group of values is absmax / 448 (absmax / 57344 for E5M2),
+ *    clamped below at 1e-12, and the code is x / scale rounded to FP8
+ *    ("Llama 3 70B FP8 deployment", dpshk.com/news/5605006, sec. 3.1).
+ *  - The cache is paged: fixed-size blocks from one pool, one block table per
+ *    request ("DeepSeek-V4.1 512K long-context TTFT", hotelren.com/news/5711065,
+ *    sec. 3.3).
+ *  - Attention is grouped-query (64 query heads share 8 KV heads for
+ *    Llama-3-70B; dpshk.com/news/5605006 sec. 1.2) with the softmax in FP32
+ *    (2kiu.com/news/4508674 sec. 2.3) computed as an online softmax
+ *    (hotelren.com/news/5711065 sec. 2.2).
+ *  - The MLA variant caches one compressed latent per token with one scale
+ *    per latent group (2kiu.com/news/4508674 sec. 2.2).
+ *
+ * Conventions common to every call:
+ *  - All data pointers are DEVICE pointers owned and allocated by the caller;
+ *    the library allocates no memory (the decode's scratch is the caller's
+ *    `workspace`).  bf16 arguments are raw bf16 bit patterns.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *    default stream).  The library never synchronises inside a call.
+ *  - Return value: FP8PA_OK (0) or a negative FP8PA_ERR_* code.  When a call
+ *    returns an error nothing was launched.
+ *  - Bad indices found on the device (a slot or block id outside the pool, a
+ *    sequence longer than its block table) never trap: the element is skipped
+ *    and a bit is set in a per-device error word, read and cleared with
+ *    fp8pa_get_device_error().
+ *
+ * Layouts (row-major, innermost last):
+ *   codes            u8  [num_blocks][n_kv_heads][block_size][head_dim]
+ *   TOKEN_HEAD scale f32 [num_blocks][n_kv_heads][block_size]
+ *   TOKEN_GROUP scale f32 [num_blocks][n_kv_heads][block_size][head_dim/group_size]
+ *   CHANNEL_STATIC scale f32 [n_kv_heads][head_dim]   (caller-given, read only)
+ *   slot s           -> block s / block_size, offset s % block_size
+ *   block_tables     i32 [batch][max_blocks_per_seq]; token t of request b
+ *                        lives in block block_tables[b][t / block_size]
+ *   q                bf16 [batch][n_q_heads][head_dim]
+ *   out              bf16 or f32 [batch][n_q_heads][head_dim_v]
+ * Query head h reads KV head h / (n_q_heads / n_kv_heads).
+ */
+#ifndef FP8PA_H
+#define FP8PA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes. */
+#define FP8PA_OK 0
+#define FP8PA_ERR_NULL_POINTER (-1)
+#define FP8PA_ERR_BAD_ENUM (-2)
+#define FP8PA_ERR_BAD_SHAPE (-3)
+#define FP8PA_ERR_UNSUPPORTED (-4)
+#define FP8PA_ERR_WORKSPACE (-5)
+#define FP8PA_ERR_ALIGNMENT (-6)
+#define FP8PA_ERR_CUDA (-7)
+
+/* Bits of the device error word. */
+#define FP8PA_DEVERR_SLOT_RANGE 1u   /* append: slot beyond num_blocks*block_size (row skipped) */
+#define FP8PA_DEVERR_BLOCK_RANGE 2u  /* decode: block id outside [0, num_blocks) (page masked) */
+#define FP8PA_DEVERR_SEQ_LEN 4u      /* decode: seq_len < 0 or > max_blocks_per_seq*block_size (clamped) */
+#define FP8PA_DEVERR_TIMEOUT 8u      /* decode: a bounded wait on an async copy ran out (work abandoned) */
+
+/* FP8 formats. */
+#define FP8PA_E4M3 0
+#define FP8PA_E5M2 1
+
+/* Scale granularities. */
+#define FP8PA_SCALE_TOKEN_HEAD 0     /* dynamic: one f32 per (token, kv head), written by append */
+#define FP8PA_SCALE_CHANNEL_STATIC 1 /* static: caller-given f32 per (kv head, dim), read only   */
+#define FP8PA_SCALE_TOKEN_GROUP 2    /* dynamic: one f32 per (token, kv head, group of dims)     */
+
+/* Output element types of the decode. */
+#define FP8PA_OUT_BF16 0
+#define FP8PA_OUT_F32 1
+
+/*
+ * Append new tokens' K/V rows to the cache.
+ * Defined by: absmax scale and FP8 cast, "Llama 3 70B FP8 deployment"
+ * (dpshk.com/news/5605006) sec. 3.1; per-latent-group scales,
+ * "DeepSeek V4 950" (2kiu.com/news/4508674) sec. 2.2; paged blocks,
+ * "DeepSeek-V4.1 512K" (hotelren.com/news/5711065) sec. 3.3.
+ *
+ * k, v          bf16 [num_tokens][n_kv_heads][head_dim]; v may be NULL (then
+ *               v_cache/v_scale are ignored: the single-latent MLA cache).
+ * slot_mapping  i32 [num_tokens]; a negative slot skips that token.  Two
+ *               tokens with the same slot in one call race (undefined).
+ * fmt           FP8PA_E4M3 or FP8PA_E5M2.
+ * scale_mode    TOKEN_HEAD: s = max(absmax(row)/FMAX, 1e-12), written to
+ *               k_scale/v_scale.  TOKEN_GROUP: the same per group of
+ *               group_size dims.  CHANNEL_STATIC: s = k_scale[h][d] given
+ *               by the caller, not written.
+ * code          = fp8_rne_satfinite(x / s), IEEE fp32 division; codes are
+ *               bit-exact with the definition above.
+ * Requirements  head_dim % 16 == 0, head_dim <= 768; group_size in
+ *               {16,32,64,128,256} dividing head_dim; block_size > 0;
+ *               16-byte aligned k, v, caches and scales.
+ * Errors        negative code, nothing launched.  A slot past the pool is
+ *               skipped and sets FP8PA_DEVERR_SLOT_RANGE.
+ */
+int fp8pa_kv_append_quant(const void* k, const void* v, const int32_t* slot_mapping,
+                          int num_tokens, int n_kv_heads, int head_dim, int fmt, int scale_mode,
+                          int group_size, uint8_t* k_cache, uint8_t* v_cache, float* k_scale,
+                          float* v_scale, int num_blocks, int block_size, void* stream);
+
+/*
+ * Static per-channel scales for CHANNEL_STATIC mode: for every (kv head, dim)
+ * s = max(absmax over the num_tokens rows / FMAX, 1e-12).
+ * Defined by: per-channel KV scales, "DeepSeek-V4.1 512K"
+ * (hotelren.com/news/5711065) sec. 3.3; absmax / FMAX, dpshk.com/news/5605006
+ * sec. 3.1.
+ * x          bf16 [num_tokens][n_kv_heads][head_dim].
+ * scale_out  f32 [n_kv_heads][head_dim], overwritten (used as scratch for the
+ *            running maximum during the call).
+ */
+int fp8pa_kv_channel_scales(const void* x, int num_tokens, int n_kv_heads, int head_dim, int fmt,
+                            float* scale_out, void* stream);
+
+/*
+ * Bytes of device workspace fp8pa_paged_decode_attention needs for these
+ * shapes on the current device (it depends on the device's SM count).
+ */
+size_t fp8pa_decode_workspace_bytes(int batch, int n_q_heads, int n_kv_heads, int head_dim,
+                                    int head_dim_v, int block_size, int max_blocks_per_seq);
+
+/*
+ * Decode-step attention of one query token per request over its paged,
+ * FP8-quantised cache: out[b][h] = sum_t softmax_t(sm_scale * q[b][h] . k^_t)
+ * * v^_t over t < seq_lens[b], with k^ = decode(code) * scale.
+ * Defined by: GQA, dpshk.com/news/5605006 sec. 1.2; FP32 softmax,
+ * 2kiu.com/news/4508674 sec. 2.3; blockwise online softmax,
+ * hotelren.com/news/5711065 sec. 2.2; paged blocks, same page sec. 3.3;
+ * MLA latent, 2kiu.com/news/4508674 sec. 2.2.
+ *
+ * Long contexts are split into chunks across the whole GPU and the per-chunk
+ * partials (running max, sum, unnormalised output) are merged by a second
+ * pass; the result does not depend on the split beyond fp32 rounding.
+ *
+ * Two layouts are served:
+ *  GQA  n_q_heads % n_kv_heads == 0, n_q_heads/n_kv_heads <= 8, head_dim in
+ *       {64, 128}, head_dim_v == head_dim, block_size in {16, 32, 64},
+ *       scale_mode TOKEN_HEAD or CHANNEL_STATIC, separate v_cache/v_scale.
+ *  MLA  n_kv_heads == 1, head_dim 576 (512 latent + 64 rope), head_dim_v
+ *       512 (the first 512 dims of the same latent), v_cache == k_cache,
+ *       v_scale == k_scale, scale_mode TOKEN_GROUP, group_size 64,
+ *       block_size 64, n_q_heads a multiple of 64.
+ *
+ * seq_lens     i32 [batch], including any token appended this step; 0 gives
+ *              a zero output row.
+ * num_blocks   size of the pool (bounds block ids; sizes the copy maps).
+ * out_dtype    FP8PA_OUT_BF16 (round to nearest even) or FP8PA_OUT_F32.
+ * workspace    device scratch of at least fp8pa_decode_workspace_bytes();
+ *              16-byte aligned; contents need no initialisation.  Calls that
+ *              share a workspace must be stream-ordered.
+ * Errors       negative code, nothing launched.  Bad block ids or lengths
+ *              are masked on the device and set an error bit.
+ */
+int fp8pa_paged_decode_attention(const void* q, const uint8_t* k_cache, const uint8_t* v_cache,
+                                 const float* k_scale, const float* v_scale,
+                                 const int32_t* block_tables, int max_blocks_per_seq,
+                                 const int32_t* seq_lens, int batch, int block_size,
+                                 int n_q_heads, int n_kv_heads, int head_dim, int head_dim_v,
+                                 int fmt, int scale_mode, int group_size, float sm_scale,
+                                 int num_blocks, void* out, int out_dtype, void* workspace,
+                                 size_t workspace_bytes, void* stream);
+
+/*
+ * Synchronise `stream`, then return (in *flags) and clear the current
+ * device's error word.  Returns FP8PA_OK or FP8PA_ERR_CUDA.
+ */
+int fp8pa_get_device_error(void* stream, uint32_t* flags);
+
+/*
+ * Tuning and testing knob: the number of split workers the decode uses
+ * (0 = one per resident warp slot on the device, the default).  It changes
+ * how the sequences are cut into partials, never the result beyond fp32
+ * rounding.  Process-wide; set it between calls, not during them.  It also
+ * changes fp8pa_decode_workspace_bytes().
+ */
+int fp8pa_set_decode_workers(int workers);
+
+/*
+ * Measurement hook: when both events are non-NULL (cudaEvent_t handles),
+ * every later fp8pa_paged_decode_attention call records `start` on its
+ * stream immediately before its split kernel and `stop` immediately after
+ * it, so a caller can time the dominant kernel alone.  NULL, NULL turns it
+ * off.  Process-wide; set it between calls.
+ */
+int fp8pa_set_split_events(void* start, void* stop);
+
+/* Static text for a status code. */
+const char* fp8pa_error_string(int code);
+
+/* ABI version: (major << 16) | minor. */
+int fp8pa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8PA_H */

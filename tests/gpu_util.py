@@ -1,0 +1,138 @@
+"""Helpers shared by the GPU parity tests: fill a cache on the GPU through
+the library and the same cache on the host through the oracle, from the
+same seeded inputs, and compare within the stated tolerance."""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import torch
+
+import oracle
+from fp8_quantised_paged_gb300 import workloads as W
+
+DEV = "cuda:0"
+
+# Attention tolerance (bf16 output): max-abs 4e-3 against the FP64 oracle
+# computed from the same codes and scales, plus half a bf16 ulp of the
+# reference for the final rounding to bf16, and rel-L2 2e-3.
+ATOL = 4e-3
+RTOL_L2 = 2e-3
+
+
+def half_ulp_bf16(x: np.ndarray) -> np.ndarray:
+    ax = np.abs(np.asarray(x, np.float64))
+    e = np.floor(np.log2(np.maximum(ax, 2.0 ** -126)))
+    return np.exp2(e - 8)
+
+
+def check_close(got, ref, bf16_out=True, what=""):
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    assert got.shape == ref.shape, (got.shape, ref.shape)
+    assert np.isfinite(got).all(), f"{what}: non-finite output"
+    err = np.abs(got - ref)
+    bound = ATOL + (half_ulp_bf16(ref) if bf16_out else 0.0)
+    worst = np.argmax(err - bound)
+    assert (err <= bound).all(), (f"{what}: max excess {float((err - bound).flat[worst]):.3g} at "
+                                  f"{np.unravel_index(worst, err.shape)}; max abs "
+                                  f"{err.max():.3g}")
+    den = np.linalg.norm(ref)
+    rel = np.linalg.norm(got - ref) / den if den > 0 else np.linalg.norm(got)
+    assert rel <= RTOL_L2, f"{what}: rel-L2 {rel:.3g}"
+    return float(err.max()), float(rel)
+
+
+def to_dev_bf16(bits: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(DEV)
+
+
+def n_scale_groups(w):
+    return w.head_dim // w.group_size if w.scale_mode == W.SCALE_TOKEN_GROUP else 1
+
+
+def gpu_cache(w, F, kvs=None):
+    """Prefill all but the last token of every request with one append call,
+    then append each request's last token with a second call (the decode
+    step).  Returns device tensors (k_cache, v_cache, k_scale, v_scale)."""
+    nb, hkv, bs, d = w.num_blocks, w.n_kv_heads, w.block_size, w.head_dim
+    kc = torch.zeros((nb, hkv, bs, d), dtype=torch.uint8, device=DEV)
+    vc = None if w.mla else torch.zeros_like(kc)
+    if kvs is None:
+        kvs = [W.request_kv(w, b) for b in range(w.batch)]
+    if w.scale_mode == W.SCALE_CHANNEL_STATIC:
+        ks = F.kv_channel_scales(to_dev_bf16(np.concatenate([k for k, _ in kvs])), w.fmt)
+        vs = F.kv_channel_scales(to_dev_bf16(np.concatenate([v for _, v in kvs])), w.fmt)
+    else:
+        ks = torch.zeros((nb, hkv, bs, n_scale_groups(w)), dtype=torch.float32, device=DEV)
+        vs = None if w.mla else torch.zeros_like(ks)
+    pk, pv, ps = [], [], []
+    for b, (k, v) in enumerate(kvs):
+        L = int(w.seq_lens[b])
+        pk.append(k[:L - 1])
+        if v is not None:
+            pv.append(v[:L - 1])
+        ps.append(W.token_slots(w, b, 0, L - 1))
+    F.kv_append_quant(to_dev_bf16(np.concatenate(pk)),
+                      None if w.mla else to_dev_bf16(np.concatenate(pv)),
+                      torch.from_numpy(np.concatenate(ps)).to(DEV), kc, vc, ks, vs, fmt=w.fmt,
+                      scale_mode=w.scale_mode, group_size=w.group_size)
+    sk = np.stack([k[-1] for k, _ in kvs])
+    sv = None if w.mla else np.stack([v[-1] for _, v in kvs])
+    F.kv_append_quant(to_dev_bf16(sk), None if w.mla else to_dev_bf16(sv),
+                      torch.from_numpy(W.step_slots(w)).to(DEV), kc, vc, ks, vs, fmt=w.fmt,
+                      scale_mode=w.scale_mode, group_size=w.group_size)
+    if w.mla:
+        vc, vs = kc, ks
+    return kc, vc, ks, vs
+
+
+def oracle_cache(w, kvs=None, requests=None):
+    """The same cache built by the oracle on the host (all requests, or only
+    `requests`; static channel scales always from every request)."""
+    nb, hkv, bs, d = w.num_blocks, w.n_kv_heads, w.block_size, w.head_dim
+    kc = np.zeros((nb, hkv, bs, d), np.uint8)
+    vc = None if w.mla else np.zeros_like(kc)
+    if kvs is None:
+        kvs = [W.request_kv(w, b) for b in range(w.batch)]
+    if w.scale_mode == W.SCALE_CHANNEL_STATIC:
+        ks = oracle.kv_channel_scales(np.concatenate([k for k, _ in kvs]), w.fmt)
+        vs = oracle.kv_channel_scales(np.concatenate([v for _, v in kvs]), w.fmt)
+    else:
+        ks = np.zeros((nb, hkv, bs, n_scale_groups(w)), np.float32)
+        vs = None if w.mla else np.zeros_like(ks)
+    for b, (k, v) in enumerate(kvs):
+        if requests is not None and b not in requests:
+            continue
+        slots = W.token_slots(w, b, 0, int(w.seq_lens[b]))
+        assert oracle.kv_append_quant(k, v, slots, w.fmt, w.scale_mode, w.group_size, kc, vc,
+                                      ks, vs, bs) == 0
+    if w.mla:
+        vc, vs = kc, ks
+    return kc, vc, ks, vs
+
+
+def oracle_attention(w, q, caches, rows=None):
+    kc, vc, ks, vs = caches
+    return oracle.paged_decode_attention(q, kc, vc, ks, vs, w.block_tables, w.seq_lens,
+                                         w.block_size, w.n_kv_heads, w.head_dim_v, w.fmt,
+                                         w.scale_mode, w.group_size, w.sm_scale, rows=rows)
+
+
+def gpu_attention(w, F, q_bits, caches, out_dtype=torch.bfloat16):
+    kc, vc, ks, vs = caches
+    out = F.paged_decode_attention(to_dev_bf16(q_bits), kc, vc, ks, vs,
+                                   torch.from_numpy(w.block_tables).to(DEV),
+                                   torch.from_numpy(w.seq_lens).to(DEV), w.n_kv_heads,
+                                   w.sm_scale, fmt=w.fmt, scale_mode=w.scale_mode,
+                                   group_size=w.group_size, head_dim_v=w.head_dim_v,
+                                   out_dtype=out_dtype)
+    return out.float().cpu().numpy().astype(np.float64)
+
+
+def nbytes_human(n):
+    return f"{n / 1e6:.1f} MB" if n < 1e9 else f"{n / 1e9:.2f} GB"
+
+
+def sqrt(x):
+    return math.sqrt(x)

@@ -1,0 +1,89 @@
+"""Host-side checks of the C ABI that need no GPU: the library builds, loads
+and exports every symbol include/fp8pa.h declares, and argument errors come
+back as status codes before anything touches a device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fp8pa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from fp8_quantised_paged_gb300 import build
+    build.build()
+    from fp8_quantised_paged_gb300 import _native
+    return _native.lib
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fp8pa_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_two_calls():
+    names = declared_functions()
+    assert "fp8pa_kv_append_quant" in names and "fp8pa_paged_decode_attention" in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    from fp8_quantised_paged_gb300 import _native
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert name in _native._SIGS, f"binding lacks {name}"
+
+
+def test_status_strings_and_version(lib):
+    assert lib.fp8pa_version() >> 16 == 1
+    for code in range(-7, 1):
+        assert lib.fp8pa_error_string(code)
+    assert lib.fp8pa_error_string(-99) == b"unknown status"
+
+
+def test_argument_errors_need_no_device(lib):
+    P = ctypes.c_void_p
+    fake = P(0x1000)
+    # bad enum
+    assert lib.fp8pa_kv_append_quant(fake, None, fake, 4, 1, 64, 7, 0, 64, fake, None, fake, None,
+                                     8, 16, None) == -2
+    # bad shape
+    assert lib.fp8pa_kv_append_quant(fake, None, fake, 4, 0, 64, 0, 0, 64, fake, None, fake, None,
+                                     8, 16, None) == -3
+    # head_dim not a multiple of 16
+    assert lib.fp8pa_kv_append_quant(fake, None, fake, 4, 1, 40, 0, 0, 64, fake, None, fake, None,
+                                     8, 16, None) == -4
+    # null pointers
+    assert lib.fp8pa_kv_append_quant(None, None, fake, 4, 1, 64, 0, 0, 64, fake, None, fake, None,
+                                     8, 16, None) == -1
+    # misaligned
+    assert lib.fp8pa_kv_append_quant(P(0x1001), None, fake, 4, 1, 64, 0, 0, 64, fake, None, fake,
+                                     None, 8, 16, None) == -6
+    # no tokens: nothing to do
+    assert lib.fp8pa_kv_append_quant(None, None, None, 0, 1, 64, 0, 0, 64, None, None, None, None,
+                                     8, 16, None) == 0
+
+    def dec(**kw):
+        a = dict(q=fake, kc=fake, vc=fake, ks=fake, vs=fake, bt=fake, mb=4, sl=fake, B=2, bs=16,
+                 hq=8, hkv=2, d=128, dv=128, fmt=0, mode=0, gs=64, sm=0.1, nb=16, out=fake,
+                 odt=0, ws=fake, wsb=1 << 30, st=None)
+        a.update(kw)
+        return lib.fp8pa_paged_decode_attention(
+            a["q"], a["kc"], a["vc"], a["ks"], a["vs"], a["bt"], a["mb"], a["sl"], a["B"],
+            a["bs"], a["hq"], a["hkv"], a["d"], a["dv"], a["fmt"], a["mode"], a["gs"],
+            ctypes.c_float(a["sm"]), a["nb"], a["out"], a["odt"], a["ws"], a["wsb"], a["st"])
+
+    assert dec(hq=7) == -3          # Hq % Hkv != 0
+    assert dec(fmt=3) == -2
+    assert dec(mode=5) == -2
+    assert dec(odt=2) == -2
+    assert dec(d=96, dv=96) == -4   # head_dim not served
+    assert dec(hq=32, hkv=2) == -4  # 16 heads per KV head
+    assert dec(bs=8) == -4
+    assert dec(q=None) == -1
+    assert dec(vc=None) == -1
+    assert dec(B=0) == 0
+    assert dec(d=576, dv=512, hkv=1, hq=128, mode=2, bs=64, vc=P(0x2000)) == -4  # MLA needs v==k

@@ -1,0 +1,140 @@
+"""GPU parity of the append step: FP8 codes, scales and slot placement must
+be bit-exact with the oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from fp8_quantised_paged_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def F():
+    import fp8_quantised_paged_gb300 as F
+    F.get_device_error()  # clear
+    return F
+
+
+def _assert_codes_equal(got, want, what):
+    got = np.asarray(got)
+    want = np.asarray(want)
+    bad = np.flatnonzero(got.reshape(-1) != want.reshape(-1))
+    assert bad.size == 0, (f"{what}: {bad.size} mismatches, first at flat {bad[0]}: "
+                           f"gpu {got.reshape(-1)[bad[0]]:#04x} oracle {want.reshape(-1)[bad[0]]:#04x}")
+
+
+@pytest.mark.parametrize("idx", [1, 2, 3, 4, 5])
+def test_append_matches_oracle(F, idx):
+    from gpu_util import gpu_cache, oracle_cache
+    w = W.make_workload(idx, "small")
+    kvs = [W.request_kv(w, b) for b in range(w.batch)]
+    g = gpu_cache(w, F, kvs)
+    o = oracle_cache(w, kvs)
+    assert F.get_device_error() == 0
+    _assert_codes_equal(g[0].cpu().numpy(), o[0], "k codes")
+    assert np.array_equal(g[2].cpu().numpy().view(np.uint32), o[2].view(np.uint32)), "k scales"
+    if not w.mla:
+        _assert_codes_equal(g[1].cpu().numpy(), o[1], "v codes")
+        assert np.array_equal(g[3].cpu().numpy().view(np.uint32), o[3].view(np.uint32))
+
+
+def _all_bf16_rows(d):
+    """Every bf16 bit pattern once, as rows of d values."""
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    return bits.reshape(-1, 1, d)
+
+
+@pytest.mark.parametrize("fmt", [W.E4M3, W.E5M2])
+@pytest.mark.parametrize("scale", [1.0, 2.0 ** -7, 0.3, 1000.0])
+def test_every_bf16_pattern_static_scale(F, fmt, scale):
+    """Static scale: code = fp8(x / s) for all 65,536 bf16 inputs."""
+    from gpu_util import DEV, to_dev_bf16
+    d = 128
+    x = _all_bf16_rows(d)
+    n = x.shape[0]
+    s = np.full((1, d), scale, np.float32)
+    kc = torch.zeros((n, 1, 1, d), dtype=torch.uint8, device=DEV)
+    slots = torch.arange(n, dtype=torch.int32, device=DEV)
+    F.kv_append_quant(to_dev_bf16(x), None, slots, kc, None, torch.from_numpy(s).to(DEV), None,
+                      fmt=fmt, scale_mode=W.SCALE_CHANNEL_STATIC)
+    got = kc.cpu().numpy().reshape(-1)
+    okc = np.zeros((n, 1, 1, d), np.uint8)
+    oracle.kv_append_quant(x, None, np.arange(n, dtype=np.int32), fmt, W.SCALE_CHANNEL_STATIC, d,
+                           okc, None, s.copy(), None, 1)
+    want = okc.reshape(-1)
+    xf = W.bf16_bits_to_f32(x.reshape(-1))
+    nan_in = np.isnan(xf)
+    # NaN inputs: any NaN code is a correct answer; everything else is unique.
+    dec = oracle.fp8_decode(got[nan_in], fmt)
+    assert np.isnan(dec).all()
+    _assert_codes_equal(got[~nan_in], want[~nan_in], f"fmt={fmt} scale={scale}")
+
+
+@pytest.mark.parametrize("fmt", [W.E4M3, W.E5M2])
+def test_every_finite_bf16_pattern_dynamic_rows(F, fmt):
+    """Dynamic per-row scales over rows that together hold every finite bf16."""
+    from gpu_util import DEV, to_dev_bf16
+    d = 128
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    xf = W.bf16_bits_to_f32(bits)
+    fin = bits[np.isfinite(xf)]
+    rng = np.random.default_rng(1)
+    fin = rng.permutation(fin)
+    pad = (-fin.size) % (2 * d)
+    fin = np.concatenate([fin, np.zeros(pad, np.uint16)])
+    x = fin.reshape(-1, 2, d)  # [tokens, hkv=2, d]
+    n = x.shape[0]
+    bs = 16
+    nb = (n + bs - 1) // bs + 1
+    kc = torch.zeros((nb, 2, bs, d), dtype=torch.uint8, device=DEV)
+    ks = torch.zeros((nb, 2, bs, 1), dtype=torch.float32, device=DEV)
+    slots = rng.permutation(nb * bs)[:n].astype(np.int32)
+    F.kv_append_quant(to_dev_bf16(x), None, torch.from_numpy(slots).to(DEV), kc, None, ks, None,
+                      fmt=fmt, scale_mode=W.SCALE_TOKEN_HEAD)
+    okc = np.zeros((nb, 2, bs, d), np.uint8)
+    oks = np.zeros((nb, 2, bs, 1), np.float32)
+    oracle.kv_append_quant(x, None, slots, fmt, W.SCALE_TOKEN_HEAD, d, okc, None, oks, None, bs)
+    _assert_codes_equal(kc.cpu().numpy(), okc, "codes")
+    assert np.array_equal(ks.cpu().numpy().view(np.uint32), oks.view(np.uint32))
+
+
+def test_edges_zero_rows_skip_and_bad_slots(F):
+    from gpu_util import DEV, to_dev_bf16
+    d, hkv, bs, nb = 64, 2, 16, 4
+    x = np.zeros((5, hkv, d), np.uint16)
+    x[1] = 0x8000                      # a row of -0.0
+    x[2, 0, 3] = 0x3F80                # one 1.0 among zeros
+    x[3, 1, :] = 0x4300                # 128.0 everywhere
+    slots = np.array([0, 5, -1, 63, 64], np.int32)  # -1 skipped, 64 past the pool
+    for fmt in (W.E4M3, W.E5M2):
+        kc = torch.full((nb, hkv, bs, d), 0xAA, dtype=torch.uint8, device=DEV)
+        vc = torch.full_like(kc, 0xAA)
+        ks = torch.full((nb, hkv, bs, 1), -1.0, dtype=torch.float32, device=DEV)
+        vs = torch.full_like(ks, -1.0)
+        F.kv_append_quant(to_dev_bf16(x), to_dev_bf16(x), torch.from_numpy(slots).to(DEV), kc,
+                          vc, ks, vs, fmt=fmt)
+        assert F.get_device_error() == 1   # FP8PA_DEVERR_SLOT_RANGE
+        okc = np.full((nb, hkv, bs, d), 0xAA, np.uint8)
+        ovc = okc.copy()
+        oks = np.full((nb, hkv, bs, 1), -1.0, np.float32)
+        ovs = oks.copy()
+        assert oracle.kv_append_quant(x, x, slots, fmt, W.SCALE_TOKEN_HEAD, d, okc, ovc, oks, ovs,
+                                      bs) == 1
+        _assert_codes_equal(kc.cpu().numpy(), okc, "k")
+        _assert_codes_equal(vc.cpu().numpy(), ovc, "v")
+        assert np.array_equal(ks.cpu().numpy().view(np.uint32), oks.view(np.uint32))
+        # -0.0 keeps its sign; a zero row gets the 1e-12 floor
+        assert (kc[0, 1, 5].cpu().numpy() == 0x80).all()
+        assert ks[0, 0, 0, 0].item() == np.float32(1e-12)
+
+
+def test_channel_scales_match_oracle(F):
+    from gpu_util import DEV, to_dev_bf16
+    w = W.make_workload(4, "small")
+    ks = np.concatenate([W.request_kv(w, b)[0] for b in range(w.batch)])
+    for fmt in (W.E4M3, W.E5M2):
+        got = F.kv_channel_scales(to_dev_bf16(ks), fmt).cpu().numpy()
+        want = oracle.kv_channel_scales(ks, fmt)
+        assert np.array_equal(got.view(np.uint32), want.view(np.uint32))

@@ -1,0 +1,219 @@
+"""GPU parity of paged decode attention against the FP64 oracle computed
+from the same codes and scales: every output at oracle-sized shapes, sampled
+rows at the full workload sizes, split-count independence and edge cases."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from fp8_quantised_paged_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def F():
+    import fp8_quantised_paged_gb300 as F
+    F.get_device_error()
+    F.set_decode_workers(0)
+    yield F
+    F.set_decode_workers(0)
+
+
+GQA = [1, 2, 3, 4]
+
+
+@pytest.mark.parametrize("idx", GQA)
+def test_decode_small_matches_oracle(F, idx):
+    from gpu_util import check_close, gpu_attention, gpu_cache, oracle_attention, oracle_cache
+    w = W.make_workload(idx, "small")
+    kvs = [W.request_kv(w, b) for b in range(w.batch)]
+    g = gpu_cache(w, F, kvs)
+    o = oracle_cache(w, kvs)
+    assert np.array_equal(g[0].cpu().numpy(), o[0])  # same codes on both sides
+    q = W.queries(w)
+    ref = oracle_attention(w, q, o)
+    got = gpu_attention(w, F, q, g)
+    check_close(got, ref, bf16_out=True, what=f"cfg{idx} bf16")
+    got32 = gpu_attention(w, F, q, g, out_dtype=torch.float32)
+    check_close(got32, ref, bf16_out=False, what=f"cfg{idx} f32")
+    assert F.get_device_error() == 0
+
+
+@pytest.mark.parametrize("idx", [1, 3, 4])
+def test_decode_independent_of_split_count(F, idx):
+    from gpu_util import check_close, gpu_attention, gpu_cache, oracle_attention, oracle_cache
+    w = W.make_workload(idx, "small")
+    kvs = [W.request_kv(w, b) for b in range(w.batch)]
+    g = gpu_cache(w, F, kvs)
+    q = W.queries(w)
+    ref = oracle_attention(w, q, oracle_cache(w, kvs))
+    outs = []
+    try:
+        for workers in (1, 2, 7, 64, 1000, 0):
+            F.set_decode_workers(workers)
+            o = gpu_attention(w, F, q, g, out_dtype=torch.float32)
+            check_close(o, ref, bf16_out=False, what=f"workers={workers}")
+            outs.append(o)
+    finally:
+        F.set_decode_workers(0)
+    for o in outs[1:]:
+        assert np.allclose(o, outs[0], rtol=2e-5, atol=2e-6)
+
+
+def test_decode_edges(F):
+    """seq_len 0 gives zeros; a bad block id is masked and flagged; a length
+    past the block table is clamped and flagged; nothing traps."""
+    from gpu_util import DEV, gpu_cache, oracle_attention, oracle_cache, check_close, to_dev_bf16
+    w = W.make_workload(2, "small")
+    kvs = [W.request_kv(w, b) for b in range(w.batch)]
+    g = gpu_cache(w, F, kvs)
+    o = oracle_cache(w, kvs)
+    q = W.queries(w)
+    kc, vc, ks, vs = g
+
+    def run(bt, sl):
+        return F.paged_decode_attention(to_dev_bf16(q), kc, vc, ks, vs,
+                                        torch.from_numpy(bt).to(DEV), torch.from_numpy(sl).to(DEV),
+                                        w.n_kv_heads, w.sm_scale, out_dtype=torch.float32)
+
+    sl = w.seq_lens.copy()
+    sl[1] = 0
+    out = run(w.block_tables, sl).cpu().numpy()
+    assert (out[1] == 0).all()
+    assert F.get_device_error() == 0
+    w2 = W.make_workload(2, "small")
+    w2.seq_lens = sl
+    check_close(out[[0, 2]], oracle_attention(w2, q, o)[[0, 2]], bf16_out=False)
+
+    bt = w.block_tables.copy()
+    bt[0, 3] = w.num_blocks + 5      # out of the pool: that page is masked
+    out = run(bt, w.seq_lens).cpu().numpy()
+    assert F.get_device_error() == 2  # FP8PA_DEVERR_BLOCK_RANGE
+    assert np.isfinite(out).all()
+    check_close(out[1:], oracle_attention(w, q, o)[1:], bf16_out=False)
+
+    sl = w.seq_lens.copy()
+    sl[2] = w.block_tables.shape[1] * w.block_size + 100
+    out = run(w.block_tables, sl).cpu().numpy()
+    assert F.get_device_error() & 4   # FP8PA_DEVERR_SEQ_LEN
+    assert np.isfinite(out).all()
+
+
+def test_decode_bad_arguments_return_codes(F):
+    from gpu_util import DEV, to_dev_bf16
+    w = W.make_workload(1, "small")
+    q = to_dev_bf16(W.queries(w))
+    kc = torch.zeros((w.num_blocks, 1, 16, 64), dtype=torch.uint8, device=DEV)
+    ks = torch.zeros((w.num_blocks, 1, 16, 1), dtype=torch.float32, device=DEV)
+    bt = torch.from_numpy(w.block_tables).to(DEV)
+    sl = torch.from_numpy(w.seq_lens).to(DEV)
+    with pytest.raises(F.Fp8paError) as e:
+        F.paged_decode_attention(q, kc, kc, ks, ks, bt, sl, 3, 0.125)  # 4 % 3 != 0
+    assert e.value.code == -3
+    with pytest.raises(F.Fp8paError) as e:
+        F.paged_decode_attention(q, kc, kc, ks, ks, bt, sl, 1, 0.125, fmt=9)
+    assert e.value.code == -2
+    small_ws = torch.zeros(16, dtype=torch.uint8, device=DEV)
+    with pytest.raises(F.Fp8paError) as e:
+        F.paged_decode_attention(q, kc, kc, ks, ks, bt, sl, 1, 0.125, workspace=small_ws)
+    assert e.value.code == -5
+    assert F.get_device_error() == 0
+
+
+def _full_size_sampled(F, idx, sample):
+    """Full-size workload through the GPU path (prefill, step append and the
+    decode in the bench's launch configuration); the oracle rebuilds only the
+    sampled requests in a compact pool and checks their codes and outputs."""
+    from gpu_util import DEV, check_close, gpu_attention, to_dev_bf16
+    w = W.make_workload(idx, "full")
+    nb, hkv, bs, d = w.num_blocks, w.n_kv_heads, w.block_size, w.head_dim
+    kc = torch.zeros((nb, hkv, bs, d), dtype=torch.uint8, device=DEV)
+    vc = None if w.mla else torch.zeros_like(kc)
+    kv_sample = {}
+    if w.scale_mode == W.SCALE_CHANNEL_STATIC:
+        allk = [W.request_kv(w, b) for b in range(w.batch)]
+        ks = F.kv_channel_scales(to_dev_bf16(np.concatenate([k for k, _ in allk])), w.fmt)
+        vs = F.kv_channel_scales(to_dev_bf16(np.concatenate([v for _, v in allk])), w.fmt)
+        oks = oracle.kv_channel_scales(np.concatenate([k for k, _ in allk]), w.fmt)
+        ovs = oracle.kv_channel_scales(np.concatenate([v for _, v in allk]), w.fmt)
+        assert np.array_equal(ks.cpu().numpy().view(np.uint32), oks.view(np.uint32))
+        assert np.array_equal(vs.cpu().numpy().view(np.uint32), ovs.view(np.uint32))
+        get = lambda b: allk[b]
+    else:
+        ng = d // w.group_size if w.scale_mode == W.SCALE_TOKEN_GROUP else 1
+        ks = torch.zeros((nb, hkv, bs, ng), dtype=torch.float32, device=DEV)
+        vs = None if w.mla else torch.zeros_like(ks)
+        get = lambda b: W.request_kv(w, b)
+    last_k, last_v = [], []
+    for b in range(w.batch):
+        k, v = get(b)
+        L = int(w.seq_lens[b])
+        if b in sample:
+            kv_sample[b] = (k, v)
+        if L > 1:
+            F.kv_append_quant(to_dev_bf16(k[:L - 1]), None if v is None else to_dev_bf16(v[:L - 1]),
+                              torch.from_numpy(W.token_slots(w, b, 0, L - 1)).to(DEV), kc, vc, ks,
+                              vs, fmt=w.fmt, scale_mode=w.scale_mode, group_size=w.group_size)
+        last_k.append(k[L - 1])
+        if v is not None:
+            last_v.append(v[L - 1])
+    F.kv_append_quant(to_dev_bf16(np.stack(last_k)), None if w.mla else to_dev_bf16(np.stack(last_v)),
+                      torch.from_numpy(W.step_slots(w)).to(DEV), kc, vc, ks, vs, fmt=w.fmt,
+                      scale_mode=w.scale_mode, group_size=w.group_size)
+    if w.mla:
+        vc, vs = kc, ks
+    q = W.queries(w)
+    got = gpu_attention(w, F, q, (kc, vc, ks, vs))
+    assert F.get_device_error() == 0
+    # Compact oracle pool holding only the sampled requests' blocks.
+    for b in sample:
+        k, v = kv_sample[b]
+        L = int(w.seq_lens[b])
+        nbl = (L + bs - 1) // bs
+        blocks = w.block_tables[b, :nbl].astype(np.int64)
+        cw = W.make_workload(idx, "full")
+        cw.batch = 1
+        cw.seq_lens = np.array([L], np.int32)
+        cw.block_tables = np.arange(nbl, dtype=np.int32)[None]
+        cw.num_blocks = nbl
+        okc = np.zeros((nbl, hkv, bs, d), np.uint8)
+        ovc = None if w.mla else np.zeros_like(okc)
+        if w.scale_mode == W.SCALE_CHANNEL_STATIC:
+            oks2, ovs2 = oks, ovs
+        else:
+            oks2 = np.zeros((nbl, hkv, bs, ks.shape[-1]), np.float32)
+            ovs2 = None if w.mla else np.zeros_like(oks2)
+        slots = W.token_slots(cw, 0, 0, L)
+        assert oracle.kv_append_quant(k, v, slots, w.fmt, w.scale_mode, w.group_size, okc, ovc,
+                                      oks2, ovs2, bs) == 0
+        gk = kc[torch.from_numpy(blocks).to(DEV)].cpu().numpy()
+        assert np.array_equal(gk, okc), f"request {b}: K codes differ"
+        if not w.mla:
+            assert np.array_equal(vc[torch.from_numpy(blocks).to(DEV)].cpu().numpy(), ovc)
+        if w.scale_mode != W.SCALE_CHANNEL_STATIC:
+            assert np.array_equal(ks[torch.from_numpy(blocks).to(DEV)].cpu().numpy().view(np.uint32),
+                                  oks2.view(np.uint32))
+        if w.mla:
+            ovc, ovs2 = okc, oks2
+        ref = oracle.paged_decode_attention(q[b:b + 1], okc, ovc, oks2, ovs2, cw.block_tables,
+                                            cw.seq_lens, bs, hkv, w.head_dim_v, w.fmt,
+                                            w.scale_mode, w.group_size, w.sm_scale)
+        check_close(got[b:b + 1], ref, bf16_out=True, what=f"cfg{idx} request {b}")
+
+
+@pytest.mark.slow
+def test_full_llama70b_layer_sampled(F):
+    _full_size_sampled(F, 2, sample=(0, 7, 11))
+
+
+@pytest.mark.slow
+def test_full_long_context_sampled(F):
+    _full_size_sampled(F, 3, sample=(2,))
+
+
+@pytest.mark.slow
+def test_full_ragged_e5m2_sampled(F):
+    w = W.make_workload(4, "full")
+    order = np.argsort(w.seq_lens)
+    _full_size_sampled(F, 4, sample=(int(order[0]), int(order[len(order) // 2]), int(order[-1])))
