@@ -131,15 +131,17 @@ def paged_decode_attention(q, k_cache, v_cache, k_scale, v_scale, block_tables, 
         raise TypeError("out must be bf16 or float32")
     _need(out, out.dtype, "out", dev)
     with torch.cuda.device(dev):
-        need = decode_workspace_bytes(B, hq, n_kv_heads, dk, dv, bs, max_blocks, dev)
-        if workspace is None:
+        need = int(N.lib.fp8pa_decode_workspace_bytes(B, hq, n_kv_heads, dk, dv, bs, max_blocks))
+        if workspace is None and need > 0:
             workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+        # need == 0 means the shapes are rejected: the call below returns the
+        # precise status code.
         _need(workspace, torch.uint8, "workspace", dev)
         rc = N.lib.fp8pa_paged_decode_attention(
             _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
             _ptr(block_tables), max_blocks, _ptr(seq_lens), B, bs, hq, n_kv_heads, dk, dv, fmt,
             scale_mode, group_size, float(sm_scale), nb, _ptr(out), odt, _ptr(workspace),
-            workspace.numel(), _stream(stream))
+            0 if workspace is None else workspace.numel(), _stream(stream))
     N.check(rc, "paged_decode_attention")
     return out
 

@@ -137,7 +137,7 @@ struct GqaSmem {
   static constexpr int kPage = BS * D;
   static constexpr int kPages = kWarps * NST * 2 * kPage;
   static constexpr int kScales = kWarps * NST * 2 * BS * 4;
-  static constexpr int kPs = kWarps * 256;
+  static constexpr int kPs = kWarps * 512;
   static constexpr int kBars = kWarps * NST * 8;
   static constexpr int kOk = kWarps * NST * 4;
   static constexpr int kBytes = kPages + kScales + kPs + kBars + kOk + 1024;
@@ -179,7 +179,8 @@ __global__ void __launch_bounds__(kWarps * 32)
   const int g = lane >> 2, c = lane & 3;
   uint8_t* pages = smem + warp * (NST * 2 * PAGE);
   float* scl = reinterpret_cast<float*>(smem + SM::kPages) + warp * (NST * 2 * BS);
-  uint16_t* ps = reinterpret_cast<uint16_t*>(smem + SM::kPages + SM::kScales) + warp * 128;
+  // P^T for the PV MMA as two f16 planes (hi + lo carry ~22 significant bits)
+  uint16_t* ps = reinterpret_cast<uint16_t*>(smem + SM::kPages + SM::kScales) + warp * 256;
   uint64_t* bars =
       reinterpret_cast<uint64_t*>(smem + SM::kPages + SM::kScales + SM::kPs) + warp * NST;
   int* okf =
@@ -263,8 +264,11 @@ __global__ void __launch_bounds__(kWarps * 32)
     }
   }
 
-  // ---- per-segment state
-  uint32_t qb[KW][2];
+  // ---- per-segment state.  Q enters the MMA as f16; with static channel
+  // scales folded in it is no longer exact in f16, so it is split into a
+  // high and a low f16 part and the contraction runs twice.
+  constexpr int QP = TOKSC ? 1 : 2;
+  uint32_t qb[QP][KW][2];
   float O[MT][4];
   float m0 = -FLT_MAX, m1 = -FLT_MAX, l0 = 0.f, l1 = 0.f, zs = 0.f;
   int erun = -127, Lb = 0;
@@ -310,9 +314,19 @@ __global__ void __launch_bounds__(kWarps * 32)
       const int eq = amax > 0.f ? exp_above(amax) : 0;
       const float fq = exp2i(14 - eq);
 #pragma unroll
+      for (int e = 0; e < D / 4; ++e) qv[e] *= fq;
+#pragma unroll
       for (int j = 0; j < KW; ++j) {
-        qb[j][0] = pack_half2(qv[4 * j] * fq, qv[4 * j + 1] * fq);
-        qb[j][1] = pack_half2(qv[4 * j + 2] * fq, qv[4 * j + 3] * fq);
+        qb[0][j][0] = pack_half2(qv[4 * j], qv[4 * j + 1]);
+        qb[0][j][1] = pack_half2(qv[4 * j + 2], qv[4 * j + 3]);
+        if constexpr (QP == 2) {
+          float r[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            r[e] = qv[4 * j + e] - __half2float(__float2half_rn(qv[4 * j + e]));
+          qb[QP - 1][j][0] = pack_half2(r[0], r[1]);
+          qb[QP - 1][j][1] = pack_half2(r[2], r[3]);
+        }
       }
       zs = p.qk_scale_log2 * exp2i(eq - 14);
       m0 = m1 = NEG_INF;
@@ -356,9 +370,11 @@ __global__ void __launch_bounds__(kWarps * 32)
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int j = 0; j < KW; ++j) {
-        mma_16816(acc, fp8x2_to_f16x2<FMT>(kw[0][j]), fp8x2_to_f16x2<FMT>(kw[1][j]),
-                  fp8x2_to_f16x2<FMT>(kw[0][j] >> 16), fp8x2_to_f16x2<FMT>(kw[1][j] >> 16),
-                  qb[j][0], qb[j][1]);
+        const uint32_t a0 = fp8x2_to_f16x2<FMT>(kw[0][j]), a1 = fp8x2_to_f16x2<FMT>(kw[1][j]);
+        const uint32_t a2 = fp8x2_to_f16x2<FMT>(kw[0][j] >> 16);
+        const uint32_t a3 = fp8x2_to_f16x2<FMT>(kw[1][j] >> 16);
+#pragma unroll
+        for (int qp = 0; qp < QP; ++qp) mma_16816(acc, a0, a1, a2, a3, qb[qp][j][0], qb[qp][j][1]);
       }
       const bool v0 = g < tv, v1 = g + 8 < tv;
       float sk0 = 1.f, sk1 = 1.f;
@@ -427,13 +443,19 @@ __global__ void __launch_bounds__(kWarps * 32)
         const int pos0 = 4 * (g >> 2) + (((g & 3) - (g >> 2)) & 3);
         const int t1 = g + 8;
         const int pos1 = 4 * (t1 >> 2) + (((t1 & 3) - (t1 >> 2)) & 3);
-        ps[(2 * c) * 16 + pos0] = __half_as_ushort(__float2half_rn(q00));
-        ps[(2 * c + 1) * 16 + pos0] = __half_as_ushort(__float2half_rn(q01));
-        ps[(2 * c) * 16 + pos1] = __half_as_ushort(__float2half_rn(q10));
-        ps[(2 * c + 1) * 16 + pos1] = __half_as_ushort(__float2half_rn(q11));
+        const int idx[4] = {(2 * c) * 16 + pos0, (2 * c + 1) * 16 + pos0, (2 * c) * 16 + pos1,
+                            (2 * c + 1) * 16 + pos1};
+        const float val[4] = {q00, q01, q10, q11};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const __half hi = __float2half_rn(val[e]);
+          ps[idx[e]] = __half_as_ushort(hi);
+          ps[128 + idx[e]] = __half_as_ushort(__float2half_rn(val[e] - __half2float(hi)));
+        }
       }
       __syncwarp();
       const uint2 pb = lds64(smem_u32(ps + g * 16 + 4 * c));
+      const uint2 pl = lds64(smem_u32(ps + 128 + g * 16 + 4 * c));
       // ---- O^T += V^T . P^T : rows = dv, cols = heads
       uint32_t vw[4][VW];
 #pragma unroll
@@ -461,8 +483,10 @@ __global__ void __launch_bounds__(kWarps * 32)
         const uint32_t sel = (t & 1) ? 0x7362u : 0x5140u;
         const uint32_t x01 = prmt(vw[0][t >> 1], vw[1][t >> 1], sel);
         const uint32_t x23 = prmt(vw[2][t >> 1], vw[3][t >> 1], sel);
-        mma_16816(O[t], fp8x2_to_f16x2<FMT>(x01), fp8x2_to_f16x2<FMT>(x01 >> 16),
-                  fp8x2_to_f16x2<FMT>(x23), fp8x2_to_f16x2<FMT>(x23 >> 16), pb.x, pb.y);
+        const uint32_t a0 = fp8x2_to_f16x2<FMT>(x01), a1 = fp8x2_to_f16x2<FMT>(x01 >> 16);
+        const uint32_t a2 = fp8x2_to_f16x2<FMT>(x23), a3 = fp8x2_to_f16x2<FMT>(x23 >> 16);
+        mma_16816(O[t], a0, a1, a2, a3, pb.x, pb.y);
+        mma_16816(O[t], a0, a1, a2, a3, pl.x, pl.y);
       }
     }
     __syncwarp();
