@@ -32,6 +32,9 @@ _SIGS = {
     "fp8pa_paged_decode_attention": (_I, [_P, _P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I,
                                           _I, _I, _I, ctypes.c_float, _I, _P, _I, _P,
                                           ctypes.c_size_t, _P]),
+    "fp8pa_paged_decode_attention_static_ws": (_I, [_P, _P, _P, _P, _P, _P, _I, _P, _I, _I, _I,
+                                                    _I, _I, _I, _I, _I, _I, ctypes.c_float, _I,
+                                                    _P, _I, _P]),
     "fp8pa_get_device_error": (_I, [_P, ctypes.POINTER(ctypes.c_uint32)]),
     "fp8pa_set_decode_workers": (_I, [_I]),
     "fp8pa_set_split_events": (_I, [_P, _P]),

@@ -177,6 +177,43 @@ int fp8pa_paged_decode_attention(const void* q, const uint8_t* k_cache, const ui
                                  size_t workspace_bytes, void* stream);
 
 /*
+ * Size of the scratch array built into the library for
+ * fp8pa_paged_decode_attention_static_ws (16 MiB per device that uses it).
+ */
+#define FP8PA_STATIC_WORKSPACE_BYTES (16u << 20)
+
+/*
+ * The source pages have no counterpart to this call; it serves users of the
+ * library who cannot allocate device memory -- for example a plugin whose
+ * host framework passes it only the input and output buffers and owns the
+ * allocator, or a server that fixes its memory at start-up and allows no
+ * allocation afterwards.
+ *
+ * Same arguments and result as fp8pa_paged_decode_attention, minus the
+ * workspace: the scratch comes from a static device array of
+ * FP8PA_STATIC_WORKSPACE_BYTES inside the library, so the call allocates
+ * nothing (no cudaMalloc, no allocator of any library).  The caller still
+ * owns every input and the output.
+ *  - The first call on each device looks up the array's device address (with
+ *    that device current); make that first call before any stream capture.
+ *  - Every call on a device shares the one array; calls whose kernels may
+ *    overlap on the GPU (unordered streams) race and give undefined output.
+ *    Nothing in the array needs clearing between calls.
+ *  - Shapes whose workspace (fp8pa_decode_workspace_bytes) exceeds
+ *    FP8PA_STATIC_WORKSPACE_BYTES return FP8PA_ERR_WORKSPACE and launch
+ *    nothing; other errors are those of fp8pa_paged_decode_attention.
+ */
+int fp8pa_paged_decode_attention_static_ws(const void* q, const uint8_t* k_cache,
+                                           const uint8_t* v_cache, const float* k_scale,
+                                           const float* v_scale, const int32_t* block_tables,
+                                           int max_blocks_per_seq, const int32_t* seq_lens,
+                                           int batch, int block_size, int n_q_heads,
+                                           int n_kv_heads, int head_dim, int head_dim_v, int fmt,
+                                           int scale_mode, int group_size, float sm_scale,
+                                           int num_blocks, void* out, int out_dtype,
+                                           void* stream);
+
+/*
  * Synchronise `stream`, then return (in *flags) and clear the current
  * device's error word.  Returns FP8PA_OK or FP8PA_ERR_CUDA.
  */
