@@ -34,6 +34,8 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float (&f)[8]) {
 
 template <int FMT, int MODE, int R>
 __global__ void __launch_bounds__(kAppendWarps * 32) append_kernel(AppendArgs a) {
+  griddep_wait();  // launched early (programmatic serialisation): inputs may be in flight
+  griddep_launch_dependents();
   const int lane = threadIdx.x & 31;
   const long row = static_cast<long>(blockIdx.x) * kAppendWarps + (threadIdx.x >> 5);
   const int per_tok = a.hkv * a.ntens;
@@ -126,13 +128,18 @@ cudaError_t launch_append_r(const AppendArgs& a, cudaStream_t stream) {
   if (rows == 0) return cudaSuccess;
   const dim3 grid(static_cast<unsigned>((rows + kAppendWarps - 1) / kAppendWarps));
   const int nch = a.d / 8;
-  if (nch <= 32)
-    append_kernel<FMT, MODE, 1><<<grid, kAppendWarps * 32, 0, stream>>>(a);
-  else if (nch <= 64)
-    append_kernel<FMT, MODE, 2><<<grid, kAppendWarps * 32, 0, stream>>>(a);
-  else
-    append_kernel<FMT, MODE, 3><<<grid, kAppendWarps * 32, 0, stream>>>(a);
-  return cudaGetLastError();
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kAppendWarps * 32);
+  cfg.stream = stream;
+  cfg.attrs = pdl;
+  cfg.numAttrs = 1;
+  if (nch <= 32) return cudaLaunchKernelEx(&cfg, append_kernel<FMT, MODE, 1>, a);
+  if (nch <= 64) return cudaLaunchKernelEx(&cfg, append_kernel<FMT, MODE, 2>, a);
+  return cudaLaunchKernelEx(&cfg, append_kernel<FMT, MODE, 3>, a);
 }
 
 template <int FMT>

@@ -48,58 +48,54 @@ __device__ __forceinline__ int ld_i32(const int* p) { return *reinterpret_cast<c
 // (B*Hkv+1 ints).  Partial buffers follow at 256-byte aligned offsets.
 constexpr int kPlanHeader = 4;
 
-__device__ int block_scan_excl(int v, int* s, int* total) {
-  const int tid = threadIdx.x;
-  s[tid] = v;
-  __syncthreads();
-  for (int off = 1; off < 1024; off <<= 1) {
-    const int t = tid >= off ? s[tid - off] : 0;
-    __syncthreads();
-    s[tid] += t;
-    __syncthreads();
-  }
-  const int incl = s[tid];
-  *total = s[1023];
-  __syncthreads();
-  return incl - v;
-}
-
 __device__ __forceinline__ int clamp_len(int L, int cap) { return L < 0 ? 0 : (L > cap ? cap : L); }
 
-__global__ void __launch_bounds__(1024) plan_kernel(const int32_t* seq_lens, int B, int hkv, int bs,
-                                                    int max_blocks, int workers, int* ws,
-                                                    uint32_t* err) {
-  __shared__ int s[1024];
-  const int tid = threadIdx.x;
+__device__ __forceinline__ int warp_incl_scan(int x) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += t;
+  }
+  return x;
+}
+
+// One warp: unit prefix per request, units per worker, and the base index of
+// each (request, kv head)'s partials.  Lets the split kernel launch at once.
+__global__ void __launch_bounds__(32) plan_kernel(const int32_t* seq_lens, int B, int hkv, int bs,
+                                                  int max_blocks, int workers, int* ws,
+                                                  uint32_t* err) {
+  griddep_wait();  // inputs may come from the kernel before us in the stream
+  griddep_launch_dependents();
+  const int lane = threadIdx.x;
   const int cap = max_blocks * bs;
   int* uprefix = ws + kPlanHeader;
   int* segbase = uprefix + B + 1;
   int carry = 0;
-  for (int base = 0; base < B; base += 1024) {
-    const int b = base + tid;
+  for (int base = 0; base < B; base += 32) {
+    const int b = base + lane;
     int n = 0;
     if (b < B) {
       const int L = seq_lens[b];
       if (L < 0 || L > cap) raise_error(err, FP8PA_DEVERR_SEQ_LEN);
       n = (clamp_len(L, cap) + bs - 1) / bs;
     }
-    int tot;
-    const int ex = block_scan_excl(n, s, &tot);
-    if (b < B) uprefix[b] = (carry + ex) * hkv;
-    carry += tot;
+    const int incl = warp_incl_scan(n);
+    if (b < B) uprefix[b] = (carry + incl - n) * hkv;
+    carry += __shfl_sync(0xffffffffu, incl, 31);
   }
   const int U = carry * hkv;
   const int upw = max(1, (U + workers - 1) / workers);
-  if (tid == 0) {
+  if (lane == 0) {
     uprefix[B] = U;
     ws[0] = U;
     ws[1] = upw;
   }
-  __syncthreads();
+  __syncwarp();
   carry = 0;
   const int E = B * hkv;
-  for (int base = 0; base < E; base += 1024) {
-    const int e = base + tid;
+  for (int base = 0; base < E; base += 32) {
+    const int e = base + lane;
     int segs = 0;
     if (e < E) {
       const int b = e / hkv, kvh = e % hkv;
@@ -109,12 +105,11 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* seq_lens, int
         segs = (fu + nb - 1) / upw - fu / upw + 1;
       }
     }
-    int tot;
-    const int ex = block_scan_excl(segs, s, &tot);
-    if (e < E) segbase[e] = carry + ex;
-    carry += tot;
+    const int incl = warp_incl_scan(segs);
+    if (e < E) segbase[e] = carry + incl - segs;
+    carry += __shfl_sync(0xffffffffu, incl, 31);
   }
-  if (tid == 0) segbase[E] = carry;
+  if (lane == 0) segbase[E] = carry;
 }
 
 // ---------------------------------------------------------------- split kernel
@@ -186,14 +181,6 @@ __global__ void __launch_bounds__(kWarps * 32)
   int* okf =
       reinterpret_cast<int*>(smem + SM::kPages + SM::kScales + SM::kPs + SM::kBars) + warp * NST;
 
-  const int* uprefix = p.plan + kPlanHeader;
-  const int* segbase = uprefix + p.B + 1;
-  const int U = ld_i32(p.plan), upw = ld_i32(p.plan + 1);
-  const long wid = static_cast<long>(blockIdx.x) * kWarps + warp;
-  const long u0 = wid * upw;
-  if (u0 >= U) return;
-  const int n_units = static_cast<int>(min(static_cast<long>(upw), U - u0));
-
   if (lane == 0) {
     for (int s = 0; s < NST; ++s) mbar_init(&bars[s], 1);
     fence_barrier_init();
@@ -201,6 +188,16 @@ __global__ void __launch_bounds__(kWarps * 32)
     prefetch_tensormap(&tmv);
   }
   __syncwarp();
+  // Everything above overlaps the planner; the plan is read only after it.
+  griddep_wait();
+  griddep_launch_dependents();
+  const int* uprefix = p.plan + kPlanHeader;
+  const int* segbase = uprefix + p.B + 1;
+  const int U = ld_i32(p.plan), upw = ld_i32(p.plan + 1);
+  const long wid = static_cast<long>(blockIdx.x) * kWarps + warp;
+  const long u0 = wid * upw;
+  if (u0 >= U) return;
+  const int n_units = static_cast<int>(min(static_cast<long>(upw), U - u0));
 
   // ---- unit cursor: (request, kv head, page) of a flat unit index
   auto locate = [&](long u) {
@@ -250,6 +247,20 @@ __global__ void __launch_bounds__(kWarps * 32)
       }
     }
   };
+
+  // Per-thread byte offsets inside a page: the swizzle phase of every row a
+  // thread touches depends only on its lane, so they are fixed for the
+  // whole kernel (tile tt adds tt * 16 rows).
+  uint32_t koff[2][KCH], voff[4];
+#pragma unroll
+  for (int rr = 0; rr < 2; ++rr)
+#pragma unroll
+    for (int qq = 0; qq < KCH; ++qq) koff[rr][qq] = swz<D>(g + 8 * rr, c * KCH + qq);
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const int tau = 4 * c + ((u + c) & 3);
+    voff[u] = D == 128 ? swz<D>(tau, g) : swz<D>(tau, g >> 1) + 8 * (g & 1);
+  }
 
   Cursor cc = locate(u0);
   Cursor pc = cc;
@@ -357,25 +368,28 @@ __global__ void __launch_bounds__(kWarps * 32)
       uint32_t kw[2][KW];
 #pragma unroll
       for (int rr = 0; rr < 2; ++rr) {
-        const int R = r0 + g + 8 * rr;
 #pragma unroll
         for (int qq = 0; qq < KCH; ++qq) {
-          const uint4 x = lds128(kbase + swz<D>(R, c * KCH + qq));
+          const uint4 x = lds128(kbase + r0 * D + koff[rr][qq]);
           kw[rr][4 * qq] = x.x;
           kw[rr][4 * qq + 1] = x.y;
           kw[rr][4 * qq + 2] = x.z;
           kw[rr][4 * qq + 3] = x.w;
         }
       }
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      // two independent accumulator chains (even / odd k-steps)
+      float acc[4] = {0.f, 0.f, 0.f, 0.f}, acc2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int j = 0; j < KW; ++j) {
         const uint32_t a0 = fp8x2_to_f16x2<FMT>(kw[0][j]), a1 = fp8x2_to_f16x2<FMT>(kw[1][j]);
         const uint32_t a2 = fp8x2_to_f16x2<FMT>(kw[0][j] >> 16);
         const uint32_t a3 = fp8x2_to_f16x2<FMT>(kw[1][j] >> 16);
 #pragma unroll
-        for (int qp = 0; qp < QP; ++qp) mma_16816(acc, a0, a1, a2, a3, qb[qp][j][0], qb[qp][j][1]);
+        for (int qp = 0; qp < QP; ++qp)
+          mma_16816((j & 1) ? acc2 : acc, a0, a1, a2, a3, qb[qp][j][0], qb[qp][j][1]);
       }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[e] += acc2[e];
       const bool v0 = g < tv, v1 = g + 8 < tv;
       float sk0 = 1.f, sk1 = 1.f;
       if constexpr (TOKSC) {
@@ -429,12 +443,15 @@ __global__ void __launch_bounds__(kWarps * 32)
         q11 = p11 * 16384.f;
       }
       const float f0 = al0 * rs, f1 = al1 * rs;
+      // Once the running maxima settle the factors are exactly 1: skip.
+      if (__any_sync(0xffffffffu, f0 != 1.f || f1 != 1.f)) {
 #pragma unroll
-      for (int t = 0; t < MT; ++t) {
-        O[t][0] *= f0;
-        O[t][2] *= f0;
-        O[t][1] *= f1;
-        O[t][3] *= f1;
+        for (int t = 0; t < MT; ++t) {
+          O[t][0] *= f0;
+          O[t][2] *= f0;
+          O[t][1] *= f1;
+          O[t][3] *= f1;
+        }
       }
       // ---- P^T through shared memory into the B layout of the PV MMA.
       // Position 4c'+u of a head row holds token 4c' + ((u + c') & 3).
@@ -461,15 +478,14 @@ __global__ void __launch_bounds__(kWarps * 32)
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int tau = 4 * c + ((u + c) & 3);
-        const int R = r0 + tau;
         if constexpr (D == 128) {
-          const uint4 x = lds128(vbase + swz<D>(R, g));
+          const uint4 x = lds128(vbase + r0 * D + voff[u]);
           vw[u][0] = x.x;
           vw[u][1] = x.y;
           vw[u][2] = x.z;
           vw[u][3] = x.w;
         } else {
-          const uint2 x = lds64(vbase + swz<D>(R, g >> 1) + 8 * (g & 1));
+          const uint2 x = lds64(vbase + r0 * D + voff[u]);
           vw[u][0] = x.x;
           vw[u][1] = x.y;
         }
@@ -556,19 +572,27 @@ struct MergeParams {
   int B, hq, hkv, G, dv, out_f32;
 };
 
+// One CTA of kMergeWarps warps per output row (b, h): the warps share the
+// row's pieces round-robin, then combine through shared memory.
+constexpr int kMergeWarps = 4;
+
 template <int DV>
-__global__ void __launch_bounds__(256) merge_kernel(const MergeParams p) {
+__global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const MergeParams p) {
   constexpr int PER = DV / 32;
-  const int gw = blockIdx.x * 8 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (gw >= p.B * p.hq) return;
-  const int b = gw / p.hq, h = gw % p.hq;
+  __shared__ float s_acc[kMergeWarps][DV];
+  __shared__ float s_l[kMergeWarps];
+  griddep_wait();
+  griddep_launch_dependents();
+  const int row = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int b = row / p.hq, h = row % p.hq;
   const int kvh = h / p.G, hh = h % p.G;
   const int* segbase = p.plan + kPlanHeader + p.B + 1;
   const int sb = segbase[b * p.hkv + kvh], se = segbase[b * p.hkv + kvh + 1];
   const float NEG_INF = __int_as_float(0xff800000);
   float M = NEG_INF;
-  for (int s = sb + lane; s < se; s += 32) M = fmaxf(M, p.part_ml[(static_cast<long>(s) * p.G + hh) * 2]);
+  for (int s = sb + lane; s < se; s += 32)
+    M = fmaxf(M, p.part_ml[(static_cast<long>(s) * p.G + hh) * 2]);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
   float acc[PER];
@@ -576,20 +600,37 @@ __global__ void __launch_bounds__(256) merge_kernel(const MergeParams p) {
   for (int e = 0; e < PER; ++e) acc[e] = 0.f;
   float L = 0.f;
   if (M != NEG_INF) {
-    for (int s = sb; s < se; ++s) {
+#pragma unroll 4
+    for (int s = sb + warp; s < se; s += kMergeWarps) {
       const long r = static_cast<long>(s) * p.G + hh;
-      const float w = ex2(p.part_ml[r * 2] - M);
-      L += w * p.part_ml[r * 2 + 1];
-      const float* po = p.part_o + r * DV + lane * PER;
+      const float2 ml = *reinterpret_cast<const float2*>(p.part_ml + r * 2);
+      const float wgt = ex2(ml.x - M);
+      L += wgt * ml.y;
+      const float2* po = reinterpret_cast<const float2*>(p.part_o + r * DV + lane * PER);
 #pragma unroll
-      for (int e = 0; e < PER; e += 2) {
-        const float2 v = *reinterpret_cast<const float2*>(po + e);
-        acc[e] += w * v.x;
-        acc[e + 1] += w * v.y;
+      for (int e = 0; e < PER / 2; ++e) {
+        const float2 v = po[e];
+        acc[2 * e] += wgt * v.x;
+        acc[2 * e + 1] += wgt * v.y;
       }
     }
   }
-  const float inv = L > 0.f ? 1.0f / L : 0.f;
+#pragma unroll
+  for (int e = 0; e < PER; ++e) s_acc[warp][lane * PER + e] = acc[e];
+  if (lane == 0) s_l[warp] = L;
+  __syncthreads();
+  if (warp != 0) return;
+  float Lt = 0.f;
+#pragma unroll
+  for (int w = 0; w < kMergeWarps; ++w) Lt += s_l[w];
+#pragma unroll
+  for (int e = 0; e < PER; ++e) {
+    float v = 0.f;
+#pragma unroll
+    for (int w = 0; w < kMergeWarps; ++w) v += s_acc[w][lane * PER + e];
+    acc[e] = v;
+  }
+  const float inv = Lt > 0.f ? 1.0f / Lt : 0.f;
   const long ob = (static_cast<long>(b) * p.hq + h) * DV + lane * PER;
   if (p.out_f32) {
     float* o = reinterpret_cast<float*>(p.out) + ob;
@@ -608,7 +649,7 @@ __global__ void __launch_bounds__(256) merge_kernel(const MergeParams p) {
 template <int D, int BS>
 constexpr int stages_for() {
   constexpr int stage = 2 * BS * D;
-  constexpr int n = 16384 / stage;
+  constexpr int n = 12288 / stage;
   return n < 2 ? 2 : (n > 8 ? 8 : n);
 }
 
@@ -707,8 +748,22 @@ cudaError_t launch_decode_gqa(const DecodeShape& s, const DecodeArgs& a, cudaStr
   float* part_ml = reinterpret_cast<float*>(ws + plan_bytes);
   float* part_o = reinterpret_cast<float*>(ws + plan_bytes + align256(segs * G * 2 * sizeof(float)));
 
-  plan_kernel<<<1, 1024, 0, stream>>>(a.seq_lens, s.batch, s.hkv, s.bs, s.max_blocks, s.workers,
-                                      plan, a.err);
+  // Every kernel of the decode is launched with programmatic stream
+  // serialisation: it may start while its predecessor drains, and waits
+  // (griddepcontrol.wait) before reading anything that predecessor wrote.
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1);
+  cfg.blockDim = dim3(32);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cfg.attrs = pdl;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, plan_kernel, a.seq_lens, s.batch, s.hkv, s.bs, s.max_blocks,
+                         s.workers, plan, a.err);
+  if (e != cudaSuccess) return e;
   GqaParams p;
   p.q = a.q;
   p.k_scale = a.k_scale;
@@ -727,16 +782,23 @@ cudaError_t launch_decode_gqa(const DecodeShape& s, const DecodeArgs& a, cudaStr
   p.num_blocks = a.num_blocks;
   p.qk_scale_log2 = a.sm_scale * 1.4426950408889634f;
   const int ctas = (s.workers + kWarps - 1) / kWarps;
+  cfg.gridDim = dim3(ctas);
+  cfg.blockDim = dim3(kWarps * 32);
+  cfg.dynamicSmemBytes = k.smem;
   if (g_split_ev_start) cudaEventRecord(g_split_ev_start, stream);
-  k.fn<<<ctas, kWarps * 32, k.smem, stream>>>(tmk, tmv, p);
+  e = cudaLaunchKernelEx(&cfg, k.fn, tmk, tmv, p);
+  if (e != cudaSuccess) return e;
   if (g_split_ev_stop) cudaEventRecord(g_split_ev_stop, stream);
 
   MergeParams mp{plan, part_ml, part_o, a.out, s.batch, s.hq, s.hkv, G, s.dv, a.out_dtype};
-  const int mblocks = (s.batch * s.hq + 7) / 8;
+  cfg.gridDim = dim3(s.batch * s.hq);
+  cfg.blockDim = dim3(kMergeWarps * 32);
+  cfg.dynamicSmemBytes = 0;
   if (s.dv == 128)
-    merge_kernel<128><<<mblocks, 256, 0, stream>>>(mp);
+    e = cudaLaunchKernelEx(&cfg, merge_kernel<128>, mp);
   else
-    merge_kernel<64><<<mblocks, 256, 0, stream>>>(mp);
+    e = cudaLaunchKernelEx(&cfg, merge_kernel<64>, mp);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
