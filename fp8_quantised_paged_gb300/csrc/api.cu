@@ -109,7 +109,7 @@ DecodePath decode_path(int batch, int hq, int hkv, int d, int dv, int bs, int ma
   if (d == 576) {
     s.mla = 1;
     if (hkv != 1 || dv != 512 || mode != FP8PA_SCALE_TOKEN_GROUP || gs != 64 || bs != 64 ||
-        hq % 64 != 0)
+        hq % 32 != 0)
       r.status = FP8PA_ERR_UNSUPPORTED;
     return r;
   }

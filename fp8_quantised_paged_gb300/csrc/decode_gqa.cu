@@ -716,10 +716,11 @@ int decode_workers(const DecodeShape& s, int fmt, int mode, int device) {
 }
 
 size_t decode_workspace_bytes(const DecodeShape& s) {
-  const int G = s.hq / s.hkv;
+  const int groups = s.mla ? s.hq / 32 : s.hkv;
+  const int G = s.hq / groups;
   const size_t plan = align256(sizeof(int) * (kPlanHeader + (s.batch + 1) +
-                                               static_cast<size_t>(s.batch) * s.hkv + 1));
-  const size_t segs = static_cast<size_t>(s.workers) + static_cast<size_t>(s.batch) * s.hkv;
+                                               static_cast<size_t>(s.batch) * groups + 1));
+  const size_t segs = static_cast<size_t>(s.workers) + static_cast<size_t>(s.batch) * groups;
   const size_t ml = align256(segs * G * 2 * sizeof(float));
   const size_t o = align256(segs * G * static_cast<size_t>(s.dv) * sizeof(float));
   return plan + ml + o;
@@ -748,6 +749,8 @@ cudaError_t launch_decode_gqa(const DecodeShape& s, const DecodeArgs& a, cudaStr
   float* part_ml = reinterpret_cast<float*>(ws + plan_bytes);
   float* part_o = reinterpret_cast<float*>(ws + plan_bytes + align256(segs * G * 2 * sizeof(float)));
 
+  e = launch_plan(a.seq_lens, s.batch, s.hkv, s.bs, s.max_blocks, s.workers, plan, a.err, stream);
+  if (e != cudaSuccess) return e;
   // Every kernel of the decode is launched with programmatic stream
   // serialisation: it may start while its predecessor drains, and waits
   // (griddepcontrol.wait) before reading anything that predecessor wrote.
@@ -755,15 +758,9 @@ cudaError_t launch_decode_gqa(const DecodeShape& s, const DecodeArgs& a, cudaStr
   pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   pdl[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(1);
-  cfg.blockDim = dim3(32);
-  cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
   cfg.attrs = pdl;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, plan_kernel, a.seq_lens, s.batch, s.hkv, s.bs, s.max_blocks,
-                         s.workers, plan, a.err);
-  if (e != cudaSuccess) return e;
   GqaParams p;
   p.q = a.q;
   p.k_scale = a.k_scale;
@@ -790,14 +787,45 @@ cudaError_t launch_decode_gqa(const DecodeShape& s, const DecodeArgs& a, cudaStr
   if (e != cudaSuccess) return e;
   if (g_split_ev_stop) cudaEventRecord(g_split_ev_stop, stream);
 
-  MergeParams mp{plan, part_ml, part_o, a.out, s.batch, s.hq, s.hkv, G, s.dv, a.out_dtype};
-  cfg.gridDim = dim3(s.batch * s.hq);
+  return launch_merge(plan, part_ml, part_o, a.out, s.batch, s.hq, s.hkv, G, s.dv, a.out_dtype,
+                      stream);
+}
+
+cudaError_t launch_plan(const int32_t* seq_lens, int batch, int groups, int bs, int max_blocks,
+                        int workers, int* plan, uint32_t* err, cudaStream_t stream) {
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1);
+  cfg.blockDim = dim3(32);
+  cfg.stream = stream;
+  cfg.attrs = pdl;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, plan_kernel, seq_lens, batch, groups, bs, max_blocks, workers,
+                            plan, err);
+}
+
+cudaError_t launch_merge(const int* plan, const float* part_ml, const float* part_o, void* out,
+                         int batch, int hq, int groups, int G, int dv, int out_dtype,
+                         cudaStream_t stream) {
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(batch * hq);
   cfg.blockDim = dim3(kMergeWarps * 32);
-  cfg.dynamicSmemBytes = 0;
-  if (s.dv == 128)
+  cfg.stream = stream;
+  cfg.attrs = pdl;
+  cfg.numAttrs = 1;
+  MergeParams mp{plan, part_ml, part_o, out, batch, hq, groups, G, dv, out_dtype};
+  cudaError_t e;
+  if (dv == 128)
     e = cudaLaunchKernelEx(&cfg, merge_kernel<128>, mp);
-  else
+  else if (dv == 64)
     e = cudaLaunchKernelEx(&cfg, merge_kernel<64>, mp);
+  else
+    e = cudaLaunchKernelEx(&cfg, merge_kernel<512>, mp);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

@@ -47,6 +47,16 @@ struct DecodeArgs {
 };
 
 int decode_workers(const DecodeShape& s, int fmt, int mode, int device);
+
+// Shared by both kernel families: the planner (flat (request, group, page)
+// list cut into equal ranges) and the log-sum-exp merge of the pieces.
+// `groups` is the number of head groups per request (KV heads for GQA, groups
+// of 32 query heads for MLA) and G the query heads per group.
+cudaError_t launch_plan(const int32_t* seq_lens, int batch, int groups, int bs, int max_blocks,
+                        int workers, int* plan, uint32_t* err, cudaStream_t stream);
+cudaError_t launch_merge(const int* plan, const float* part_ml, const float* part_o, void* out,
+                         int batch, int hq, int groups, int G, int dv, int out_dtype,
+                         cudaStream_t stream);
 cudaError_t launch_decode_gqa(const DecodeShape& s, const DecodeArgs& a, cudaStream_t stream);
 cudaError_t launch_decode_mla(const DecodeShape& s, const DecodeArgs& a, cudaStream_t stream);
 

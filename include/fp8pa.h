@@ -155,7 +155,7 @@ size_t fp8pa_decode_workspace_bytes(int batch, int n_q_heads, int n_kv_heads, in
  *  MLA  n_kv_heads == 1, head_dim 576 (512 latent + 64 rope), head_dim_v
  *       512 (the first 512 dims of the same latent), v_cache == k_cache,
  *       v_scale == k_scale, scale_mode TOKEN_GROUP, group_size 64,
- *       block_size 64, n_q_heads a multiple of 64.
+ *       block_size 64, n_q_heads a multiple of 32.
  *
  * seq_lens     i32 [batch], including any token appended this step; 0 gives
  *              a zero output row.

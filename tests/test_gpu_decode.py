@@ -20,10 +20,10 @@ def F():
     F.set_decode_workers(0)
 
 
-GQA = [1, 2, 3, 4]
+ALL = [1, 2, 3, 4, 5]
 
 
-@pytest.mark.parametrize("idx", GQA)
+@pytest.mark.parametrize("idx", ALL)
 def test_decode_small_matches_oracle(F, idx):
     from gpu_util import check_close, gpu_attention, gpu_cache, oracle_attention, oracle_cache
     w = W.make_workload(idx, "small")
@@ -40,7 +40,7 @@ def test_decode_small_matches_oracle(F, idx):
     assert F.get_device_error() == 0
 
 
-@pytest.mark.parametrize("idx", [1, 3, 4])
+@pytest.mark.parametrize("idx", [1, 3, 4, 5])
 def test_decode_independent_of_split_count(F, idx):
     from gpu_util import check_close, gpu_attention, gpu_cache, oracle_attention, oracle_cache
     w = W.make_workload(idx, "small")
@@ -217,3 +217,8 @@ def test_full_ragged_e5m2_sampled(F):
     w = W.make_workload(4, "full")
     order = np.argsort(w.seq_lens)
     _full_size_sampled(F, 4, sample=(int(order[0]), int(order[len(order) // 2]), int(order[-1])))
+
+
+@pytest.mark.slow
+def test_full_mla_latent_sampled(F):
+    _full_size_sampled(F, 5, sample=(0, 31))
