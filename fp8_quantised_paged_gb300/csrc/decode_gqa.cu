@@ -570,6 +570,9 @@ struct MergeParams {
   const float* part_o;
   void* out;
   int B, hq, hkv, G, dv, out_f32;
+  // 0: pieces are numbered per (request, group) (GQA planner with KV heads as
+  // groups); 1: per request, with the group folded into the piece row (MLA).
+  int per_request;
 };
 
 // One CTA of kMergeWarps warps per output row (b, h): the warps share the
@@ -588,11 +591,16 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const MergePara
   const int b = row / p.hq, h = row % p.hq;
   const int kvh = h / p.G, hh = h % p.G;
   const int* segbase = p.plan + kPlanHeader + p.B + 1;
-  const int sb = segbase[b * p.hkv + kvh], se = segbase[b * p.hkv + kvh + 1];
+  const int e0 = p.per_request ? b : b * p.hkv + kvh;
+  const int sb = segbase[e0], se = segbase[e0 + 1];
+  // row of piece s for this head
+  auto prow = [&](int s) -> long {
+    return p.per_request ? (static_cast<long>(s) * p.hkv + kvh) * p.G + hh
+                         : static_cast<long>(s) * p.G + hh;
+  };
   const float NEG_INF = __int_as_float(0xff800000);
   float M = NEG_INF;
-  for (int s = sb + lane; s < se; s += 32)
-    M = fmaxf(M, p.part_ml[(static_cast<long>(s) * p.G + hh) * 2]);
+  for (int s = sb + lane; s < se; s += 32) M = fmaxf(M, p.part_ml[prow(s) * 2]);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
   float acc[PER];
@@ -602,7 +610,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const MergePara
   if (M != NEG_INF) {
 #pragma unroll 4
     for (int s = sb + warp; s < se; s += kMergeWarps) {
-      const long r = static_cast<long>(s) * p.G + hh;
+      const long r = prow(s);
       const float2 ml = *reinterpret_cast<const float2*>(p.part_ml + r * 2);
       const float wgt = ex2(ml.x - M);
       L += wgt * ml.y;
@@ -699,11 +707,16 @@ cudaEvent_t g_split_ev_start = nullptr, g_split_ev_stop = nullptr;
 
 // Split workers for the GQA kernel: one per resident warp slot.
 int decode_workers(const DecodeShape& s, int fmt, int mode, int device) {
-  if (g_decode_workers_override > 0) return g_decode_workers_override;
+  if (g_decode_workers_override > 0 && !s.mla) return g_decode_workers_override;
   int sms = 0;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess || sms <= 0)
     sms = 1;
-  if (s.mla) return sms;  // the shared-latent kernel decides per CTA
+  if (s.mla) {
+    // one 202 KB CTA per SM; a whole number of head-group sets (H = Hq / 32)
+    const int H = s.hq / 32;
+    int ranges = (g_decode_workers_override > 0 ? g_decode_workers_override : sms) / H;
+    return (ranges < 1 ? 1 : ranges) * H;
+  }
   const SplitKernel k = pick(s.d, s.bs, fmt, mode);
   cudaFuncSetAttribute(reinterpret_cast<const void*>(k.fn),
                        cudaFuncAttributeMaxDynamicSharedMemorySize, k.smem);
@@ -718,9 +731,11 @@ int decode_workers(const DecodeShape& s, int fmt, int mode, int device) {
 size_t decode_workspace_bytes(const DecodeShape& s) {
   const int groups = s.mla ? s.hq / 32 : s.hkv;
   const int G = s.hq / groups;
+  // MLA: pieces per request (ranges of pages) times head groups
   const size_t plan = align256(sizeof(int) * (kPlanHeader + (s.batch + 1) +
-                                               static_cast<size_t>(s.batch) * groups + 1));
-  const size_t segs = static_cast<size_t>(s.workers) + static_cast<size_t>(s.batch) * groups;
+                                               static_cast<size_t>(s.batch) * (s.mla ? 1 : groups) + 1));
+  const size_t segs = s.mla ? (static_cast<size_t>(s.workers / groups) + s.batch) * groups
+                            : static_cast<size_t>(s.workers) + static_cast<size_t>(s.batch) * groups;
   const size_t ml = align256(segs * G * 2 * sizeof(float));
   const size_t o = align256(segs * G * static_cast<size_t>(s.dv) * sizeof(float));
   return plan + ml + o;
@@ -788,7 +803,7 @@ cudaError_t launch_decode_gqa(const DecodeShape& s, const DecodeArgs& a, cudaStr
   if (g_split_ev_stop) cudaEventRecord(g_split_ev_stop, stream);
 
   return launch_merge(plan, part_ml, part_o, a.out, s.batch, s.hq, s.hkv, G, s.dv, a.out_dtype,
-                      stream);
+                      /*pieces_per_request=*/false, stream);
 }
 
 cudaError_t launch_plan(const int32_t* seq_lens, int batch, int groups, int bs, int max_blocks,
@@ -808,7 +823,7 @@ cudaError_t launch_plan(const int32_t* seq_lens, int batch, int groups, int bs, 
 
 cudaError_t launch_merge(const int* plan, const float* part_ml, const float* part_o, void* out,
                          int batch, int hq, int groups, int G, int dv, int out_dtype,
-                         cudaStream_t stream) {
+                         bool pieces_per_request, cudaStream_t stream) {
   cudaLaunchAttribute pdl[1];
   pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   pdl[0].val.programmaticStreamSerializationAllowed = 1;
@@ -818,7 +833,8 @@ cudaError_t launch_merge(const int* plan, const float* part_ml, const float* par
   cfg.stream = stream;
   cfg.attrs = pdl;
   cfg.numAttrs = 1;
-  MergeParams mp{plan, part_ml, part_o, out, batch, hq, groups, G, dv, out_dtype};
+  MergeParams mp{plan,      part_ml, part_o, out, batch, hq, groups, G, dv, out_dtype,
+                 pieces_per_request ? 1 : 0};
   cudaError_t e;
   if (dv == 128)
     e = cudaLaunchKernelEx(&cfg, merge_kernel<128>, mp);

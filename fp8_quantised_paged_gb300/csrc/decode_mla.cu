@@ -12,8 +12,10 @@
 // GB300 design.  128 heads x 576 dims against one latent per token is a real
 // dense contraction (~455 flop per cached byte), so the kernel is built around
 // the tensor cores:
-//  * Work = (request, group of 32 heads, 64-token page); the planner cuts the
-//    flat list into one contiguous range per CTA (one CTA per SM) and the
+//  * Work = (request, 64-token page); the planner cuts the flat page list into
+//    contiguous ranges, and each range is processed by H = Hq / 32 CTAs with
+//    adjacent block indices, one per group of 32 heads.  They run together, so
+//    a page comes from DRAM once and from L2 for the other head groups.  The
 //    merge kernel folds the partial pieces, as for the GQA layout.
 //  * A page (36,864 code bytes + 2,304 scale bytes) arrives by 1-D bulk copy
 //    into a two-stage ring; all 256 threads convert its codes once to exact f16
@@ -122,13 +124,14 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const MlaParams 
   const int* segbase = uprefix + p.B + 1;
   const int U = *reinterpret_cast<const volatile int*>(p.plan);
   const int upw = *reinterpret_cast<const volatile int*>(p.plan + 1);
-  const long wid = blockIdx.x;
+  const int H = p.ngroups_h;              // head groups per request
+  const int hg = blockIdx.x % H;          // this CTA's group of 32 heads
+  const long wid = blockIdx.x / H;        // its page range
   const long u0 = wid * upw;
   if (u0 >= U) return;
   const int n_units = static_cast<int>(min(static_cast<long>(upw), U - u0));
-  const int H = p.ngroups_h;  // head groups per request
 
-  // unit -> (request b, head group hg, page j)
+  // unit -> (request b, page j)
   struct Cur {
     int b, hg, j, nb;
   };
@@ -140,21 +143,18 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const MlaParams 
     }
     Cur cu;
     cu.b = lo;
-    cu.nb = (uprefix[lo + 1] - uprefix[lo]) / H;
-    const int local = static_cast<int>(u - uprefix[lo]);
-    cu.hg = local / cu.nb;
-    cu.j = local % cu.nb;
+    cu.nb = uprefix[lo + 1] - uprefix[lo];
+    cu.hg = hg;
+    cu.j = static_cast<int>(u - uprefix[lo]);
     return cu;
   };
   auto advance = [&](Cur& cu) {
     if (++cu.j < cu.nb) return;
     cu.j = 0;
-    if (++cu.hg < H) return;
-    cu.hg = 0;
     do {
       ++cu.b;
     } while (cu.b < p.B && uprefix[cu.b + 1] == uprefix[cu.b]);
-    if (cu.b < p.B) cu.nb = (uprefix[cu.b + 1] - uprefix[cu.b]) / H;
+    if (cu.b < p.B) cu.nb = uprefix[cu.b + 1] - uprefix[cu.b];
   };
   auto issue = [&](const Cur& cu, int s) {  // thread 0 only
     const int blk = __ldg(p.block_tables + static_cast<long>(cu.b) * p.max_blocks + cu.j);
@@ -437,8 +437,9 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const MlaParams 
         red[tq * kHeads + 16 * ht + g8 + 8] = l_h[1];
       }
       __syncthreads();
-      const int fu = uprefix[cc.b] + cc.hg * cc.nb;
-      const long seg = segbase[cc.b * H + cc.hg] + (wid - fu / upw);
+      // piece rows: (piece of request b) x head group x head
+      const int fu = uprefix[cc.b];
+      const long seg = (segbase[cc.b] + (wid - fu / upw)) * H + cc.hg;
       const float fin = exp2i(erun - 15);
 #pragma unroll
       for (int r = 0; r < 2; ++r) {
@@ -477,6 +478,7 @@ size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 // head groups of 32 in the role of KV heads.
 cudaError_t launch_decode_mla(const DecodeShape& s, const DecodeArgs& a, cudaStream_t stream) {
   const int H = s.hq / kHeads;
+  const int ranges = s.workers / H;
   const int smem = MlaSmem::kBytes;
   auto kfn = a.fmt == FP8PA_E4M3 ? mla_split_kernel<FP8PA_E4M3> : mla_split_kernel<FP8PA_E5M2>;
   cudaError_t e =
@@ -486,13 +488,13 @@ cudaError_t launch_decode_mla(const DecodeShape& s, const DecodeArgs& a, cudaStr
   char* ws = static_cast<char*>(a.workspace);
   int* plan = reinterpret_cast<int*>(ws);
   const size_t plan_bytes =
-      align256(sizeof(int) * (kPlanHeader + (s.batch + 1) + static_cast<size_t>(s.batch) * H + 1));
-  const size_t segs = static_cast<size_t>(s.workers) + static_cast<size_t>(s.batch) * H;
+      align256(sizeof(int) * (kPlanHeader + (s.batch + 1) + static_cast<size_t>(s.batch) + 1));
+  const size_t segs = (static_cast<size_t>(ranges) + s.batch) * H;
   float* part_ml = reinterpret_cast<float*>(ws + plan_bytes);
   float* part_o =
       reinterpret_cast<float*>(ws + plan_bytes + align256(segs * kHeads * 2 * sizeof(float)));
 
-  e = launch_plan(a.seq_lens, s.batch, H, kBs, s.max_blocks, s.workers, plan, a.err, stream);
+  e = launch_plan(a.seq_lens, s.batch, 1, kBs, s.max_blocks, ranges, plan, a.err, stream);
   if (e != cudaSuccess) return e;
   MlaParams p;
   p.q = a.q;
@@ -526,7 +528,7 @@ cudaError_t launch_decode_mla(const DecodeShape& s, const DecodeArgs& a, cudaStr
   if (e != cudaSuccess) return e;
   if (g_split_ev_stop) cudaEventRecord(g_split_ev_stop, stream);
   return launch_merge(plan, part_ml, part_o, a.out, s.batch, s.hq, H, kHeads, kDv, a.out_dtype,
-                      stream);
+                      /*pieces_per_request=*/true, stream);
 }
 
 }  // namespace fp8pa
