@@ -10,7 +10,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/fp8pa.h"
+#include "fp8pa.h"
 
 namespace fp8pa {
 
@@ -120,6 +120,23 @@ __device__ __forceinline__ uint32_t fp8x2_to_f16x2(uint32_t two_codes) {
     asm("cvt.rn.f16x2.e5m2x2 %0, %1;" : "=r"(r) : "h"(v));
   }
   return r;
+}
+
+// Four FP8 codes (byte i = element i) -> two f16x2: lo = elements 0,1 and
+// hi = elements 2,3; the two halves of the word are converted in place.
+template <int FMT>
+__device__ __forceinline__ void fp8x4_to_f16x2x2(uint32_t four_codes, uint32_t& lo, uint32_t& hi) {
+  if constexpr (FMT == FP8PA_E4M3) {
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(four_codes));
+  } else {
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+        "cvt.rn.f16x2.e5m2x2 %0, l;\n\tcvt.rn.f16x2.e5m2x2 %1, h;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(four_codes));
+  }
 }
 
 // Two fp32 values -> two FP8 codes (lo -> low byte), round to nearest even,

@@ -38,7 +38,7 @@ namespace fp8pa {
 
 namespace {
 
-constexpr int kWarps = 4;  // warps (= workers) per CTA
+constexpr int kMaxWarps = 8;  // warps per CTA: one per KV head of the CTA's head set
 
 __device__ __forceinline__ int ld_i32(const int* p) { return *reinterpret_cast<const volatile int*>(p); }
 
@@ -127,15 +127,18 @@ struct GqaParams {
   float qk_scale_log2;
 };
 
+// Shared-memory layout for `w` warps (each with its own NST-stage ring).
 template <int D, int BS, int NST>
 struct GqaSmem {
   static constexpr int kPage = BS * D;
-  static constexpr int kPages = kWarps * NST * 2 * kPage;
-  static constexpr int kScales = kWarps * NST * 2 * BS * 4;
-  static constexpr int kPs = kWarps * 512;
-  static constexpr int kBars = kWarps * NST * 8;
-  static constexpr int kOk = kWarps * NST * 4;
-  static constexpr int kBytes = kPages + kScales + kPs + kBars + kOk + 1024;
+  __host__ __device__ static constexpr int pages(int w) { return w * NST * 2 * kPage; }
+  __host__ __device__ static constexpr int scales(int w) { return w * NST * 2 * BS * 4; }
+  __host__ __device__ static constexpr int ps(int w) { return w * 512; }
+  __host__ __device__ static constexpr int bars(int w) { return w * NST * 8; }
+  __host__ __device__ static constexpr int oks(int w) { return w * NST * 4; }
+  __host__ __device__ static constexpr int bytes(int w) {
+    return pages(w) + scales(w) + ps(w) + bars(w) + oks(w) + 1024;
+  }
 };
 
 // Byte offset of 16-byte chunk `ch` of row `r` in a TMA box written with the
@@ -150,11 +153,11 @@ __device__ __forceinline__ uint32_t swz(int r, int ch) {
 }
 
 struct Cursor {
-  int b, kvh, j, nb;
+  int b, j, nb;
 };
 
 template <int D, int BS, int FMT, int MODE, int NST>
-__global__ void __launch_bounds__(kWarps * 32)
+__global__ void __launch_bounds__(kMaxWarps * 32)
     gqa_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                      const GqaParams p) {
   using SM = GqaSmem<D, BS, NST>;
@@ -172,14 +175,15 @@ __global__ void __launch_bounds__(kWarps * 32)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
+  const int W = blockDim.x >> 5;  // warps in this CTA
   uint8_t* pages = smem + warp * (NST * 2 * PAGE);
-  float* scl = reinterpret_cast<float*>(smem + SM::kPages) + warp * (NST * 2 * BS);
+  float* scl = reinterpret_cast<float*>(smem + SM::pages(W)) + warp * (NST * 2 * BS);
   // P^T for the PV MMA as two f16 planes (hi + lo carry ~22 significant bits)
-  uint16_t* ps = reinterpret_cast<uint16_t*>(smem + SM::kPages + SM::kScales) + warp * 256;
+  uint16_t* ps = reinterpret_cast<uint16_t*>(smem + SM::pages(W) + SM::scales(W)) + warp * 256;
   uint64_t* bars =
-      reinterpret_cast<uint64_t*>(smem + SM::kPages + SM::kScales + SM::kPs) + warp * NST;
-  int* okf =
-      reinterpret_cast<int*>(smem + SM::kPages + SM::kScales + SM::kPs + SM::kBars) + warp * NST;
+      reinterpret_cast<uint64_t*>(smem + SM::pages(W) + SM::scales(W) + SM::ps(W)) + warp * NST;
+  int* okf = reinterpret_cast<int*>(smem + SM::pages(W) + SM::scales(W) + SM::ps(W) +
+                                    SM::bars(W)) + warp * NST;
 
   if (lane == 0) {
     for (int s = 0; s < NST; ++s) mbar_init(&bars[s], 1);
@@ -194,12 +198,17 @@ __global__ void __launch_bounds__(kWarps * 32)
   const int* uprefix = p.plan + kPlanHeader;
   const int* segbase = uprefix + p.B + 1;
   const int U = ld_i32(p.plan), upw = ld_i32(p.plan + 1);
-  const long wid = static_cast<long>(blockIdx.x) * kWarps + warp;
+  // CTA = (page range, set of W KV heads); warp = one KV head.  All warps of
+  // a CTA walk the same pages, so together they read a block's adjacent
+  // per-head slices.
+  const int hsets = p.hkv / W;
+  const long wid = blockIdx.x / hsets;                  // page range
+  const int kvh = (blockIdx.x % hsets) * W + warp;      // this warp's KV head
   const long u0 = wid * upw;
   if (u0 >= U) return;
   const int n_units = static_cast<int>(min(static_cast<long>(upw), U - u0));
 
-  // ---- unit cursor: (request, kv head, page) of a flat unit index
+  // ---- unit cursor: (request, page) of a flat page index
   auto locate = [&](long u) {
     int lo = 0, hi = p.B;
     while (hi - lo > 1) {
@@ -208,21 +217,17 @@ __global__ void __launch_bounds__(kWarps * 32)
     }
     Cursor cu;
     cu.b = lo;
-    cu.nb = (uprefix[lo + 1] - uprefix[lo]) / p.hkv;
-    const int local = static_cast<int>(u - uprefix[lo]);
-    cu.kvh = local / cu.nb;
-    cu.j = local % cu.nb;
+    cu.nb = uprefix[lo + 1] - uprefix[lo];
+    cu.j = static_cast<int>(u - uprefix[lo]);
     return cu;
   };
   auto advance = [&](Cursor& cu) {
     if (++cu.j < cu.nb) return;
     cu.j = 0;
-    if (++cu.kvh < p.hkv) return;
-    cu.kvh = 0;
     do {
       ++cu.b;
     } while (cu.b < p.B && uprefix[cu.b + 1] == uprefix[cu.b]);
-    if (cu.b < p.B) cu.nb = (uprefix[cu.b + 1] - uprefix[cu.b]) / p.hkv;
+    if (cu.b < p.B) cu.nb = uprefix[cu.b + 1] - uprefix[cu.b];
   };
   auto block_of = [&](const Cursor& cu) {
     return __ldg(p.block_tables + static_cast<long>(cu.b) * p.max_blocks + cu.j);
@@ -233,7 +238,7 @@ __global__ void __launch_bounds__(kWarps * 32)
       const bool ok = blk >= 0 && blk < p.num_blocks;
       okf[s] = ok ? 1 : 0;
       if (ok) {
-        const int row = (blk * p.hkv + cu.kvh) * BS;
+        const int row = (blk * p.hkv + kvh) * BS;
         mbar_arrive_expect_tx(&bars[s], TX);
         tma_load_2d(pages + s * 2 * PAGE, &tmk, 0, row, &bars[s]);
         tma_load_2d(pages + s * 2 * PAGE + PAGE, &tmv, 0, row, &bars[s]);
@@ -274,7 +279,6 @@ __global__ void __launch_bounds__(kWarps * 32)
       if (ip + 1 < n_units) pblk = block_of(pc);
     }
   }
-
   // ---- per-segment state.  Q enters the MMA as f16; with static channel
   // scales folded in it is no longer exact in f16, so it is split into a
   // high and a low f16 part and the contraction runs twice.
@@ -293,7 +297,7 @@ __global__ void __launch_bounds__(kWarps * 32)
     if (i == 0 || cc.j == 0) {
       // ---- new segment: load q for the G heads of (b, kv head)
       Lb = clamp_len(__ldg(p.seq_lens + cc.b), p.max_blocks * BS);
-      const int h = cc.kvh * p.G + g;
+      const int h = kvh * p.G + g;
       float qv[D / 4];
       if (g < p.G) {
         const uint4* src = reinterpret_cast<const uint4*>(
@@ -309,7 +313,7 @@ __global__ void __launch_bounds__(kWarps * 32)
           }
         }
         if constexpr (!TOKSC) {
-          const float* ksc = p.k_scale + cc.kvh * D + c * (D / 4);
+          const float* ksc = p.k_scale + kvh * D + c * (D / 4);
 #pragma unroll
           for (int e = 0; e < D / 4; ++e) qv[e] *= __ldg(ksc + e);
         }
@@ -364,6 +368,7 @@ __global__ void __launch_bounds__(kWarps * 32)
       const int r0 = tt * 16;
       if (r0 >= valid) break;
       const int tv = valid - r0;
+      const bool full = tv >= 16;  // warp-uniform
       // ---- S^T = K . Q^T : rows = tokens (g, g+8), cols = heads (2c, 2c+1)
       uint32_t kw[2][KW];
 #pragma unroll
@@ -377,25 +382,27 @@ __global__ void __launch_bounds__(kWarps * 32)
           kw[rr][4 * qq + 3] = x.w;
         }
       }
+      const bool v0 = full || g < tv, v1 = full || g + 8 < tv;
+      float sk0 = 1.f, sk1 = 1.f, sv0 = 1.f, sv1 = 1.f;
+      if constexpr (TOKSC) {
+        sk0 = sks[r0 + g];
+        sk1 = sks[r0 + g + 8];
+        sv0 = v0 ? svs[r0 + g] : 0.f;
+        sv1 = v1 ? svs[r0 + g + 8] : 0.f;
+      }
       // two independent accumulator chains (even / odd k-steps)
       float acc[4] = {0.f, 0.f, 0.f, 0.f}, acc2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int j = 0; j < KW; ++j) {
-        const uint32_t a0 = fp8x2_to_f16x2<FMT>(kw[0][j]), a1 = fp8x2_to_f16x2<FMT>(kw[1][j]);
-        const uint32_t a2 = fp8x2_to_f16x2<FMT>(kw[0][j] >> 16);
-        const uint32_t a3 = fp8x2_to_f16x2<FMT>(kw[1][j] >> 16);
+        uint32_t a0, a1, a2, a3;
+        fp8x4_to_f16x2x2<FMT>(kw[0][j], a0, a2);
+        fp8x4_to_f16x2x2<FMT>(kw[1][j], a1, a3);
 #pragma unroll
         for (int qp = 0; qp < QP; ++qp)
           mma_16816((j & 1) ? acc2 : acc, a0, a1, a2, a3, qb[qp][j][0], qb[qp][j][1]);
       }
 #pragma unroll
       for (int e = 0; e < 4; ++e) acc[e] += acc2[e];
-      const bool v0 = g < tv, v1 = g + 8 < tv;
-      float sk0 = 1.f, sk1 = 1.f;
-      if constexpr (TOKSC) {
-        sk0 = sks[r0 + g];
-        sk1 = sks[r0 + g + 8];
-      }
       const float z00 = v0 ? acc[0] * (zs * sk0) : NEG_INF;
       const float z01 = v0 ? acc[1] * (zs * sk0) : NEG_INF;
       const float z10 = v1 ? acc[2] * (zs * sk1) : NEG_INF;
@@ -421,8 +428,6 @@ __global__ void __launch_bounds__(kWarps * 32)
       // ---- fold the V scale into P, normalised by a running power of two
       float rs = 1.f, q00, q01, q10, q11;
       if constexpr (TOKSC) {
-        const float sv0 = v0 ? svs[r0 + g] : 0.f;
-        const float sv1 = v1 ? svs[r0 + g + 8] : 0.f;
         float svm = fmaxf(sv0, sv1);
 #pragma unroll
         for (int o = 4; o < 32; o <<= 1) svm = fmaxf(svm, __shfl_xor_sync(0xffffffffu, svm, o));
@@ -462,18 +467,25 @@ __global__ void __launch_bounds__(kWarps * 32)
         const int pos1 = 4 * (t1 >> 2) + (((t1 & 3) - (t1 >> 2)) & 3);
         const int idx[4] = {(2 * c) * 16 + pos0, (2 * c + 1) * 16 + pos0, (2 * c) * 16 + pos1,
                             (2 * c + 1) * 16 + pos1};
-        const float val[4] = {q00, q01, q10, q11};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const __half hi = __float2half_rn(val[e]);
-          ps[idx[e]] = __half_as_ushort(hi);
-          ps[128 + idx[e]] = __half_as_ushort(__float2half_rn(val[e] - __half2float(hi)));
-        }
+        // hi = f16(x), lo = f16(x - hi), two values per conversion
+        const __half2 h01 = __floats2half2_rn(q00, q01), h23 = __floats2half2_rn(q10, q11);
+        const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
+        const __half2 l01 = __floats2half2_rn(q00 - f01.x, q01 - f01.y);
+        const __half2 l23 = __floats2half2_rn(q10 - f23.x, q11 - f23.y);
+        ps[idx[0]] = __half_as_ushort(__low2half(h01));
+        ps[idx[1]] = __half_as_ushort(__high2half(h01));
+        ps[idx[2]] = __half_as_ushort(__low2half(h23));
+        ps[idx[3]] = __half_as_ushort(__high2half(h23));
+        ps[128 + idx[0]] = __half_as_ushort(__low2half(l01));
+        ps[128 + idx[1]] = __half_as_ushort(__high2half(l01));
+        ps[128 + idx[2]] = __half_as_ushort(__low2half(l23));
+        ps[128 + idx[3]] = __half_as_ushort(__high2half(l23));
       }
       __syncwarp();
       const uint2 pb = lds64(smem_u32(ps + g * 16 + 4 * c));
       const uint2 pl = lds64(smem_u32(ps + 128 + g * 16 + 4 * c));
-      // ---- O^T += V^T . P^T : rows = dv, cols = heads
+      // ---- O^T += V^T . P^T : rows = dv, cols = heads (V token order
+      // rotated per lane for conflict-free reads)
       uint32_t vw[4][VW];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
@@ -489,7 +501,7 @@ __global__ void __launch_bounds__(kWarps * 32)
           vw[u][0] = x.x;
           vw[u][1] = x.y;
         }
-        if (tau >= tv) {
+        if (!full && tau >= tv) {
 #pragma unroll
           for (int e = 0; e < VW; ++e) vw[u][e] = 0u;
         }
@@ -499,8 +511,9 @@ __global__ void __launch_bounds__(kWarps * 32)
         const uint32_t sel = (t & 1) ? 0x7362u : 0x5140u;
         const uint32_t x01 = prmt(vw[0][t >> 1], vw[1][t >> 1], sel);
         const uint32_t x23 = prmt(vw[2][t >> 1], vw[3][t >> 1], sel);
-        const uint32_t a0 = fp8x2_to_f16x2<FMT>(x01), a1 = fp8x2_to_f16x2<FMT>(x01 >> 16);
-        const uint32_t a2 = fp8x2_to_f16x2<FMT>(x23), a3 = fp8x2_to_f16x2<FMT>(x23 >> 16);
+        uint32_t a0, a1, a2, a3;
+        fp8x4_to_f16x2x2<FMT>(x01, a0, a1);
+        fp8x4_to_f16x2x2<FMT>(x23, a2, a3);
         mma_16816(O[t], a0, a1, a2, a3, pb.x, pb.y);
         mma_16816(O[t], a0, a1, a2, a3, pl.x, pl.y);
       }
@@ -522,8 +535,8 @@ __global__ void __launch_bounds__(kWarps * 32)
         l0 += __shfl_xor_sync(0xffffffffu, l0, o);
         l1 += __shfl_xor_sync(0xffffffffu, l1, o);
       }
-      const int fu = uprefix[cc.b] + cc.kvh * cc.nb;
-      const long seg = segbase[cc.b * p.hkv + cc.kvh] + (wid - fu / upw);
+      // piece rows: (piece of request b) x KV head x query head of the group
+      const long seg = (segbase[cc.b] + (wid - uprefix[cc.b] / upw)) * p.hkv + kvh;
       const float fin = TOKSC ? exp2i(erun - 15) : (1.0f / 16384.f);
 #pragma unroll
       for (int hsel = 0; hsel < 2; ++hsel) {
@@ -537,7 +550,7 @@ __global__ void __launch_bounds__(kWarps * 32)
         }
         const int dv0 = (D / 8) * g;
         if constexpr (!TOKSC) {
-          const float* vsc = p.v_scale + cc.kvh * D + dv0;
+          const float* vsc = p.v_scale + kvh * D + dv0;
 #pragma unroll
           for (int e = 0; e < D / 8; ++e) vals[e] *= __ldg(vsc + e);
         }
@@ -665,13 +678,15 @@ using SplitFn = void (*)(const CUtensorMap, const CUtensorMap, const GqaParams);
 
 struct SplitKernel {
   SplitFn fn;
-  int smem;
+  int per_warp;  // shared-memory bytes per warp (the CTA adds 1024 for alignment)
+  int smem(int w) const { return w * per_warp + 1024; }
 };
 
 template <int D, int BS, int FMT, int MODE>
 SplitKernel pick4() {
   constexpr int NST = stages_for<D, BS>();
-  return {gqa_split_kernel<D, BS, FMT, MODE, NST>, GqaSmem<D, BS, NST>::kBytes};
+  using SM = GqaSmem<D, BS, NST>;
+  return {gqa_split_kernel<D, BS, FMT, MODE, NST>, SM::bytes(1) - 1024};
 }
 
 template <int D, int BS, int FMT>
@@ -700,14 +715,17 @@ SplitKernel pick(int d, int bs, int fmt, int mode) {
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
+// Warps per CTA (one per KV head of the CTA's head set) and head sets.
+int gqa_wpc(int hkv) { return hkv <= kMaxWarps ? hkv : kMaxWarps; }
+
 }  // namespace
 
 int g_decode_workers_override = 0;
 cudaEvent_t g_split_ev_start = nullptr, g_split_ev_stop = nullptr;
 
-// Split workers for the GQA kernel: one per resident warp slot.
+// Number of page ranges the planner cuts (GQA: one per resident CTA over the
+// head sets; MLA: one per SM over the head groups, times the head groups).
 int decode_workers(const DecodeShape& s, int fmt, int mode, int device) {
-  if (g_decode_workers_override > 0 && !s.mla) return g_decode_workers_override;
   int sms = 0;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess || sms <= 0)
     sms = 1;
@@ -717,35 +735,41 @@ int decode_workers(const DecodeShape& s, int fmt, int mode, int device) {
     int ranges = (g_decode_workers_override > 0 ? g_decode_workers_override : sms) / H;
     return (ranges < 1 ? 1 : ranges) * H;
   }
+  if (g_decode_workers_override > 0) return g_decode_workers_override;
+  const int wpc = gqa_wpc(s.hkv), hsets = s.hkv / wpc;
   const SplitKernel k = pick(s.d, s.bs, fmt, mode);
   cudaFuncSetAttribute(reinterpret_cast<const void*>(k.fn),
-                       cudaFuncAttributeMaxDynamicSharedMemorySize, k.smem);
+                       cudaFuncAttributeMaxDynamicSharedMemorySize, k.smem(wpc));
   int per_sm = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, reinterpret_cast<const void*>(k.fn),
-                                                    kWarps * 32, k.smem) != cudaSuccess ||
+                                                    wpc * 32, k.smem(wpc)) != cudaSuccess ||
       per_sm <= 0)
     per_sm = 1;
-  return sms * per_sm * kWarps;
+  const int ranges = sms * per_sm / hsets;
+  return ranges < 1 ? 1 : ranges;
 }
 
+// Pieces are numbered per request (the planner runs over pages only) and
+// each piece holds one row per head group (KV head for GQA, 32-head group for
+// MLA) and query head of the group.
 size_t decode_workspace_bytes(const DecodeShape& s) {
   const int groups = s.mla ? s.hq / 32 : s.hkv;
   const int G = s.hq / groups;
-  // MLA: pieces per request (ranges of pages) times head groups
-  const size_t plan = align256(sizeof(int) * (kPlanHeader + (s.batch + 1) +
-                                               static_cast<size_t>(s.batch) * (s.mla ? 1 : groups) + 1));
-  const size_t segs = s.mla ? (static_cast<size_t>(s.workers / groups) + s.batch) * groups
-                            : static_cast<size_t>(s.workers) + static_cast<size_t>(s.batch) * groups;
-  const size_t ml = align256(segs * G * 2 * sizeof(float));
-  const size_t o = align256(segs * G * static_cast<size_t>(s.dv) * sizeof(float));
+  const size_t ranges = s.mla ? static_cast<size_t>(s.workers / groups) : s.workers;
+  const size_t plan = align256(sizeof(int) * (kPlanHeader + 2 * (s.batch + 1)));
+  const size_t rows = (ranges + s.batch) * groups * G;
+  const size_t ml = align256(rows * 2 * sizeof(float));
+  const size_t o = align256(rows * static_cast<size_t>(s.dv) * sizeof(float));
   return plan + ml + o;
 }
 
 cudaError_t launch_decode_gqa(const DecodeShape& s, const DecodeArgs& a, cudaStream_t stream) {
   const int G = s.hq / s.hkv;
+  const int wpc = gqa_wpc(s.hkv), hsets = s.hkv / wpc;
   const SplitKernel k = pick(s.d, s.bs, a.fmt, a.mode);
+  const int smem = k.smem(wpc);
   cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(k.fn),
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, k.smem);
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
 
   CUtensorMap tmk, tmv;
@@ -758,13 +782,12 @@ cudaError_t launch_decode_gqa(const DecodeShape& s, const DecodeArgs& a, cudaStr
 
   char* ws = static_cast<char*>(a.workspace);
   int* plan = reinterpret_cast<int*>(ws);
-  const size_t plan_bytes = align256(sizeof(int) * (kPlanHeader + (s.batch + 1) +
-                                                     static_cast<size_t>(s.batch) * s.hkv + 1));
-  const size_t segs = static_cast<size_t>(s.workers) + static_cast<size_t>(s.batch) * s.hkv;
+  const size_t plan_bytes = align256(sizeof(int) * (kPlanHeader + 2 * (s.batch + 1)));
+  const size_t prow = (static_cast<size_t>(s.workers) + s.batch) * s.hkv * G;
   float* part_ml = reinterpret_cast<float*>(ws + plan_bytes);
-  float* part_o = reinterpret_cast<float*>(ws + plan_bytes + align256(segs * G * 2 * sizeof(float)));
+  float* part_o = reinterpret_cast<float*>(ws + plan_bytes + align256(prow * 2 * sizeof(float)));
 
-  e = launch_plan(a.seq_lens, s.batch, s.hkv, s.bs, s.max_blocks, s.workers, plan, a.err, stream);
+  e = launch_plan(a.seq_lens, s.batch, 1, s.bs, s.max_blocks, s.workers, plan, a.err, stream);
   if (e != cudaSuccess) return e;
   // Every kernel of the decode is launched with programmatic stream
   // serialisation: it may start while its predecessor drains, and waits
@@ -793,17 +816,16 @@ cudaError_t launch_decode_gqa(const DecodeShape& s, const DecodeArgs& a, cudaStr
   p.max_blocks = s.max_blocks;
   p.num_blocks = a.num_blocks;
   p.qk_scale_log2 = a.sm_scale * 1.4426950408889634f;
-  const int ctas = (s.workers + kWarps - 1) / kWarps;
-  cfg.gridDim = dim3(ctas);
-  cfg.blockDim = dim3(kWarps * 32);
-  cfg.dynamicSmemBytes = k.smem;
+  cfg.gridDim = dim3(static_cast<unsigned>(s.workers) * hsets);
+  cfg.blockDim = dim3(wpc * 32);
+  cfg.dynamicSmemBytes = smem;
   if (g_split_ev_start) cudaEventRecord(g_split_ev_start, stream);
   e = cudaLaunchKernelEx(&cfg, k.fn, tmk, tmv, p);
   if (e != cudaSuccess) return e;
   if (g_split_ev_stop) cudaEventRecord(g_split_ev_stop, stream);
 
   return launch_merge(plan, part_ml, part_o, a.out, s.batch, s.hq, s.hkv, G, s.dv, a.out_dtype,
-                      /*pieces_per_request=*/false, stream);
+                      /*pieces_per_request=*/true, stream);
 }
 
 cudaError_t launch_plan(const int32_t* seq_lens, int batch, int groups, int bs, int max_blocks,

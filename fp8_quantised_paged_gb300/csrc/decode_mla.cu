@@ -487,12 +487,10 @@ cudaError_t launch_decode_mla(const DecodeShape& s, const DecodeArgs& a, cudaStr
   if (e != cudaSuccess) return e;
   char* ws = static_cast<char*>(a.workspace);
   int* plan = reinterpret_cast<int*>(ws);
-  const size_t plan_bytes =
-      align256(sizeof(int) * (kPlanHeader + (s.batch + 1) + static_cast<size_t>(s.batch) + 1));
-  const size_t segs = (static_cast<size_t>(ranges) + s.batch) * H;
+  const size_t plan_bytes = align256(sizeof(int) * (kPlanHeader + 2 * (s.batch + 1)));
+  const size_t rows = (static_cast<size_t>(ranges) + s.batch) * H * kHeads;
   float* part_ml = reinterpret_cast<float*>(ws + plan_bytes);
-  float* part_o =
-      reinterpret_cast<float*>(ws + plan_bytes + align256(segs * kHeads * 2 * sizeof(float)));
+  float* part_o = reinterpret_cast<float*>(ws + plan_bytes + align256(rows * 2 * sizeof(float)));
 
   e = launch_plan(a.seq_lens, s.batch, 1, kBs, s.max_blocks, ranges, plan, a.err, stream);
   if (e != cudaSuccess) return e;
