@@ -22,7 +22,8 @@ from . import _native as N
 from ._native import (E4M3, E5M2, OUT_BF16, OUT_F32, SCALE_CHANNEL_STATIC, SCALE_TOKEN_GROUP,
                       SCALE_TOKEN_HEAD, Fp8paError)
 
-__all__ = ["kv_append_quant", "kv_channel_scales", "paged_decode_attention",
+__all__ = ["kv_append_quant", "kv_channel_scales", "kv_channel_absmax_update",
+           "kv_scales_from_absmax", "paged_decode_attention",
            "decode_workspace_bytes", "get_device_error", "set_decode_workers", "version",
            "E4M3", "E5M2", "SCALE_TOKEN_HEAD", "SCALE_CHANNEL_STATIC", "SCALE_TOKEN_GROUP",
            "OUT_BF16", "OUT_F32", "Fp8paError"]
@@ -91,6 +92,32 @@ def kv_channel_scales(x, fmt=E5M2, out=None, stream=None):
     with torch.cuda.device(x.device):
         rc = N.lib.fp8pa_kv_channel_scales(_ptr(x), n, hkv, d, fmt, _ptr(out), _stream(stream))
     N.check(rc, "kv_channel_scales")
+    return out
+
+
+def kv_channel_absmax_update(x, running_absmax, stream=None):
+    """Fold a prefill batch x (bf16 [N, Hkv, D]) into a running per-channel
+    absmax (float32 [Hkv, D], zero-initialised by the caller)."""
+    _need(x, torch.bfloat16, "x")
+    _need(running_absmax, torch.float32, "running_absmax", x.device)
+    n, hkv, d = x.shape
+    with torch.cuda.device(x.device):
+        rc = N.lib.fp8pa_kv_channel_absmax_update(_ptr(x), n, hkv, d, _ptr(running_absmax),
+                                                  _stream(stream))
+    N.check(rc, "kv_channel_absmax_update")
+    return running_absmax
+
+
+def kv_scales_from_absmax(absmax, fmt=E5M2, out=None, stream=None):
+    """Static scales max(absmax / FMAX, 1e-12) from a running absmax."""
+    _need(absmax, torch.float32, "absmax")
+    if out is None:
+        out = torch.empty_like(absmax)
+    _need(out, torch.float32, "out", absmax.device)
+    with torch.cuda.device(absmax.device):
+        rc = N.lib.fp8pa_kv_scales_from_absmax(_ptr(absmax), absmax.numel(), fmt, _ptr(out),
+                                               _stream(stream))
+    N.check(rc, "kv_scales_from_absmax")
     return out
 
 

@@ -205,6 +205,26 @@ int fp8pa_kv_channel_scales(const void* x, int num_tokens, int n_kv_heads, int h
                                            static_cast<cudaStream_t>(stream)));
 }
 
+int fp8pa_kv_channel_absmax_update(const void* x, int num_tokens, int n_kv_heads, int head_dim,
+                                   float* running_absmax, void* stream) {
+  if (num_tokens < 0 || n_kv_heads <= 0 || head_dim <= 0) return FP8PA_ERR_BAD_SHAPE;
+  if (head_dim % 16 != 0) return FP8PA_ERR_UNSUPPORTED;
+  if (!running_absmax || (num_tokens > 0 && !x)) return FP8PA_ERR_NULL_POINTER;
+  if ((num_tokens > 0 && !aligned16(x)) || !aligned16(running_absmax)) return FP8PA_ERR_ALIGNMENT;
+  return cuda_status(launch_channel_absmax(static_cast<const uint16_t*>(x), num_tokens,
+                                           n_kv_heads * head_dim, running_absmax,
+                                           static_cast<cudaStream_t>(stream)));
+}
+
+int fp8pa_kv_scales_from_absmax(const float* absmax, int n, int fmt, float* scale_out,
+                                void* stream) {
+  if (n <= 0) return FP8PA_ERR_BAD_SHAPE;
+  if (fmt != FP8PA_E4M3 && fmt != FP8PA_E5M2) return FP8PA_ERR_BAD_ENUM;
+  if (!absmax || !scale_out) return FP8PA_ERR_NULL_POINTER;
+  return cuda_status(
+      launch_scales_from_absmax(absmax, n, fmt, scale_out, static_cast<cudaStream_t>(stream)));
+}
+
 size_t fp8pa_decode_workspace_bytes(int batch, int n_q_heads, int n_kv_heads, int head_dim,
                                     int head_dim_v, int block_size, int max_blocks_per_seq) {
   const int mode = head_dim == 576 ? FP8PA_SCALE_TOKEN_GROUP : FP8PA_SCALE_TOKEN_HEAD;

@@ -179,11 +179,10 @@ __global__ void __launch_bounds__(256) chanmax_kernel(const uint16_t* x, int n, 
 }
 
 template <int FMT>
-__global__ void chanscale_finalize_kernel(float* s, int hd) {
+__global__ void chanscale_finalize_kernel(const float* amax, float* s, int hd) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= hd) return;
-  const float amax = s[i];
-  s[i] = fmaxf(__fdiv_rn(amax, fp8_max<FMT>()), 1e-12f);
+  s[i] = fmaxf(__fdiv_rn(amax[i], fp8_max<FMT>()), 1e-12f);
 }
 
 }  // namespace
@@ -193,20 +192,32 @@ cudaError_t launch_append(const AppendArgs& a, int fmt, int mode, cudaStream_t s
                            : launch_append_m<FP8PA_E5M2>(a, mode, stream);
 }
 
+cudaError_t launch_channel_absmax(const uint16_t* x, int num_tokens, int hd, float* amax,
+                                  cudaStream_t stream) {
+  if (num_tokens > 0) {
+    const dim3 grid((hd / 8 + 255) / 256, (num_tokens + kCalTokens - 1) / kCalTokens);
+    chanmax_kernel<<<grid, 256, 0, stream>>>(x, num_tokens, hd, reinterpret_cast<uint32_t*>(amax));
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scales_from_absmax(const float* amax, int n, int fmt, float* out,
+                                      cudaStream_t stream) {
+  const int blocks = (n + 255) / 256;
+  if (fmt == FP8PA_E4M3)
+    chanscale_finalize_kernel<FP8PA_E4M3><<<blocks, 256, 0, stream>>>(amax, out, n);
+  else
+    chanscale_finalize_kernel<FP8PA_E5M2><<<blocks, 256, 0, stream>>>(amax, out, n);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_channel_scales(const uint16_t* x, int num_tokens, int hd, int fmt, float* out,
                                   cudaStream_t stream) {
   cudaError_t e = cudaMemsetAsync(out, 0, sizeof(float) * static_cast<size_t>(hd), stream);
   if (e != cudaSuccess) return e;
-  if (num_tokens > 0) {
-    const dim3 grid((hd / 8 + 255) / 256, (num_tokens + kCalTokens - 1) / kCalTokens);
-    chanmax_kernel<<<grid, 256, 0, stream>>>(x, num_tokens, hd, reinterpret_cast<uint32_t*>(out));
-  }
-  const int blocks = (hd + 255) / 256;
-  if (fmt == FP8PA_E4M3)
-    chanscale_finalize_kernel<FP8PA_E4M3><<<blocks, 256, 0, stream>>>(out, hd);
-  else
-    chanscale_finalize_kernel<FP8PA_E5M2><<<blocks, 256, 0, stream>>>(out, hd);
-  return cudaGetLastError();
+  e = launch_channel_absmax(x, num_tokens, hd, out, stream);
+  if (e != cudaSuccess) return e;
+  return launch_scales_from_absmax(out, hd, fmt, out, stream);
 }
 
 }  // namespace fp8pa

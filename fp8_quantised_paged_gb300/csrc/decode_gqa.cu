@@ -667,6 +667,9 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const MergePara
 }
 
 // ---------------------------------------------------------------- host side
+// Stages of one warp's ring: 12 KB of K+V pages (3 stages at head_dim 128,
+// block 16), which keeps 16 warps resident per SM; deeper rings cost warps
+// and measured slower.
 template <int D, int BS>
 constexpr int stages_for() {
   constexpr int stage = 2 * BS * D;

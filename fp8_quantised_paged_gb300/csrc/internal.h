@@ -21,6 +21,10 @@ struct AppendArgs {
 cudaError_t launch_append(const AppendArgs& a, int fmt, int mode, cudaStream_t stream);
 cudaError_t launch_channel_scales(const uint16_t* x, int num_tokens, int hd, int fmt, float* out,
                                   cudaStream_t stream);
+cudaError_t launch_channel_absmax(const uint16_t* x, int num_tokens, int hd, float* amax,
+                                  cudaStream_t stream);
+cudaError_t launch_scales_from_absmax(const float* amax, int n, int fmt, float* out,
+                                      cudaStream_t stream);
 
 // Workspace layout of the split-K decode, shared by planner, split and merge.
 struct DecodeShape {

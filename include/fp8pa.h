@@ -129,6 +129,29 @@ int fp8pa_kv_channel_scales(const void* x, int num_tokens, int n_kv_heads, int h
                             float* scale_out, void* stream);
 
 /*
+ * Online calibration of static per-channel scales, one prefill batch at a
+ * time: running_absmax[h][d] = max(running_absmax[h][d], max_t |x[t][h][d]|).
+ * Defined by: a running maximum per attention layer, updated with each
+ * prefill batch and used for the scales of later tokens, after a warm-up on
+ * representative inputs ("Llama 3 70B FP8 deployment", dpshk.com/news/5605006,
+ * sec. 3.2).
+ * x               bf16 [num_tokens][n_kv_heads][head_dim].
+ * running_absmax  f32 [n_kv_heads][head_dim], caller-owned, zero before the
+ *                 first batch, updated in place (values stay non-negative).
+ * Calls on the same running_absmax are commutative (order does not matter).
+ */
+int fp8pa_kv_channel_absmax_update(const void* x, int num_tokens, int n_kv_heads, int head_dim,
+                                   float* running_absmax, void* stream);
+
+/*
+ * Static scales from a running absmax: scale[i] = max(absmax[i] / FMAX, 1e-12)
+ * (IEEE fp32 division; dpshk.com/news/5605006 sec. 3.1).  n = n_kv_heads *
+ * head_dim.  scale_out may alias absmax.
+ */
+int fp8pa_kv_scales_from_absmax(const float* absmax, int n, int fmt, float* scale_out,
+                                void* stream);
+
+/*
  * Bytes of device workspace fp8pa_paged_decode_attention needs for these
  * shapes on the current device (it depends on the device's SM count).
  */

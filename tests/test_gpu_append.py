@@ -138,3 +138,22 @@ def test_channel_scales_match_oracle(F):
         got = F.kv_channel_scales(to_dev_bf16(ks), fmt).cpu().numpy()
         want = oracle.kv_channel_scales(ks, fmt)
         assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
+
+
+def test_running_absmax_calibration_matches_oracle(F):
+    """Online calibration: folding prefill batches into a running absmax in
+    any order gives the one-shot static scales of all tokens, bit for bit."""
+    from gpu_util import DEV, to_dev_bf16
+    w = W.make_workload(4, "small")
+    ks = [W.request_kv(w, b)[0] for b in range(w.batch)]
+    for fmt in (W.E4M3, W.E5M2):
+        amax = torch.zeros((w.n_kv_heads, w.head_dim), dtype=torch.float32, device=DEV)
+        for b in (3, 0, 5, 1, 4, 2):          # batches arrive in any order
+            F.kv_channel_absmax_update(to_dev_bf16(ks[b]), amax)
+        got = F.kv_scales_from_absmax(amax, fmt).cpu().numpy()
+        want = oracle.kv_channel_scales(np.concatenate(ks), fmt)
+        assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
+        # scale_out may alias the running absmax
+        amax2 = amax.clone()
+        F.kv_scales_from_absmax(amax2, fmt, out=amax2)
+        assert np.array_equal(amax2.cpu().numpy().view(np.uint32), want.view(np.uint32))
