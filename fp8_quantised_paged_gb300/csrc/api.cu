@@ -88,6 +88,7 @@ DecodePath decode_path(int batch, int hq, int hkv, int d, int dv, int bs, int ma
   s.bs = bs;
   s.max_blocks = max_blocks;
   s.mla = 0;
+  s.qlen = 1;
   if ((fmt != FP8PA_E4M3 && fmt != FP8PA_E5M2) ||
       (mode != FP8PA_SCALE_TOKEN_HEAD && mode != FP8PA_SCALE_CHANNEL_STATIC &&
        mode != FP8PA_SCALE_TOKEN_GROUP) ||
@@ -117,6 +118,62 @@ DecodePath decode_path(int batch, int hq, int hkv, int d, int dv, int bs, int ma
       mode == FP8PA_SCALE_TOKEN_GROUP || (hkv > 8 && hkv % 8 != 0))
     r.status = FP8PA_ERR_UNSUPPORTED;
   return r;
+}
+
+// The decode of `batch` requests with `q_len` queries each (a causal chunk;
+// q_len = 1 is plain decode).  The kernels see batch * q_len virtual
+// requests; q and out rows are (request, query) in that order.
+int attention_impl(const void* q, const uint8_t* k_cache, const uint8_t* v_cache,
+                   const float* k_scale, const float* v_scale, const int32_t* block_tables,
+                   int max_blocks_per_seq, const int32_t* seq_lens, int batch, int q_len,
+                   int block_size, int n_q_heads, int n_kv_heads, int head_dim, int head_dim_v,
+                   int fmt, int scale_mode, int group_size, float sm_scale, int num_blocks,
+                   void* out, int out_dtype, void* workspace, size_t workspace_bytes,
+                   void* stream) {
+  if (q_len <= 0 || batch < 0) return FP8PA_ERR_BAD_SHAPE;
+  if (static_cast<long long>(batch) * q_len >= (1ll << 31)) return FP8PA_ERR_UNSUPPORTED;
+  DecodePath path = decode_path(batch * q_len, n_q_heads, n_kv_heads, head_dim, head_dim_v,
+                                block_size, max_blocks_per_seq, fmt, scale_mode, group_size,
+                                num_blocks, out_dtype);
+  if (path.status != FP8PA_OK) return path.status;
+  path.shape.qlen = q_len;
+  if (batch == 0) return FP8PA_OK;
+  if (!q || !k_cache || !k_scale || !block_tables || !seq_lens || !out || !workspace)
+    return FP8PA_ERR_NULL_POINTER;
+  if (path.shape.mla) {
+    if (v_cache != k_cache || v_scale != k_scale) return FP8PA_ERR_UNSUPPORTED;
+  } else if (!v_cache || !v_scale) {
+    return FP8PA_ERR_NULL_POINTER;
+  }
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k_scale) ||
+      !aligned16(v_scale) || !aligned16(workspace) || !aligned16(out))
+    return FP8PA_ERR_ALIGNMENT;
+  int dev = 0;
+  uint32_t* err = device_error_ptr(&dev);
+  if (!err) return FP8PA_ERR_CUDA;
+  path.shape.workers = decode_workers(path.shape, fmt, scale_mode, dev);
+  if (workspace_bytes < decode_workspace_bytes(path.shape)) return FP8PA_ERR_WORKSPACE;
+  DecodeArgs a{};
+  a.q = static_cast<const uint16_t*>(q);
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.k_scale = k_scale;
+  a.v_scale = v_scale;
+  a.block_tables = block_tables;
+  a.seq_lens = seq_lens;
+  a.num_blocks = num_blocks;
+  a.fmt = fmt;
+  a.mode = scale_mode;
+  a.gs = group_size;
+  a.out_dtype = out_dtype;
+  a.sm_scale = sm_scale;
+  a.out = out;
+  a.workspace = workspace;
+  a.err = err;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const cudaError_t e = path.shape.mla ? launch_decode_mla(path.shape, a, st)
+                                       : launch_decode_gqa(path.shape, a, st);
+  return cuda_status(e);
 }
 
 }  // namespace
@@ -245,47 +302,25 @@ int fp8pa_paged_decode_attention(const void* q, const uint8_t* k_cache, const ui
                                  int fmt, int scale_mode, int group_size, float sm_scale,
                                  int num_blocks, void* out, int out_dtype, void* workspace,
                                  size_t workspace_bytes, void* stream) {
-  DecodePath path = decode_path(batch, n_q_heads, n_kv_heads, head_dim, head_dim_v, block_size,
-                                max_blocks_per_seq, fmt, scale_mode, group_size, num_blocks,
-                                out_dtype);
-  if (path.status != FP8PA_OK) return path.status;
-  if (batch == 0) return FP8PA_OK;
-  if (!q || !k_cache || !k_scale || !block_tables || !seq_lens || !out || !workspace)
-    return FP8PA_ERR_NULL_POINTER;
-  if (path.shape.mla) {
-    if (v_cache != k_cache || v_scale != k_scale) return FP8PA_ERR_UNSUPPORTED;
-  } else if (!v_cache || !v_scale) {
-    return FP8PA_ERR_NULL_POINTER;
-  }
-  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k_scale) ||
-      !aligned16(v_scale) || !aligned16(workspace) || !aligned16(out))
-    return FP8PA_ERR_ALIGNMENT;
-  int dev = 0;
-  uint32_t* err = device_error_ptr(&dev);
-  if (!err) return FP8PA_ERR_CUDA;
-  path.shape.workers = decode_workers(path.shape, fmt, scale_mode, dev);
-  if (workspace_bytes < decode_workspace_bytes(path.shape)) return FP8PA_ERR_WORKSPACE;
-  DecodeArgs a{};
-  a.q = static_cast<const uint16_t*>(q);
-  a.k_cache = k_cache;
-  a.v_cache = v_cache;
-  a.k_scale = k_scale;
-  a.v_scale = v_scale;
-  a.block_tables = block_tables;
-  a.seq_lens = seq_lens;
-  a.num_blocks = num_blocks;
-  a.fmt = fmt;
-  a.mode = scale_mode;
-  a.gs = group_size;
-  a.out_dtype = out_dtype;
-  a.sm_scale = sm_scale;
-  a.out = out;
-  a.workspace = workspace;
-  a.err = err;
-  const cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const cudaError_t e = path.shape.mla ? launch_decode_mla(path.shape, a, st)
-                                       : launch_decode_gqa(path.shape, a, st);
-  return cuda_status(e);
+  return attention_impl(q, k_cache, v_cache, k_scale, v_scale, block_tables, max_blocks_per_seq,
+                        seq_lens, batch, 1, block_size, n_q_heads, n_kv_heads, head_dim,
+                        head_dim_v, fmt, scale_mode, group_size, sm_scale, num_blocks, out,
+                        out_dtype, workspace, workspace_bytes, stream);
+}
+
+int fp8pa_paged_multiquery_attention(const void* q, const uint8_t* k_cache,
+                                     const uint8_t* v_cache, const float* k_scale,
+                                     const float* v_scale, const int32_t* block_tables,
+                                     int max_blocks_per_seq, const int32_t* seq_lens, int batch,
+                                     int q_len, int block_size, int n_q_heads, int n_kv_heads,
+                                     int head_dim, int head_dim_v, int fmt, int scale_mode,
+                                     int group_size, float sm_scale, int num_blocks, void* out,
+                                     int out_dtype, void* workspace, size_t workspace_bytes,
+                                     void* stream) {
+  return attention_impl(q, k_cache, v_cache, k_scale, v_scale, block_tables, max_blocks_per_seq,
+                        seq_lens, batch, q_len, block_size, n_q_heads, n_kv_heads, head_dim,
+                        head_dim_v, fmt, scale_mode, group_size, sm_scale, num_blocks, out,
+                        out_dtype, workspace, workspace_bytes, stream);
 }
 
 int fp8pa_get_device_error(void* stream, uint32_t* flags) {

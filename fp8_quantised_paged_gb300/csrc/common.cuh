@@ -207,6 +207,18 @@ __device__ __forceinline__ void griddep_launch_dependents() {
 }
 
 // Cycles a bounded wait may spin (about two seconds at GB300 clocks).
+// Visible length of virtual request v in a causal chunk of `qlen` queries per
+// request: query i of request b (v = b * qlen + i) sees the first
+// seq_lens[b] - (qlen - 1 - i) cached tokens; qlen = 1 is plain decode.
+// `bad` reports a length outside [0, cap], or shorter than the chunk.
+__device__ __forceinline__ int visible_len(const int32_t* seq_lens, int v, int qlen, int cap,
+                                           bool* bad) {
+  const int L = seq_lens[v / qlen];
+  *bad = L < 0 || L > cap || (qlen > 1 && L < qlen);
+  const int vis = min(L, cap) - (qlen - 1 - v % qlen);
+  return vis < 0 ? 0 : vis;
+}
+
 constexpr long long kWaitLimitCycles = 4000000000ll;
 
 }  // namespace fp8pa

@@ -48,8 +48,6 @@ __device__ __forceinline__ int ld_i32(const int* p) { return *reinterpret_cast<c
 // (B*Hkv+1 ints).  Partial buffers follow at 256-byte aligned offsets.
 constexpr int kPlanHeader = 4;
 
-__device__ __forceinline__ int clamp_len(int L, int cap) { return L < 0 ? 0 : (L > cap ? cap : L); }
-
 __device__ __forceinline__ int warp_incl_scan(int x) {
   const int lane = threadIdx.x & 31;
 #pragma unroll
@@ -62,9 +60,9 @@ __device__ __forceinline__ int warp_incl_scan(int x) {
 
 // One warp: unit prefix per request, units per worker, and the base index of
 // each (request, kv head)'s partials.  Lets the split kernel launch at once.
-__global__ void __launch_bounds__(32) plan_kernel(const int32_t* seq_lens, int B, int hkv, int bs,
-                                                  int max_blocks, int workers, int* ws,
-                                                  uint32_t* err) {
+__global__ void __launch_bounds__(32) plan_kernel(const int32_t* seq_lens, int B, int qlen,
+                                                  int hkv, int bs, int max_blocks, int workers,
+                                                  int* ws, uint32_t* err) {
   griddep_wait();  // inputs may come from the kernel before us in the stream
   griddep_launch_dependents();
   const int lane = threadIdx.x;
@@ -76,9 +74,10 @@ __global__ void __launch_bounds__(32) plan_kernel(const int32_t* seq_lens, int B
     const int b = base + lane;
     int n = 0;
     if (b < B) {
-      const int L = seq_lens[b];
-      if (L < 0 || L > cap) raise_error(err, FP8PA_DEVERR_SEQ_LEN);
-      n = (clamp_len(L, cap) + bs - 1) / bs;
+      bool bad;
+      const int L = visible_len(seq_lens, b, qlen, cap, &bad);
+      if (bad) raise_error(err, FP8PA_DEVERR_SEQ_LEN);
+      n = (L + bs - 1) / bs;
     }
     const int incl = warp_incl_scan(n);
     if (b < B) uprefix[b] = (carry + incl - n) * hkv;
@@ -124,6 +123,7 @@ struct GqaParams {
   float* part_o;
   uint32_t* err;
   int B, hq, hkv, G, max_blocks, num_blocks;
+  int qlen;  // queries per request: B counts (request, query) pairs
   float qk_scale_log2;
 };
 
@@ -154,6 +154,7 @@ __device__ __forceinline__ uint32_t swz(int r, int ch) {
 
 struct Cursor {
   int b, j, nb;
+  long brow;  // offset of request b's block-table row (b / qlen)
 };
 
 template <int D, int BS, int FMT, int MODE, int NST>
@@ -219,6 +220,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32)
     cu.b = lo;
     cu.nb = uprefix[lo + 1] - uprefix[lo];
     cu.j = static_cast<int>(u - uprefix[lo]);
+    cu.brow = static_cast<long>(lo / p.qlen) * p.max_blocks;
     return cu;
   };
   auto advance = [&](Cursor& cu) {
@@ -227,11 +229,12 @@ __global__ void __launch_bounds__(kMaxWarps * 32)
     do {
       ++cu.b;
     } while (cu.b < p.B && uprefix[cu.b + 1] == uprefix[cu.b]);
-    if (cu.b < p.B) cu.nb = uprefix[cu.b + 1] - uprefix[cu.b];
+    if (cu.b < p.B) {
+      cu.nb = uprefix[cu.b + 1] - uprefix[cu.b];
+      cu.brow = static_cast<long>(cu.b / p.qlen) * p.max_blocks;
+    }
   };
-  auto block_of = [&](const Cursor& cu) {
-    return __ldg(p.block_tables + static_cast<long>(cu.b) * p.max_blocks + cu.j);
-  };
+  auto block_of = [&](const Cursor& cu) { return __ldg(p.block_tables + cu.brow + cu.j); };
   // Issue the copies of one page into stage s (lane 0 only acts).
   auto issue = [&](const Cursor& cu, int blk, int s) {
     if (lane == 0) {
@@ -296,7 +299,8 @@ __global__ void __launch_bounds__(kMaxWarps * 32)
     const uint32_t par = static_cast<uint32_t>((i / NST) & 1);
     if (i == 0 || cc.j == 0) {
       // ---- new segment: load q for the G heads of (b, kv head)
-      Lb = clamp_len(__ldg(p.seq_lens + cc.b), p.max_blocks * BS);
+      bool bad;
+      Lb = visible_len(p.seq_lens, cc.b, p.qlen, p.max_blocks * BS, &bad);
       const int h = kvh * p.G + g;
       float qv[D / 4];
       if (g < p.G) {
@@ -790,7 +794,8 @@ cudaError_t launch_decode_gqa(const DecodeShape& s, const DecodeArgs& a, cudaStr
   float* part_ml = reinterpret_cast<float*>(ws + plan_bytes);
   float* part_o = reinterpret_cast<float*>(ws + plan_bytes + align256(prow * 2 * sizeof(float)));
 
-  e = launch_plan(a.seq_lens, s.batch, 1, s.bs, s.max_blocks, s.workers, plan, a.err, stream);
+  e = launch_plan(a.seq_lens, s.batch, s.qlen, 1, s.bs, s.max_blocks, s.workers, plan, a.err,
+                  stream);
   if (e != cudaSuccess) return e;
   // Every kernel of the decode is launched with programmatic stream
   // serialisation: it may start while its predecessor drains, and waits
@@ -818,6 +823,7 @@ cudaError_t launch_decode_gqa(const DecodeShape& s, const DecodeArgs& a, cudaStr
   p.G = G;
   p.max_blocks = s.max_blocks;
   p.num_blocks = a.num_blocks;
+  p.qlen = s.qlen;
   p.qk_scale_log2 = a.sm_scale * 1.4426950408889634f;
   cfg.gridDim = dim3(static_cast<unsigned>(s.workers) * hsets);
   cfg.blockDim = dim3(wpc * 32);
@@ -831,8 +837,9 @@ cudaError_t launch_decode_gqa(const DecodeShape& s, const DecodeArgs& a, cudaStr
                       /*pieces_per_request=*/true, stream);
 }
 
-cudaError_t launch_plan(const int32_t* seq_lens, int batch, int groups, int bs, int max_blocks,
-                        int workers, int* plan, uint32_t* err, cudaStream_t stream) {
+cudaError_t launch_plan(const int32_t* seq_lens, int batch, int qlen, int groups, int bs,
+                        int max_blocks, int workers, int* plan, uint32_t* err,
+                        cudaStream_t stream) {
   cudaLaunchAttribute pdl[1];
   pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   pdl[0].val.programmaticStreamSerializationAllowed = 1;
@@ -842,8 +849,8 @@ cudaError_t launch_plan(const int32_t* seq_lens, int batch, int groups, int bs, 
   cfg.stream = stream;
   cfg.attrs = pdl;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, plan_kernel, seq_lens, batch, groups, bs, max_blocks, workers,
-                            plan, err);
+  return cudaLaunchKernelEx(&cfg, plan_kernel, seq_lens, batch, qlen, groups, bs, max_blocks,
+                            workers, plan, err);
 }
 
 cudaError_t launch_merge(const int* plan, const float* part_ml, const float* part_o, void* out,

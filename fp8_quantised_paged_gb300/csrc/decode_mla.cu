@@ -70,6 +70,7 @@ struct MlaParams {
   float* part_o;
   uint32_t* err;
   int B, hq, ngroups_h, max_blocks, num_blocks;
+  int qlen;  // queries per request: B counts (request, query) pairs
   float qk_scale_log2;
 };
 
@@ -134,6 +135,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const MlaParams 
   // unit -> (request b, page j)
   struct Cur {
     int b, hg, j, nb;
+    long brow;  // offset of request b's block-table row (b / qlen)
   };
   auto locate = [&](long u) {
     int lo = 0, hi = p.B;
@@ -146,6 +148,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const MlaParams 
     cu.nb = uprefix[lo + 1] - uprefix[lo];
     cu.hg = hg;
     cu.j = static_cast<int>(u - uprefix[lo]);
+    cu.brow = static_cast<long>(lo / p.qlen) * p.max_blocks;
     return cu;
   };
   auto advance = [&](Cur& cu) {
@@ -154,10 +157,13 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const MlaParams 
     do {
       ++cu.b;
     } while (cu.b < p.B && uprefix[cu.b + 1] == uprefix[cu.b]);
-    if (cu.b < p.B) cu.nb = uprefix[cu.b + 1] - uprefix[cu.b];
+    if (cu.b < p.B) {
+      cu.nb = uprefix[cu.b + 1] - uprefix[cu.b];
+      cu.brow = static_cast<long>(cu.b / p.qlen) * p.max_blocks;
+    }
   };
   auto issue = [&](const Cur& cu, int s) {  // thread 0 only
-    const int blk = __ldg(p.block_tables + static_cast<long>(cu.b) * p.max_blocks + cu.j);
+    const int blk = __ldg(p.block_tables + cu.brow + cu.j);
     const bool ok = blk >= 0 && blk < p.num_blocks;
     okf[s] = ok ? 1 : 0;
     if (ok) {
@@ -195,9 +201,8 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const MlaParams 
     if (i == 0 || cc.j == 0) {
       // ---- new segment: q of the 32 heads -> f16 (power-of-two normalised)
       __syncthreads();
-      Lb = __ldg(p.seq_lens + cc.b);
-      const int cap = p.max_blocks * kBs;
-      Lb = Lb < 0 ? 0 : (Lb > cap ? cap : Lb);
+      bool bad;
+      Lb = visible_len(p.seq_lens, cc.b, p.qlen, p.max_blocks * kBs, &bad);
       const uint16_t* qsrc = p.q + (static_cast<long>(cc.b) * p.hq + cc.hg * kHeads) * kDk;
       float amax = 0.f;
       for (int e = tid; e < kHeads * kDk / 8; e += kThreads) {
@@ -492,7 +497,8 @@ cudaError_t launch_decode_mla(const DecodeShape& s, const DecodeArgs& a, cudaStr
   float* part_ml = reinterpret_cast<float*>(ws + plan_bytes);
   float* part_o = reinterpret_cast<float*>(ws + plan_bytes + align256(rows * 2 * sizeof(float)));
 
-  e = launch_plan(a.seq_lens, s.batch, 1, kBs, s.max_blocks, ranges, plan, a.err, stream);
+  e = launch_plan(a.seq_lens, s.batch, s.qlen, 1, kBs, s.max_blocks, ranges, plan, a.err,
+                  stream);
   if (e != cudaSuccess) return e;
   MlaParams p;
   p.q = a.q;
@@ -509,6 +515,7 @@ cudaError_t launch_decode_mla(const DecodeShape& s, const DecodeArgs& a, cudaStr
   p.ngroups_h = H;
   p.max_blocks = s.max_blocks;
   p.num_blocks = a.num_blocks;
+  p.qlen = s.qlen;
   p.qk_scale_log2 = a.sm_scale * 1.4426950408889634f;
 
   cudaLaunchAttribute pdl[1];

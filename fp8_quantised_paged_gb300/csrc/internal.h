@@ -31,6 +31,7 @@ struct DecodeShape {
   int batch, hq, hkv, d, dv, bs, max_blocks;
   int workers;        // split workers (warps or CTAs, per kernel family)
   int mla;            // 1 for the shared-latent kernel
+  int qlen;           // queries per request (batch counts request x query)
 };
 
 size_t decode_workspace_bytes(const DecodeShape& s);
@@ -55,9 +56,11 @@ int decode_workers(const DecodeShape& s, int fmt, int mode, int device);
 // Shared by both kernel families: the planner (flat (request, group, page)
 // list cut into equal ranges) and the log-sum-exp merge of the pieces.
 // `groups` is the number of head groups per request (KV heads for GQA, groups
-// of 32 query heads for MLA) and G the query heads per group.
-cudaError_t launch_plan(const int32_t* seq_lens, int batch, int groups, int bs, int max_blocks,
-                        int workers, int* plan, uint32_t* err, cudaStream_t stream);
+// of 32 query heads for MLA) and G the query heads per group.  `batch`
+// counts virtual requests (request x query of a causal chunk of `qlen`).
+cudaError_t launch_plan(const int32_t* seq_lens, int batch, int qlen, int groups, int bs,
+                        int max_blocks, int workers, int* plan, uint32_t* err,
+                        cudaStream_t stream);
 cudaError_t launch_merge(const int* plan, const float* part_ml, const float* part_o, void* out,
                          int batch, int hq, int groups, int G, int dv, int out_dtype,
                          bool pieces_per_request, cudaStream_t stream);

@@ -227,6 +227,14 @@ def queries(w: Workload) -> np.ndarray:
                                                 dtype=np.float32))
 
 
+def chunk_queries(w: Workload, q_len: int) -> np.ndarray:
+    """bf16 bits of a causal chunk's queries, [B, q_len, Hq, Dk], ~N(0, 1)
+    (the chunk is the last q_len cached tokens of each request)."""
+    rng = _rng(w.seed, 5, q_len)
+    return f32_to_bf16_bits(rng.standard_normal((w.batch, q_len, w.n_q_heads, w.head_dim),
+                                                dtype=np.float32))
+
+
 def token_slots(w: Workload, b: int, t0: int, t1: int) -> np.ndarray:
     """Slot numbers (block id * block_size + offset) of tokens [t0, t1) of
     request b under its block table."""

@@ -201,6 +201,38 @@ int fp8pa_paged_decode_attention(const void* q, const uint8_t* k_cache, const ui
                                  size_t workspace_bytes, void* stream);
 
 /*
+ * Attention of a causal chunk of q_len query tokens per request over the
+ * paged FP8 cache: the chunk's own tokens were appended to the cache first,
+ * so query i (0 <= i < q_len) of request b sees the first
+ * seq_lens[b] - (q_len - 1 - i) cached tokens, and the last query sees them
+ * all.  q_len = 1 is fp8pa_paged_decode_attention.
+ * Serves the chunks that a scheduler interleaves with decode steps when it
+ * splits a long prompt (chunked prefill: dpshk.com/news/5605006, sec. 2.1 and
+ * 3.3; hotelren.com/news/5711065, sec. 3.4) and the verify step of
+ * speculative decoding, where the target model scores several draft tokens
+ * at once (dpshk.com/news/5605006, sec. 4.3).  Each query row is computed
+ * exactly as a decode row over its visible prefix.
+ *
+ * q            bf16 [batch][q_len][n_q_heads][head_dim].
+ * out          [batch][q_len][n_q_heads][head_dim_v], bf16 or f32.
+ * seq_lens     i32 [batch], the cached length including the whole chunk.
+ *              A request shorter than q_len (or outside [0, cap]) sets
+ *              FP8PA_DEVERR_SEQ_LEN; its rows that would see no token are 0.
+ * workspace    at least fp8pa_decode_workspace_bytes(batch * q_len, ...).
+ * Layout limits, other arguments and errors as fp8pa_paged_decode_attention;
+ * q_len <= 0 returns FP8PA_ERR_BAD_SHAPE.
+ */
+int fp8pa_paged_multiquery_attention(const void* q, const uint8_t* k_cache,
+                                     const uint8_t* v_cache, const float* k_scale,
+                                     const float* v_scale, const int32_t* block_tables,
+                                     int max_blocks_per_seq, const int32_t* seq_lens, int batch,
+                                     int q_len, int block_size, int n_q_heads, int n_kv_heads,
+                                     int head_dim, int head_dim_v, int fmt, int scale_mode,
+                                     int group_size, float sm_scale, int num_blocks, void* out,
+                                     int out_dtype, void* workspace, size_t workspace_bytes,
+                                     void* stream);
+
+/*
  * Size of the scratch array built into the library for
  * fp8pa_paged_decode_attention_static_ws (16 MiB per device that uses it).
  */

@@ -191,3 +191,43 @@ def test_gqa_group_of_one_is_plain_mha():
     q = W.queries(w)
     got = run_oracle(w, q, kc, vc, ks, vs)
     assert np.allclose(got, sdpa_reference(w, q, kc, vc, ks, vs), rtol=1e-10, atol=1e-10)
+
+
+@pytest.mark.parametrize("idx,q_len", [(2, 3), (4, 4), (5, 2)])
+def test_multiquery_rows_are_a_causal_chunk(idx, q_len):
+    """A chunk of q_len queries over a cache that already holds the chunk:
+    running every (request, query) as a decode row over its visible prefix
+    equals causal attention of the chunk (torch SDPA with a boolean mask) --
+    the reading under which the multi-query call is checked."""
+    w = W.make_workload(idx, "small")
+    kc, vc, ks, vs = build_cache(w)
+    qc = W.chunk_queries(w, q_len)                                   # [B, q_len, Hq, D]
+    # decode rows: request b's table repeated, query i sees L - (q_len - 1 - i)
+    tables = np.repeat(w.block_tables, q_len, axis=0)
+    lens = np.array([max(0, int(L) - (q_len - 1 - i)) for L in w.seq_lens for i in range(q_len)],
+                    np.int32)
+    got = oracle.paged_decode_attention(
+        qc.reshape(-1, w.n_q_heads, w.head_dim), kc, vc, ks, vs, tables, lens, w.block_size,
+        w.n_kv_heads, w.head_dim_v, w.fmt, w.scale_mode, w.group_size, w.sm_scale)
+    got = got.reshape(w.batch, q_len, w.n_q_heads, w.head_dim_v)
+    G = w.n_q_heads // w.n_kv_heads
+    # a row that sees no token is zero (a request shorter than the chunk)
+    assert (got.reshape(-1, w.n_q_heads, w.head_dim_v)[lens == 0] == 0).all()
+    checked = 0
+    for b in range(w.batch):
+        L = int(w.seq_lens[b])
+        if L < q_len:
+            continue
+        checked += 1
+        K = dequant_request(w, kc, ks, b).permute(1, 0, 2).repeat_interleave(G, dim=0)
+        V = dequant_request(w, vc, vs, b)[..., :w.head_dim_v]
+        V = V.permute(1, 0, 2).repeat_interleave(G, dim=0)
+        qf = torch.from_numpy(W.bf16_bits_to_f32(qc[b]).astype(np.float64)).permute(1, 0, 2)
+        t = torch.arange(L)[None, :]
+        pos = torch.arange(L - q_len, L)[:, None]          # the chunk's own positions
+        mask = t <= pos                                     # [q_len, L]
+        o = torch.nn.functional.scaled_dot_product_attention(qf, K, V, attn_mask=mask,
+                                                             scale=w.sm_scale)
+        ref = o.permute(1, 0, 2).numpy()
+        assert np.allclose(got[b], ref, rtol=1e-10, atol=1e-10), np.abs(got[b] - ref).max()
+    assert checked >= w.batch - 1
