@@ -671,13 +671,14 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const MergePara
 }
 
 // ---------------------------------------------------------------- host side
-// Stages of one warp's ring: 12 KB of K+V pages (3 stages at head_dim 128,
-// block 16), which keeps 16 warps resident per SM; deeper rings cost warps
-// and measured slower.
+// Stages of one warp's ring: 8 KB of K+V pages (2 stages at head_dim 128,
+// block 16).  Registers hold 16 warps per SM; one page in flight per warp
+// while it computes on the other already covers the memory latency (a third
+// stage measured 1 % slower, and 24 warps with 2 stages spill registers).
 template <int D, int BS>
 constexpr int stages_for() {
   constexpr int stage = 2 * BS * D;
-  constexpr int n = 12288 / stage;
+  constexpr int n = 8192 / stage;
   return n < 2 ? 2 : (n > 8 ? 8 : n);
 }
 
