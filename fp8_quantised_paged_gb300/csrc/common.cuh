@@ -175,6 +175,15 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// (x0, x1) as two f16x2 planes: hi = f16(x), lo = f16(x - hi); hi + lo carries
+// about 22 significant bits.
+__device__ __forceinline__ void split_pack(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  const __half2 h = __floats2half2_rn(x0, x1);
+  const float2 hf = __half22float2(h);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = pack_half2(x0 - hf.x, x1 - hf.y);
+}
+
 // 2^e as a float for integer e (0 below the normal range).
 __device__ __forceinline__ float exp2i(int e) {
   if (e < -126) return 0.0f;
@@ -206,7 +215,6 @@ __device__ __forceinline__ void griddep_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-// Cycles a bounded wait may spin (about two seconds at GB300 clocks).
 // Visible length of virtual request v in a causal chunk of `qlen` queries per
 // request: query i of request b (v = b * qlen + i) sees the first
 // seq_lens[b] - (qlen - 1 - i) cached tokens; qlen = 1 is plain decode.
@@ -219,6 +227,7 @@ __device__ __forceinline__ int visible_len(const int32_t* seq_lens, int v, int q
   return vis < 0 ? 0 : vis;
 }
 
+// Cycles a bounded wait may spin (about two seconds at GB300 clocks).
 constexpr long long kWaitLimitCycles = 4000000000ll;
 
 }  // namespace fp8pa

@@ -87,13 +87,6 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t&
                : "r"(addr));
 }
 
-__device__ __forceinline__ void split_pack(float x0, float x1, uint32_t& hi, uint32_t& lo) {
-  const __half2 h = __floats2half2_rn(x0, x1);
-  const float2 hf = __half22float2(h);
-  hi = *reinterpret_cast<const uint32_t*>(&h);
-  lo = pack_half2(x0 - hf.x, x1 - hf.y);
-}
-
 template <int FMT>
 __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const MlaParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
