@@ -320,11 +320,11 @@ def run_gpu(args, rank, world, local_rank):
                                               w.max_blocks, dev), dtype=torch.uint8, device=dev)
 
     def step(q_, kn_, vn_, slots_, sl_):
-        F.kv_append_quant(kn_, vn_, slots_, kc, vc, ks, vs, fmt=w.fmt, scale_mode=w.scale_mode,
-                          group_size=w.group_size)
-        F.paged_decode_attention(q_, kc, vc_, ks, vs_, bt, sl_, hkv, w.sm_scale, fmt=w.fmt,
-                                 scale_mode=w.scale_mode, group_size=w.group_size,
-                                 head_dim_v=w.head_dim_v, out=out, workspace=ws)
+        # one call: append (with the split planner in the same launch),
+        # split kernel, merge
+        F.decode_step(kn_, vn_, slots_, q_, kc, vc_, ks, vs_, bt, sl_, hkv, w.sm_scale,
+                      fmt=w.fmt, scale_mode=w.scale_mode, group_size=w.group_size,
+                      head_dim_v=w.head_dim_v, out=out, workspace=ws)
 
     def barrier():
         if world > 1:
@@ -452,12 +452,11 @@ def run_gpu(args, rank, world, local_rank):
                            compute="fp8 codes -> exact f16, warp MMA (m16n8k16), f32 accumulate "
                                    "and softmax",
                            l2="no flush: every step reads the whole cache, larger than L2",
-                           step="append (1 token/request) + plan + split + merge",
+                           step="fp8pa_decode_step: append (1 token/request) and plan, split, merge",
                            bytes_per_step=acc["step"]),
             "roofline": roof,
-            "gpu_launches": 4 * args.steps,
-            "gpu_launches_per_step": {"append_kernel": 1, "plan_kernel": 1, kname: 1,
-                                      "merge_kernel": 1},
+            "gpu_launches": 3 * args.steps,
+            "gpu_launches_per_step": {"append_plan_kernel": 1, kname: 1, "merge_kernel": 1},
             "clocks": clk,
             "e2e": e2e}
     if not args.no_cpu_baseline:

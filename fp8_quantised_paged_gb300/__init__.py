@@ -15,6 +15,7 @@ and raises if it is missing: there is no fallback path.
 """
 _API = ("kv_append_quant", "kv_channel_scales", "kv_channel_absmax_update",
         "kv_scales_from_absmax", "paged_decode_attention", "paged_multiquery_attention",
+        "decode_step",
         "decode_workspace_bytes", "get_device_error", "set_decode_workers", "version",
         "E4M3", "E5M2", "SCALE_TOKEN_HEAD", "SCALE_CHANNEL_STATIC", "SCALE_TOKEN_GROUP",
         "OUT_BF16", "OUT_F32", "Fp8paError")

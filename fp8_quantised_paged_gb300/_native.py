@@ -37,6 +37,9 @@ _SIGS = {
     "fp8pa_paged_multiquery_attention": (_I, [_P, _P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I,
                                               _I, _I, _I, _I, _I, ctypes.c_float, _I, _P, _I, _P,
                                               ctypes.c_size_t, _P]),
+    "fp8pa_decode_step": (_I, [_P, _P, _P, _I, _P, _P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I,
+                               _I, _I, _I, _I, _I, ctypes.c_float, _I, _P, _I, _P,
+                               ctypes.c_size_t, _P]),
     "fp8pa_paged_decode_attention_static_ws": (_I, [_P, _P, _P, _P, _P, _P, _I, _P, _I, _I, _I,
                                                     _I, _I, _I, _I, _I, _I, ctypes.c_float, _I,
                                                     _P, _I, _P]),

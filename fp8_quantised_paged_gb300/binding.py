@@ -23,7 +23,7 @@ from ._native import (E4M3, E5M2, OUT_BF16, OUT_F32, SCALE_CHANNEL_STATIC, SCALE
                       SCALE_TOKEN_HEAD, Fp8paError)
 
 __all__ = ["kv_append_quant", "kv_channel_scales", "kv_channel_absmax_update",
-           "kv_scales_from_absmax", "paged_decode_attention", "paged_multiquery_attention",
+           "kv_scales_from_absmax", "paged_decode_attention", "paged_multiquery_attention", "decode_step",
            "decode_workspace_bytes", "get_device_error", "set_decode_workers", "version",
            "E4M3", "E5M2", "SCALE_TOKEN_HEAD", "SCALE_CHANNEL_STATIC", "SCALE_TOKEN_GROUP",
            "OUT_BF16", "OUT_F32", "Fp8paError"]
@@ -210,6 +210,53 @@ def paged_multiquery_attention(q, k_cache, v_cache, k_scale, v_scale, block_tabl
             fmt, scale_mode, group_size, float(sm_scale), nb, _ptr(out), odt, _ptr(workspace),
             0 if workspace is None else workspace.numel(), _stream(stream))
     N.check(rc, "paged_multiquery_attention")
+    return out
+
+
+def decode_step(k_new, v_new, slot_mapping, q, k_cache, v_cache, k_scale, v_scale,
+                block_tables, seq_lens, n_kv_heads, sm_scale, fmt=E4M3,
+                scale_mode=SCALE_TOKEN_HEAD, group_size=64, head_dim_v=None, out=None,
+                out_dtype=None, workspace=None, stream=None):
+    """Append the new rows (as kv_append_quant), then attend (as
+    paged_decode_attention for q [B, Hq, Dk], or paged_multiquery_attention
+    for q [B, q_len, Hq, Dk]) in one call.  For MLA pass v_new=None and
+    v_cache/v_scale equal to k_cache/k_scale.  Returns out."""
+    _need(q, torch.bfloat16, "q")
+    dev = q.device
+    _need(k_new, torch.bfloat16, "k_new", dev)
+    _need(v_new, torch.bfloat16, "v_new", dev)
+    for t, dt, name in ((k_cache, torch.uint8, "k_cache"), (v_cache, torch.uint8, "v_cache"),
+                        (k_scale, torch.float32, "k_scale"), (v_scale, torch.float32, "v_scale"),
+                        (block_tables, torch.int32, "block_tables"),
+                        (seq_lens, torch.int32, "seq_lens"),
+                        (slot_mapping, torch.int32, "slot_mapping")):
+        _need(t, dt, name, dev)
+    multi = q.dim() == 4
+    B, qlen, hq, dk = q.shape if multi else (q.shape[0], 1, q.shape[1], q.shape[2])
+    dv = dk if head_dim_v is None else head_dim_v
+    nb, _, bs, _ = k_cache.shape
+    max_blocks = block_tables.shape[1]
+    n_new = k_new.shape[0]
+    if out is None:
+        shape = (B, qlen, hq, dv) if multi else (B, hq, dv)
+        out = torch.empty(shape, dtype=out_dtype or torch.bfloat16, device=dev)
+    if out.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("out must be bf16 or float32")
+    odt = OUT_F32 if out.dtype == torch.float32 else OUT_BF16
+    _need(out, out.dtype, "out", dev)
+    with torch.cuda.device(dev):
+        need = int(N.lib.fp8pa_decode_workspace_bytes(B * qlen, hq, n_kv_heads, dk, dv, bs,
+                                                      max_blocks))
+        if workspace is None and need > 0:
+            workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+        _need(workspace, torch.uint8, "workspace", dev)
+        rc = N.lib.fp8pa_decode_step(
+            _ptr(k_new), _ptr(v_new), _ptr(slot_mapping), n_new, _ptr(q), _ptr(k_cache),
+            _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), _ptr(block_tables), max_blocks,
+            _ptr(seq_lens), B, qlen, bs, hq, n_kv_heads, dk, dv, fmt, scale_mode, group_size,
+            float(sm_scale), nb, _ptr(out), odt, _ptr(workspace),
+            0 if workspace is None else workspace.numel(), _stream(stream))
+    N.check(rc, "decode_step")
     return out
 
 

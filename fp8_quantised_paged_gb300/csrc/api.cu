@@ -120,27 +120,28 @@ DecodePath decode_path(int batch, int hq, int hkv, int d, int dv, int bs, int ma
   return r;
 }
 
-// The decode of `batch` requests with `q_len` queries each (a causal chunk;
-// q_len = 1 is plain decode).  The kernels see batch * q_len virtual
-// requests; q and out rows are (request, query) in that order.
-int attention_impl(const void* q, const uint8_t* k_cache, const uint8_t* v_cache,
-                   const float* k_scale, const float* v_scale, const int32_t* block_tables,
-                   int max_blocks_per_seq, const int32_t* seq_lens, int batch, int q_len,
-                   int block_size, int n_q_heads, int n_kv_heads, int head_dim, int head_dim_v,
-                   int fmt, int scale_mode, int group_size, float sm_scale, int num_blocks,
-                   void* out, int out_dtype, void* workspace, size_t workspace_bytes,
-                   void* stream) {
+// Validate the attention arguments of `batch` requests with `q_len` queries
+// each (a causal chunk; q_len = 1 is plain decode) and fill the launch
+// description.  The kernels see batch * q_len virtual requests; q and out
+// rows are (request, query) in that order.  Returns FP8PA_OK with
+// path->shape.batch == 0 when there is nothing to launch.
+int attention_prepare(const void* q, const uint8_t* k_cache, const uint8_t* v_cache,
+                      const float* k_scale, const float* v_scale, const int32_t* block_tables,
+                      int max_blocks_per_seq, const int32_t* seq_lens, int batch, int q_len,
+                      int block_size, int n_q_heads, int n_kv_heads, int head_dim,
+                      int head_dim_v, int fmt, int scale_mode, int group_size, float sm_scale,
+                      int num_blocks, void* out, int out_dtype, void* workspace,
+                      size_t workspace_bytes, DecodePath* path, DecodeArgs* a) {
   if (q_len <= 0 || batch < 0) return FP8PA_ERR_BAD_SHAPE;
   if (static_cast<long long>(batch) * q_len >= (1ll << 31)) return FP8PA_ERR_UNSUPPORTED;
-  DecodePath path = decode_path(batch * q_len, n_q_heads, n_kv_heads, head_dim, head_dim_v,
-                                block_size, max_blocks_per_seq, fmt, scale_mode, group_size,
-                                num_blocks, out_dtype);
-  if (path.status != FP8PA_OK) return path.status;
-  path.shape.qlen = q_len;
+  *path = decode_path(batch * q_len, n_q_heads, n_kv_heads, head_dim, head_dim_v, block_size,
+                      max_blocks_per_seq, fmt, scale_mode, group_size, num_blocks, out_dtype);
+  if (path->status != FP8PA_OK) return path->status;
+  path->shape.qlen = q_len;
   if (batch == 0) return FP8PA_OK;
   if (!q || !k_cache || !k_scale || !block_tables || !seq_lens || !out || !workspace)
     return FP8PA_ERR_NULL_POINTER;
-  if (path.shape.mla) {
+  if (path->shape.mla) {
     if (v_cache != k_cache || v_scale != k_scale) return FP8PA_ERR_UNSUPPORTED;
   } else if (!v_cache || !v_scale) {
     return FP8PA_ERR_NULL_POINTER;
@@ -151,29 +152,90 @@ int attention_impl(const void* q, const uint8_t* k_cache, const uint8_t* v_cache
   int dev = 0;
   uint32_t* err = device_error_ptr(&dev);
   if (!err) return FP8PA_ERR_CUDA;
-  path.shape.workers = decode_workers(path.shape, fmt, scale_mode, dev);
-  if (workspace_bytes < decode_workspace_bytes(path.shape)) return FP8PA_ERR_WORKSPACE;
-  DecodeArgs a{};
-  a.q = static_cast<const uint16_t*>(q);
-  a.k_cache = k_cache;
-  a.v_cache = v_cache;
-  a.k_scale = k_scale;
-  a.v_scale = v_scale;
-  a.block_tables = block_tables;
-  a.seq_lens = seq_lens;
-  a.num_blocks = num_blocks;
-  a.fmt = fmt;
-  a.mode = scale_mode;
-  a.gs = group_size;
-  a.out_dtype = out_dtype;
-  a.sm_scale = sm_scale;
-  a.out = out;
-  a.workspace = workspace;
-  a.err = err;
-  const cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const cudaError_t e = path.shape.mla ? launch_decode_mla(path.shape, a, st)
-                                       : launch_decode_gqa(path.shape, a, st);
-  return cuda_status(e);
+  path->shape.workers = decode_workers(path->shape, fmt, scale_mode, dev);
+  if (workspace_bytes < decode_workspace_bytes(path->shape)) return FP8PA_ERR_WORKSPACE;
+  *a = DecodeArgs{};
+  a->q = static_cast<const uint16_t*>(q);
+  a->k_cache = k_cache;
+  a->v_cache = v_cache;
+  a->k_scale = k_scale;
+  a->v_scale = v_scale;
+  a->block_tables = block_tables;
+  a->seq_lens = seq_lens;
+  a->num_blocks = num_blocks;
+  a->fmt = fmt;
+  a->mode = scale_mode;
+  a->gs = group_size;
+  a->out_dtype = out_dtype;
+  a->sm_scale = sm_scale;
+  a->out = out;
+  a->workspace = workspace;
+  a->err = err;
+  a->plan_ready = false;
+  return FP8PA_OK;
+}
+
+cudaError_t launch_decode(const DecodePath& path, const DecodeArgs& a, cudaStream_t st) {
+  return path.shape.mla ? launch_decode_mla(path.shape, a, st)
+                         : launch_decode_gqa(path.shape, a, st);
+}
+
+int attention_impl(const void* q, const uint8_t* k_cache, const uint8_t* v_cache,
+                   const float* k_scale, const float* v_scale, const int32_t* block_tables,
+                   int max_blocks_per_seq, const int32_t* seq_lens, int batch, int q_len,
+                   int block_size, int n_q_heads, int n_kv_heads, int head_dim, int head_dim_v,
+                   int fmt, int scale_mode, int group_size, float sm_scale, int num_blocks,
+                   void* out, int out_dtype, void* workspace, size_t workspace_bytes,
+                   void* stream) {
+  DecodePath path;
+  DecodeArgs a;
+  const int st = attention_prepare(q, k_cache, v_cache, k_scale, v_scale, block_tables,
+                                   max_blocks_per_seq, seq_lens, batch, q_len, block_size,
+                                   n_q_heads, n_kv_heads, head_dim, head_dim_v, fmt, scale_mode,
+                                   group_size, sm_scale, num_blocks, out, out_dtype, workspace,
+                                   workspace_bytes, &path, &a);
+  if (st != FP8PA_OK || batch == 0) return st;
+  return cuda_status(launch_decode(path, a, static_cast<cudaStream_t>(stream)));
+}
+
+// Validate the append arguments and fill `a` (its error word excluded).
+int append_prepare(const void* k, const void* v, const int32_t* slot_mapping, int num_tokens,
+                   int n_kv_heads, int head_dim, int fmt, int scale_mode, int group_size,
+                   uint8_t* k_cache, uint8_t* v_cache, float* k_scale, float* v_scale,
+                   int num_blocks, int block_size, AppendArgs* a) {
+  if (num_tokens < 0 || n_kv_heads <= 0 || head_dim <= 0 || num_blocks <= 0 || block_size <= 0)
+    return FP8PA_ERR_BAD_SHAPE;
+  if ((fmt != FP8PA_E4M3 && fmt != FP8PA_E5M2) ||
+      (scale_mode != FP8PA_SCALE_TOKEN_HEAD && scale_mode != FP8PA_SCALE_CHANNEL_STATIC &&
+       scale_mode != FP8PA_SCALE_TOKEN_GROUP))
+    return FP8PA_ERR_BAD_ENUM;
+  if (head_dim % 16 != 0 || head_dim > 768) return FP8PA_ERR_UNSUPPORTED;
+  if (scale_mode == FP8PA_SCALE_TOKEN_GROUP &&
+      (!pow2(group_size) || group_size < 16 || group_size > 256 || head_dim % group_size != 0))
+    return FP8PA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(num_blocks) * block_size >= (1ll << 31)) return FP8PA_ERR_UNSUPPORTED;
+  *a = AppendArgs{};
+  a->num_tokens = num_tokens;
+  if (num_tokens == 0) return FP8PA_OK;
+  if (!k || !slot_mapping || !k_cache || !k_scale) return FP8PA_ERR_NULL_POINTER;
+  if (v && (!v_cache || !v_scale)) return FP8PA_ERR_NULL_POINTER;
+  if (!aligned16(k) || !aligned16(k_cache) || (v && (!aligned16(v) || !aligned16(v_cache))) ||
+      !aligned16(k_scale) || (v && !aligned16(v_scale)))
+    return FP8PA_ERR_ALIGNMENT;
+  a->src[0] = static_cast<const uint16_t*>(k);
+  a->src[1] = static_cast<const uint16_t*>(v);
+  a->cache[0] = k_cache;
+  a->cache[1] = v_cache;
+  a->scale[0] = k_scale;
+  a->scale[1] = v_scale;
+  a->slot_mapping = slot_mapping;
+  a->hkv = n_kv_heads;
+  a->d = head_dim;
+  a->ntens = v ? 2 : 1;
+  a->gs = scale_mode == FP8PA_SCALE_TOKEN_GROUP ? group_size : head_dim;
+  a->num_blocks = num_blocks;
+  a->bs = block_size;
+  return FP8PA_OK;
 }
 
 }  // namespace
@@ -213,38 +275,11 @@ int fp8pa_kv_append_quant(const void* k, const void* v, const int32_t* slot_mapp
                           int num_tokens, int n_kv_heads, int head_dim, int fmt, int scale_mode,
                           int group_size, uint8_t* k_cache, uint8_t* v_cache, float* k_scale,
                           float* v_scale, int num_blocks, int block_size, void* stream) {
-  if (num_tokens < 0 || n_kv_heads <= 0 || head_dim <= 0 || num_blocks <= 0 || block_size <= 0)
-    return FP8PA_ERR_BAD_SHAPE;
-  if ((fmt != FP8PA_E4M3 && fmt != FP8PA_E5M2) ||
-      (scale_mode != FP8PA_SCALE_TOKEN_HEAD && scale_mode != FP8PA_SCALE_CHANNEL_STATIC &&
-       scale_mode != FP8PA_SCALE_TOKEN_GROUP))
-    return FP8PA_ERR_BAD_ENUM;
-  if (head_dim % 16 != 0 || head_dim > 768) return FP8PA_ERR_UNSUPPORTED;
-  if (scale_mode == FP8PA_SCALE_TOKEN_GROUP &&
-      (!pow2(group_size) || group_size < 16 || group_size > 256 || head_dim % group_size != 0))
-    return FP8PA_ERR_UNSUPPORTED;
-  if (static_cast<long long>(num_blocks) * block_size >= (1ll << 31)) return FP8PA_ERR_UNSUPPORTED;
-  if (num_tokens == 0) return FP8PA_OK;
-  if (!k || !slot_mapping || !k_cache || !k_scale) return FP8PA_ERR_NULL_POINTER;
-  if (v && (!v_cache || !v_scale)) return FP8PA_ERR_NULL_POINTER;
-  if (!aligned16(k) || !aligned16(k_cache) || (v && (!aligned16(v) || !aligned16(v_cache))) ||
-      !aligned16(k_scale) || (v && !aligned16(v_scale)))
-    return FP8PA_ERR_ALIGNMENT;
-  AppendArgs a{};
-  a.src[0] = static_cast<const uint16_t*>(k);
-  a.src[1] = static_cast<const uint16_t*>(v);
-  a.cache[0] = k_cache;
-  a.cache[1] = v_cache;
-  a.scale[0] = k_scale;
-  a.scale[1] = v_scale;
-  a.slot_mapping = slot_mapping;
-  a.num_tokens = num_tokens;
-  a.hkv = n_kv_heads;
-  a.d = head_dim;
-  a.ntens = v ? 2 : 1;
-  a.gs = scale_mode == FP8PA_SCALE_TOKEN_GROUP ? group_size : head_dim;
-  a.num_blocks = num_blocks;
-  a.bs = block_size;
+  AppendArgs a;
+  const int st = append_prepare(k, v, slot_mapping, num_tokens, n_kv_heads, head_dim, fmt,
+                                scale_mode, group_size, k_cache, v_cache, k_scale, v_scale,
+                                num_blocks, block_size, &a);
+  if (st != FP8PA_OK || num_tokens == 0) return st;
   a.err = device_error_ptr(nullptr);
   if (!a.err) return FP8PA_ERR_CUDA;
   return cuda_status(launch_append(a, fmt, scale_mode, static_cast<cudaStream_t>(stream)));
@@ -321,6 +356,46 @@ int fp8pa_paged_multiquery_attention(const void* q, const uint8_t* k_cache,
                         seq_lens, batch, q_len, block_size, n_q_heads, n_kv_heads, head_dim,
                         head_dim_v, fmt, scale_mode, group_size, sm_scale, num_blocks, out,
                         out_dtype, workspace, workspace_bytes, stream);
+}
+
+int fp8pa_decode_step(const void* k_new, const void* v_new, const int32_t* slot_mapping,
+                      int num_new_tokens, const void* q, uint8_t* k_cache, uint8_t* v_cache,
+                      float* k_scale, float* v_scale, const int32_t* block_tables,
+                      int max_blocks_per_seq, const int32_t* seq_lens, int batch, int q_len,
+                      int block_size, int n_q_heads, int n_kv_heads, int head_dim,
+                      int head_dim_v, int fmt, int scale_mode, int group_size, float sm_scale,
+                      int num_blocks, void* out, int out_dtype, void* workspace,
+                      size_t workspace_bytes, void* stream) {
+  AppendArgs ap;
+  int st = append_prepare(k_new, v_new, slot_mapping, num_new_tokens, n_kv_heads, head_dim, fmt,
+                          scale_mode, group_size, k_cache, v_cache, k_scale, v_scale, num_blocks,
+                          block_size, &ap);
+  if (st != FP8PA_OK) return st;
+  DecodePath path;
+  DecodeArgs a;
+  st = attention_prepare(q, k_cache, v_cache, k_scale, v_scale, block_tables, max_blocks_per_seq,
+                         seq_lens, batch, q_len, block_size, n_q_heads, n_kv_heads, head_dim,
+                         head_dim_v, fmt, scale_mode, group_size, sm_scale, num_blocks, out,
+                         out_dtype, workspace, workspace_bytes, &path, &a);
+  if (st != FP8PA_OK) return st;
+  const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  ap.err = device_error_ptr(nullptr);
+  if (!ap.err) return FP8PA_ERR_CUDA;
+  if (batch == 0)
+    return num_new_tokens == 0 ? FP8PA_OK : cuda_status(launch_append(ap, fmt, scale_mode, cs));
+  PlanArgs pl;
+  pl.seq_lens = seq_lens;
+  pl.batch = path.shape.batch;
+  pl.qlen = q_len;
+  pl.bs = plan_block_size(path.shape);
+  pl.max_blocks = max_blocks_per_seq;
+  pl.workers = plan_workers(path.shape);
+  pl.plan = static_cast<int*>(workspace);
+  pl.err = a.err;
+  cudaError_t e = launch_append_plan(ap, fmt, scale_mode, pl, cs);
+  if (e != cudaSuccess) return FP8PA_ERR_CUDA;
+  a.plan_ready = true;
+  return cuda_status(launch_decode(path, a, cs));
 }
 
 int fp8pa_get_device_error(void* stream, uint32_t* flags) {

@@ -16,6 +16,7 @@
 // cvt.rn.satfinite, so codes and scales are bit-exact with the definition.
 #include "common.cuh"
 #include "internal.h"
+#include "plan.cuh"
 
 namespace fp8pa {
 
@@ -32,12 +33,9 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float (&f)[8]) {
   }
 }
 
+// One (token, kv head, K-or-V) row per warp.
 template <int FMT, int MODE, int R>
-__global__ void __launch_bounds__(kAppendWarps * 32) append_kernel(AppendArgs a) {
-  griddep_wait();  // launched early (programmatic serialisation): inputs may be in flight
-  griddep_launch_dependents();
-  const int lane = threadIdx.x & 31;
-  const long row = static_cast<long>(blockIdx.x) * kAppendWarps + (threadIdx.x >> 5);
+__device__ __forceinline__ void append_row(const AppendArgs& a, long row, int lane) {
   const int per_tok = a.hkv * a.ntens;
   if (row >= static_cast<long>(a.num_tokens) * per_tok) return;
   const int t = static_cast<int>(row / per_tok);
@@ -122,11 +120,38 @@ __global__ void __launch_bounds__(kAppendWarps * 32) append_kernel(AppendArgs a)
   }
 }
 
+template <int FMT, int MODE, int R>
+__global__ void __launch_bounds__(kAppendWarps * 32) append_kernel(AppendArgs a) {
+  griddep_wait();  // launched early (programmatic serialisation): inputs may be in flight
+  griddep_launch_dependents();
+  append_row<FMT, MODE, R>(a, static_cast<long>(blockIdx.x) * kAppendWarps + (threadIdx.x >> 5),
+                           threadIdx.x & 31);
+}
+
+// A decode step's prologue in one launch: CTA 0's first warp plans the
+// split of the attention that follows, the other CTAs append the new rows.
+template <int FMT, int MODE, int R>
+__global__ void __launch_bounds__(kAppendWarps * 32) append_plan_kernel(AppendArgs a, PlanArgs pl) {
+  griddep_wait();
+  griddep_launch_dependents();
+  if (blockIdx.x == 0) {
+    if (threadIdx.x < 32)
+      plan_warp(pl.seq_lens, pl.batch, pl.qlen, 1, pl.bs, pl.max_blocks, pl.workers, pl.plan,
+                pl.err);
+    return;
+  }
+  append_row<FMT, MODE, R>(a,
+                           static_cast<long>(blockIdx.x - 1) * kAppendWarps + (threadIdx.x >> 5),
+                           threadIdx.x & 31);
+}
+
+// pl == nullptr: the append alone; else the fused append + plan prologue.
 template <int FMT, int MODE>
-cudaError_t launch_append_r(const AppendArgs& a, cudaStream_t stream) {
+cudaError_t launch_append_r(const AppendArgs& a, const PlanArgs* pl, cudaStream_t stream) {
   const long rows = static_cast<long>(a.num_tokens) * a.hkv * a.ntens;
-  if (rows == 0) return cudaSuccess;
-  const dim3 grid(static_cast<unsigned>((rows + kAppendWarps - 1) / kAppendWarps));
+  if (rows == 0 && !pl) return cudaSuccess;
+  const dim3 grid(
+      static_cast<unsigned>((rows + kAppendWarps - 1) / kAppendWarps + (pl ? 1 : 0)));
   const int nch = a.d / 8;
   cudaLaunchAttribute pdl[1];
   pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -137,20 +162,26 @@ cudaError_t launch_append_r(const AppendArgs& a, cudaStream_t stream) {
   cfg.stream = stream;
   cfg.attrs = pdl;
   cfg.numAttrs = 1;
+  if (pl) {
+    if (nch <= 32) return cudaLaunchKernelEx(&cfg, append_plan_kernel<FMT, MODE, 1>, a, *pl);
+    if (nch <= 64) return cudaLaunchKernelEx(&cfg, append_plan_kernel<FMT, MODE, 2>, a, *pl);
+    return cudaLaunchKernelEx(&cfg, append_plan_kernel<FMT, MODE, 3>, a, *pl);
+  }
   if (nch <= 32) return cudaLaunchKernelEx(&cfg, append_kernel<FMT, MODE, 1>, a);
   if (nch <= 64) return cudaLaunchKernelEx(&cfg, append_kernel<FMT, MODE, 2>, a);
   return cudaLaunchKernelEx(&cfg, append_kernel<FMT, MODE, 3>, a);
 }
 
 template <int FMT>
-cudaError_t launch_append_m(const AppendArgs& a, int mode, cudaStream_t stream) {
+cudaError_t launch_append_m(const AppendArgs& a, int mode, const PlanArgs* pl,
+                            cudaStream_t stream) {
   switch (mode) {
     case FP8PA_SCALE_TOKEN_HEAD:
-      return launch_append_r<FMT, FP8PA_SCALE_TOKEN_HEAD>(a, stream);
+      return launch_append_r<FMT, FP8PA_SCALE_TOKEN_HEAD>(a, pl, stream);
     case FP8PA_SCALE_CHANNEL_STATIC:
-      return launch_append_r<FMT, FP8PA_SCALE_CHANNEL_STATIC>(a, stream);
+      return launch_append_r<FMT, FP8PA_SCALE_CHANNEL_STATIC>(a, pl, stream);
     default:
-      return launch_append_r<FMT, FP8PA_SCALE_TOKEN_GROUP>(a, stream);
+      return launch_append_r<FMT, FP8PA_SCALE_TOKEN_GROUP>(a, pl, stream);
   }
 }
 
@@ -188,8 +219,14 @@ __global__ void chanscale_finalize_kernel(const float* amax, float* s, int hd) {
 }  // namespace
 
 cudaError_t launch_append(const AppendArgs& a, int fmt, int mode, cudaStream_t stream) {
-  return fmt == FP8PA_E4M3 ? launch_append_m<FP8PA_E4M3>(a, mode, stream)
-                           : launch_append_m<FP8PA_E5M2>(a, mode, stream);
+  return fmt == FP8PA_E4M3 ? launch_append_m<FP8PA_E4M3>(a, mode, nullptr, stream)
+                           : launch_append_m<FP8PA_E5M2>(a, mode, nullptr, stream);
+}
+
+cudaError_t launch_append_plan(const AppendArgs& a, int fmt, int mode, const PlanArgs& pl,
+                               cudaStream_t stream) {
+  return fmt == FP8PA_E4M3 ? launch_append_m<FP8PA_E4M3>(a, mode, &pl, stream)
+                           : launch_append_m<FP8PA_E5M2>(a, mode, &pl, stream);
 }
 
 cudaError_t launch_channel_absmax(const uint16_t* x, int num_tokens, int hd, float* amax,

@@ -33,6 +33,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "plan.cuh"
 
 namespace fp8pa {
 
@@ -43,72 +44,13 @@ constexpr int kMaxWarps = 8;  // warps per CTA: one per KV head of the CTA's hea
 __device__ __forceinline__ int ld_i32(const int* p) { return *reinterpret_cast<const volatile int*>(p); }
 
 // ---------------------------------------------------------------- planner
-// Workspace header: [0] U = total units, [1] units per worker, [4..] unit
-// prefix per request (B+1 ints), then segment base per (b, kv head)
-// (B*Hkv+1 ints).  Partial buffers follow at 256-byte aligned offsets.
-constexpr int kPlanHeader = 4;
-
-__device__ __forceinline__ int warp_incl_scan(int x) {
-  const int lane = threadIdx.x & 31;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int t = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += t;
-  }
-  return x;
-}
-
-// One warp: unit prefix per request, units per worker, and the base index of
-// each (request, kv head)'s partials.  Lets the split kernel launch at once.
+// One warp; lets the split kernel launch at once (it waits for the plan).
 __global__ void __launch_bounds__(32) plan_kernel(const int32_t* seq_lens, int B, int qlen,
-                                                  int hkv, int bs, int max_blocks, int workers,
+                                                  int groups, int bs, int max_blocks, int workers,
                                                   int* ws, uint32_t* err) {
   griddep_wait();  // inputs may come from the kernel before us in the stream
   griddep_launch_dependents();
-  const int lane = threadIdx.x;
-  const int cap = max_blocks * bs;
-  int* uprefix = ws + kPlanHeader;
-  int* segbase = uprefix + B + 1;
-  int carry = 0;
-  for (int base = 0; base < B; base += 32) {
-    const int b = base + lane;
-    int n = 0;
-    if (b < B) {
-      bool bad;
-      const int L = visible_len(seq_lens, b, qlen, cap, &bad);
-      if (bad) raise_error(err, FP8PA_DEVERR_SEQ_LEN);
-      n = (L + bs - 1) / bs;
-    }
-    const int incl = warp_incl_scan(n);
-    if (b < B) uprefix[b] = (carry + incl - n) * hkv;
-    carry += __shfl_sync(0xffffffffu, incl, 31);
-  }
-  const int U = carry * hkv;
-  const int upw = max(1, (U + workers - 1) / workers);
-  if (lane == 0) {
-    uprefix[B] = U;
-    ws[0] = U;
-    ws[1] = upw;
-  }
-  __syncwarp();
-  carry = 0;
-  const int E = B * hkv;
-  for (int base = 0; base < E; base += 32) {
-    const int e = base + lane;
-    int segs = 0;
-    if (e < E) {
-      const int b = e / hkv, kvh = e % hkv;
-      const int nb = (uprefix[b + 1] - uprefix[b]) / hkv;
-      if (nb > 0) {
-        const int fu = uprefix[b] + kvh * nb;
-        segs = (fu + nb - 1) / upw - fu / upw + 1;
-      }
-    }
-    const int incl = warp_incl_scan(segs);
-    if (e < E) segbase[e] = carry + incl - segs;
-    carry += __shfl_sync(0xffffffffu, incl, 31);
-  }
-  if (lane == 0) segbase[E] = carry;
+  plan_warp(seq_lens, B, qlen, groups, bs, max_blocks, workers, ws, err);
 }
 
 // ---------------------------------------------------------------- split kernel
@@ -600,7 +542,7 @@ template <int DV>
 __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const MergeParams p) {
   constexpr int PER = DV / 32;
   __shared__ float s_acc[kMergeWarps][DV];
-  __shared__ float s_l[kMergeWarps];
+  __shared__ float s_ml[kMergeWarps][2];
   griddep_wait();
   griddep_launch_dependents();
   const int row = blockIdx.x;
@@ -616,43 +558,53 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const MergePara
                          : static_cast<long>(s) * p.G + hh;
   };
   const float NEG_INF = __int_as_float(0xff800000);
-  float M = NEG_INF;
-  for (int s = sb + lane; s < se; s += 32) M = fmaxf(M, p.part_ml[prow(s) * 2]);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  // One pass per warp over its pieces with a running maximum: the pieces'
+  // loads do not wait on a global maximum first.
+  float M = NEG_INF, L = 0.f;
   float acc[PER];
 #pragma unroll
   for (int e = 0; e < PER; ++e) acc[e] = 0.f;
-  float L = 0.f;
-  if (M != NEG_INF) {
-#pragma unroll 4
-    for (int s = sb + warp; s < se; s += kMergeWarps) {
-      const long r = prow(s);
-      const float2 ml = *reinterpret_cast<const float2*>(p.part_ml + r * 2);
-      const float wgt = ex2(ml.x - M);
-      L += wgt * ml.y;
-      const float2* po = reinterpret_cast<const float2*>(p.part_o + r * DV + lane * PER);
+#pragma unroll 2
+  for (int s = sb + warp; s < se; s += kMergeWarps) {
+    const long r = prow(s);
+    const float2 ml = *reinterpret_cast<const float2*>(p.part_ml + r * 2);
+    const float2* po = reinterpret_cast<const float2*>(p.part_o + r * DV + lane * PER);
+    float2 v[PER / 2];
 #pragma unroll
-      for (int e = 0; e < PER / 2; ++e) {
-        const float2 v = po[e];
-        acc[2 * e] += wgt * v.x;
-        acc[2 * e + 1] += wgt * v.y;
-      }
+    for (int e = 0; e < PER / 2; ++e) v[e] = po[e];
+    if (ml.x == NEG_INF) continue;  // a piece that saw no token
+    const float mn = fmaxf(M, ml.x);
+    const float a = ex2(M - mn), wgt = ex2(ml.x - mn);  // ex2(-inf) = 0
+    M = mn;
+    L = L * a + wgt * ml.y;
+#pragma unroll
+    for (int e = 0; e < PER / 2; ++e) {
+      acc[2 * e] = acc[2 * e] * a + wgt * v[e].x;
+      acc[2 * e + 1] = acc[2 * e + 1] * a + wgt * v[e].y;
     }
   }
 #pragma unroll
   for (int e = 0; e < PER; ++e) s_acc[warp][lane * PER + e] = acc[e];
-  if (lane == 0) s_l[warp] = L;
+  if (lane == 0) {
+    s_ml[warp][0] = M;
+    s_ml[warp][1] = L;
+  }
   __syncthreads();
   if (warp != 0) return;
-  float Lt = 0.f;
+  float Mt = NEG_INF;
 #pragma unroll
-  for (int w = 0; w < kMergeWarps; ++w) Lt += s_l[w];
+  for (int w = 0; w < kMergeWarps; ++w) Mt = fmaxf(Mt, s_ml[w][0]);
+  float f[kMergeWarps], Lt = 0.f;
+#pragma unroll
+  for (int w = 0; w < kMergeWarps; ++w) {
+    f[w] = Mt == NEG_INF ? 0.f : ex2(s_ml[w][0] - Mt);
+    Lt += f[w] * s_ml[w][1];
+  }
 #pragma unroll
   for (int e = 0; e < PER; ++e) {
     float v = 0.f;
 #pragma unroll
-    for (int w = 0; w < kMergeWarps; ++w) v += s_acc[w][lane * PER + e];
+    for (int w = 0; w < kMergeWarps; ++w) v += f[w] * s_acc[w][lane * PER + e];
     acc[e] = v;
   }
   const float inv = Lt > 0.f ? 1.0f / Lt : 0.f;
@@ -795,9 +747,11 @@ cudaError_t launch_decode_gqa(const DecodeShape& s, const DecodeArgs& a, cudaStr
   float* part_ml = reinterpret_cast<float*>(ws + plan_bytes);
   float* part_o = reinterpret_cast<float*>(ws + plan_bytes + align256(prow * 2 * sizeof(float)));
 
-  e = launch_plan(a.seq_lens, s.batch, s.qlen, 1, s.bs, s.max_blocks, s.workers, plan, a.err,
-                  stream);
-  if (e != cudaSuccess) return e;
+  if (!a.plan_ready) {
+    e = launch_plan(a.seq_lens, s.batch, s.qlen, 1, s.bs, s.max_blocks, s.workers, plan, a.err,
+                    stream);
+    if (e != cudaSuccess) return e;
+  }
   // Every kernel of the decode is launched with programmatic stream
   // serialisation: it may start while its predecessor drains, and waits
   // (griddepcontrol.wait) before reading anything that predecessor wrote.

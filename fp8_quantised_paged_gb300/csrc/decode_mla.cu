@@ -31,6 +31,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "plan.cuh"
 
 namespace fp8pa {
 
@@ -44,7 +45,6 @@ constexpr int kPStride = 68;                     // padded fp32 P row
 constexpr int kCodeBytes = kBs * kDk;            // 36,864
 constexpr int kScaleBytes = kBs * kGroups * 4;   // 2,304
 constexpr int kStageBytes = kCodeBytes + kScaleBytes;
-constexpr int kPlanHeader = 4;
 
 struct MlaSmem {
   static constexpr int kStages = 0;                                     // 2 x stage
@@ -490,9 +490,11 @@ cudaError_t launch_decode_mla(const DecodeShape& s, const DecodeArgs& a, cudaStr
   float* part_ml = reinterpret_cast<float*>(ws + plan_bytes);
   float* part_o = reinterpret_cast<float*>(ws + plan_bytes + align256(rows * 2 * sizeof(float)));
 
-  e = launch_plan(a.seq_lens, s.batch, s.qlen, 1, kBs, s.max_blocks, ranges, plan, a.err,
-                  stream);
-  if (e != cudaSuccess) return e;
+  if (!a.plan_ready) {
+    e = launch_plan(a.seq_lens, s.batch, s.qlen, 1, kBs, s.max_blocks, ranges, plan, a.err,
+                    stream);
+    if (e != cudaSuccess) return e;
+  }
   MlaParams p;
   p.q = a.q;
   p.cache = a.k_cache;

@@ -19,6 +19,18 @@ struct AppendArgs {
 };
 
 cudaError_t launch_append(const AppendArgs& a, int fmt, int mode, cudaStream_t stream);
+
+// The planner's inputs (see plan.cuh); `plan` is the head of the workspace.
+struct PlanArgs {
+  const int32_t* seq_lens;
+  int batch, qlen, bs, max_blocks, workers;
+  int* plan;
+  uint32_t* err;
+};
+
+// Append and plan in one launch (the prologue of fp8pa_decode_step).
+cudaError_t launch_append_plan(const AppendArgs& a, int fmt, int mode, const PlanArgs& pl,
+                               cudaStream_t stream);
 cudaError_t launch_channel_scales(const uint16_t* x, int num_tokens, int hd, int fmt, float* out,
                                   cudaStream_t stream);
 cudaError_t launch_channel_absmax(const uint16_t* x, int num_tokens, int hd, float* amax,
@@ -49,7 +61,13 @@ struct DecodeArgs {
   void* out;
   void* workspace;
   uint32_t* err;
+  bool plan_ready;  // the workspace already holds this call's plan
 };
+
+// Page ranges the planner cuts for this shape (its `workers`), and the
+// block size of the pages it counts.
+inline int plan_workers(const DecodeShape& s) { return s.mla ? s.workers / (s.hq / 32) : s.workers; }
+inline int plan_block_size(const DecodeShape& s) { return s.mla ? 64 : s.bs; }
 
 int decode_workers(const DecodeShape& s, int fmt, int mode, int device);
 

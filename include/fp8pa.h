@@ -233,6 +233,30 @@ int fp8pa_paged_multiquery_attention(const void* q, const uint8_t* k_cache,
                                      void* stream);
 
 /*
+ * One decode step in one call: the append of fp8pa_kv_append_quant
+ * (k_new, v_new, slot_mapping, num_new_tokens into the cache), then the
+ * attention of fp8pa_paged_multiquery_attention over the updated cache
+ * (q_len = 1: fp8pa_paged_decode_attention).  The result equals the two
+ * calls made in that order, bit for bit; the split planner runs inside the
+ * append's launch, so the step is three kernel launches instead of four.
+ * Defined by: the two steps of the decode path, append then attend
+ * ("Llama 3 70B FP8 deployment", dpshk.com/news/5605006, sec. 3.2: decode
+ * quantises each new KV with the current scale; "DeepSeek-V4.1 512K",
+ * hotelren.com/news/5711065, sec. 3.3: paged KV blocks).
+ * Arguments, layouts, errors: those of the two calls; the cache and scale
+ * tensors are shared by both.  Nothing is launched if either argument set
+ * is rejected.
+ */
+int fp8pa_decode_step(const void* k_new, const void* v_new, const int32_t* slot_mapping,
+                      int num_new_tokens, const void* q, uint8_t* k_cache, uint8_t* v_cache,
+                      float* k_scale, float* v_scale, const int32_t* block_tables,
+                      int max_blocks_per_seq, const int32_t* seq_lens, int batch, int q_len,
+                      int block_size, int n_q_heads, int n_kv_heads, int head_dim,
+                      int head_dim_v, int fmt, int scale_mode, int group_size, float sm_scale,
+                      int num_blocks, void* out, int out_dtype, void* workspace,
+                      size_t workspace_bytes, void* stream);
+
+/*
  * Size of the scratch array built into the library for
  * fp8pa_paged_decode_attention_static_ws (16 MiB per device that uses it).
  */

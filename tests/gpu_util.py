@@ -59,10 +59,11 @@ def n_scale_groups(w):
     return w.head_dim // w.group_size if w.scale_mode == W.SCALE_TOKEN_GROUP else 1
 
 
-def gpu_cache(w, F, kvs=None):
-    """Prefill all but the last token of every request with one append call,
-    then append each request's last token with a second call (the decode
-    step).  Returns device tensors (k_cache, v_cache, k_scale, v_scale)."""
+def gpu_cache(w, F, kvs=None, step=True, back=1):
+    """Prefill all but the last `back` tokens of every request with one
+    append call, then (step=True, back=1) append each request's last token
+    with a second call (the decode step).  Returns device tensors
+    (k_cache, v_cache, k_scale, v_scale)."""
     nb, hkv, bs, d = w.num_blocks, w.n_kv_heads, w.block_size, w.head_dim
     kc = torch.zeros((nb, hkv, bs, d), dtype=torch.uint8, device=DEV)
     vc = None if w.mla else torch.zeros_like(kc)
@@ -77,14 +78,17 @@ def gpu_cache(w, F, kvs=None):
     pk, pv, ps = [], [], []
     for b, (k, v) in enumerate(kvs):
         L = int(w.seq_lens[b])
-        pk.append(k[:L - 1])
+        n = max(L - back, 0)
+        pk.append(k[:n])
         if v is not None:
-            pv.append(v[:L - 1])
-        ps.append(W.token_slots(w, b, 0, L - 1))
+            pv.append(v[:n])
+        ps.append(W.token_slots(w, b, 0, n))
     F.kv_append_quant(to_dev_bf16(np.concatenate(pk)),
                       None if w.mla else to_dev_bf16(np.concatenate(pv)),
                       torch.from_numpy(np.concatenate(ps)).to(DEV), kc, vc, ks, vs, fmt=w.fmt,
                       scale_mode=w.scale_mode, group_size=w.group_size)
+    if not step:
+        return (kc, kc, ks, ks) if w.mla else (kc, vc, ks, vs)
     sk = np.stack([k[-1] for k, _ in kvs])
     sv = None if w.mla else np.stack([v[-1] for _, v in kvs])
     F.kv_append_quant(to_dev_bf16(sk), None if w.mla else to_dev_bf16(sv),
