@@ -377,28 +377,37 @@ def run_gpu(args, rank, world, local_rank):
     # ---- end to end through the public API with pinned host buffers
     e2e = None
     if not args.no_e2e:
-        def pin(a):
-            return torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
-        q_p = pin(q_h.view(np.int16))
-        kn_p = pin(kn_h.view(np.int16))
-        vn_p = None if w.mla else pin(vn_h.view(np.int16))
-        sl_p = pin(w.seq_lens)
-        slot_p = pin(slot_h)
+        # The step's inputs (q, new K/V rows, slots, lengths) are staged in
+        # one pinned host buffer and copied in one transfer to a device
+        # buffer holding the same layout, as a serving loop would.
+        parts = [q_h.view(np.uint8).reshape(-1), kn_h.view(np.uint8).reshape(-1),
+                 None if w.mla else vn_h.view(np.uint8).reshape(-1),
+                 slot_h.view(np.uint8).reshape(-1), w.seq_lens.view(np.uint8).reshape(-1)]
+        offs, total = [], 0
+        for a in parts:
+            offs.append(total)
+            total += 0 if a is None else (a.size + 255) // 256 * 256
+        host = torch.zeros(total, dtype=torch.uint8).pin_memory()
+        hv = host.numpy()
+        for o, a in zip(offs, parts):
+            if a is not None:
+                hv[o:o + a.size] = a
+        dbuf = torch.empty(total, dtype=torch.uint8, device=dev)
+
+        def dview(k, dtype, shape):
+            n = int(np.prod(shape)) * torch.tensor([], dtype=dtype).element_size()
+            return dbuf[offs[k]:offs[k] + n].view(dtype).view(shape)
+        qd = dview(0, torch.bfloat16, q.shape)
+        knd = dview(1, torch.bfloat16, kn.shape)
+        vnd = None if w.mla else dview(2, torch.bfloat16, vn.shape)
+        slotd = dview(3, torch.int32, slots.shape)
+        sld = dview(4, torch.int32, sl.shape)
         out_p = torch.empty(out.shape, dtype=torch.bfloat16).pin_memory()
-        qd, knd = torch.empty_like(q), torch.empty_like(kn)
-        vnd = None if w.mla else torch.empty_like(vn)
-        sld, slotd = torch.empty_like(sl), torch.empty_like(slots)
-        h2d = q_p.numel() * 2 + kn_p.numel() * 2 + (0 if vn_p is None else vn_p.numel() * 2) \
-            + sl_p.numel() * 4 + slot_p.numel() * 4
+        h2d = total
         d2h = out_p.numel() * 2
 
         def e2e_step():
-            qd.view(torch.int16).copy_(q_p, non_blocking=True)
-            knd.view(torch.int16).copy_(kn_p, non_blocking=True)
-            if vnd is not None:
-                vnd.view(torch.int16).copy_(vn_p, non_blocking=True)
-            sld.copy_(sl_p, non_blocking=True)
-            slotd.copy_(slot_p, non_blocking=True)
+            dbuf.copy_(host, non_blocking=True)
             step(qd, knd, vnd, slotd, sld)
             out_p.copy_(out, non_blocking=True)
             torch.cuda.current_stream().synchronize()

@@ -33,6 +33,22 @@ def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
+class _Nop:
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *a):
+        return False
+
+
+_NOP = _Nop()
+
+
+def _on(dev):
+    """Make `dev` current for a call (a no-op when it already is)."""
+    return _NOP if dev.index == torch.cuda.current_device() else torch.cuda.device(dev)
+
+
 def _need(t, dtype, name, device=None):
     if t is None:
         return
@@ -74,7 +90,7 @@ def kv_append_quant(k, v, slot_mapping, k_cache, v_cache, k_scale, v_scale, fmt=
     _need(v_scale, torch.float32, "v_scale", dev)
     n, hkv, d = k.shape
     nb, _, bs, _ = k_cache.shape
-    with torch.cuda.device(dev):
+    with _on(dev):
         rc = N.lib.fp8pa_kv_append_quant(_ptr(k), _ptr(v), _ptr(slot_mapping), n, hkv, d, fmt,
                                          scale_mode, group_size, _ptr(k_cache), _ptr(v_cache),
                                          _ptr(k_scale), _ptr(v_scale), nb, bs, _stream(stream))
@@ -157,10 +173,12 @@ def paged_decode_attention(q, k_cache, v_cache, k_scale, v_scale, block_tables, 
     if out.dtype not in (torch.float32, torch.bfloat16):
         raise TypeError("out must be bf16 or float32")
     _need(out, out.dtype, "out", dev)
-    with torch.cuda.device(dev):
-        need = int(N.lib.fp8pa_decode_workspace_bytes(B, hq, n_kv_heads, dk, dv, bs, max_blocks))
-        if workspace is None and need > 0:
-            workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    with _on(dev):
+        if workspace is None:
+            need = int(N.lib.fp8pa_decode_workspace_bytes(B, hq, n_kv_heads, dk, dv, bs,
+                                                          max_blocks))
+            if need > 0:
+                workspace = torch.empty(need, dtype=torch.uint8, device=dev)
         # need == 0 means the shapes are rejected: the call below returns the
         # precise status code.
         _need(workspace, torch.uint8, "workspace", dev)
@@ -198,11 +216,12 @@ def paged_multiquery_attention(q, k_cache, v_cache, k_scale, v_scale, block_tabl
         raise TypeError("out must be bf16 or float32")
     odt = OUT_F32 if out.dtype == torch.float32 else OUT_BF16
     _need(out, out.dtype, "out", dev)
-    with torch.cuda.device(dev):
-        need = int(N.lib.fp8pa_decode_workspace_bytes(B * qlen, hq, n_kv_heads, dk, dv, bs,
-                                                      max_blocks))
-        if workspace is None and need > 0:
-            workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    with _on(dev):
+        if workspace is None:
+            need = int(N.lib.fp8pa_decode_workspace_bytes(B * qlen, hq, n_kv_heads, dk, dv, bs,
+                                                          max_blocks))
+            if need > 0:
+                workspace = torch.empty(need, dtype=torch.uint8, device=dev)
         _need(workspace, torch.uint8, "workspace", dev)
         rc = N.lib.fp8pa_paged_multiquery_attention(
             _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
@@ -244,11 +263,12 @@ def decode_step(k_new, v_new, slot_mapping, q, k_cache, v_cache, k_scale, v_scal
         raise TypeError("out must be bf16 or float32")
     odt = OUT_F32 if out.dtype == torch.float32 else OUT_BF16
     _need(out, out.dtype, "out", dev)
-    with torch.cuda.device(dev):
-        need = int(N.lib.fp8pa_decode_workspace_bytes(B * qlen, hq, n_kv_heads, dk, dv, bs,
-                                                      max_blocks))
-        if workspace is None and need > 0:
-            workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    with _on(dev):
+        if workspace is None:
+            need = int(N.lib.fp8pa_decode_workspace_bytes(B * qlen, hq, n_kv_heads, dk, dv, bs,
+                                                          max_blocks))
+            if need > 0:
+                workspace = torch.empty(need, dtype=torch.uint8, device=dev)
         _need(workspace, torch.uint8, "workspace", dev)
         rc = N.lib.fp8pa_decode_step(
             _ptr(k_new), _ptr(v_new), _ptr(slot_mapping), n_new, _ptr(q), _ptr(k_cache),

@@ -4,6 +4,8 @@
 #include <cudaTypedefs.h>
 
 #include <mutex>
+#include <utility>
+#include <vector>
 
 #include "common.cuh"
 #include "internal.h"
@@ -39,6 +41,64 @@ bool pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? FP8PA_OK : FP8PA_ERR_CUDA; }
 
 }  // namespace
+
+// Per-device host caches of the launch set-up that does not change between
+// calls: the SM count, the dynamic shared-memory opt-in of each kernel, and
+// each kernel's resident CTAs per SM.
+namespace {
+struct FnKey {
+  int dev;
+  const void* fn;
+  int threads, smem;
+};
+std::mutex g_cache_mu;
+int g_sms[kMaxDevices] = {0};
+std::vector<std::pair<FnKey, int>> g_occ;  // (key, CTAs per SM)
+std::vector<FnKey> g_attr;                 // smem opt-ins already made
+}  // namespace
+
+int sm_count(int dev) {
+  if (dev < 0 || dev >= kMaxDevices) return 1;
+  std::lock_guard<std::mutex> lock(g_cache_mu);
+  if (g_sms[dev] <= 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      return 1;
+    g_sms[dev] = n;
+  }
+  return g_sms[dev];
+}
+
+cudaError_t ensure_smem_attr(const void* fn, int smem) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_cache_mu);
+  for (const FnKey& k : g_attr)
+    if (k.dev == dev && k.fn == fn && k.smem >= smem) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e == cudaSuccess) g_attr.push_back(FnKey{dev, fn, 0, smem});
+  return e;
+}
+
+int ctas_per_sm(const void* fn, int threads, int smem) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  {
+    std::lock_guard<std::mutex> lock(g_cache_mu);
+    for (const auto& kv : g_occ)
+      if (kv.first.dev == dev && kv.first.fn == fn && kv.first.threads == threads &&
+          kv.first.smem == smem)
+        return kv.second;
+  }
+  if (ensure_smem_attr(fn, smem) != cudaSuccess) return 1;
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, threads, smem) != cudaSuccess ||
+      per_sm <= 0)
+    return 1;
+  std::lock_guard<std::mutex> lock(g_cache_mu);
+  g_occ.push_back({FnKey{dev, fn, threads, smem}, per_sm});
+  return per_sm;
+}
 
 bool encode_tensor_map_2d_u8(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows,
                              uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle swz) {

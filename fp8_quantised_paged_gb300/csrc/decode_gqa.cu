@@ -522,106 +522,6 @@ __global__ void __launch_bounds__(kMaxWarps * 32)
   }
 }
 
-// ---------------------------------------------------------------- merge
-struct MergeParams {
-  const int* plan;
-  const float* part_ml;
-  const float* part_o;
-  void* out;
-  int B, hq, hkv, G, dv, out_f32;
-  // 0: pieces are numbered per (request, group) (GQA planner with KV heads as
-  // groups); 1: per request, with the group folded into the piece row (MLA).
-  int per_request;
-};
-
-// One CTA of kMergeWarps warps per output row (b, h): the warps share the
-// row's pieces round-robin, then combine through shared memory.
-constexpr int kMergeWarps = 4;
-
-template <int DV>
-__global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const MergeParams p) {
-  constexpr int PER = DV / 32;
-  __shared__ float s_acc[kMergeWarps][DV];
-  __shared__ float s_ml[kMergeWarps][2];
-  griddep_wait();
-  griddep_launch_dependents();
-  const int row = blockIdx.x;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int b = row / p.hq, h = row % p.hq;
-  const int kvh = h / p.G, hh = h % p.G;
-  const int* segbase = p.plan + kPlanHeader + p.B + 1;
-  const int e0 = p.per_request ? b : b * p.hkv + kvh;
-  const int sb = segbase[e0], se = segbase[e0 + 1];
-  // row of piece s for this head
-  auto prow = [&](int s) -> long {
-    return p.per_request ? (static_cast<long>(s) * p.hkv + kvh) * p.G + hh
-                         : static_cast<long>(s) * p.G + hh;
-  };
-  const float NEG_INF = __int_as_float(0xff800000);
-  // One pass per warp over its pieces with a running maximum: the pieces'
-  // loads do not wait on a global maximum first.
-  float M = NEG_INF, L = 0.f;
-  float acc[PER];
-#pragma unroll
-  for (int e = 0; e < PER; ++e) acc[e] = 0.f;
-#pragma unroll 2
-  for (int s = sb + warp; s < se; s += kMergeWarps) {
-    const long r = prow(s);
-    const float2 ml = *reinterpret_cast<const float2*>(p.part_ml + r * 2);
-    const float2* po = reinterpret_cast<const float2*>(p.part_o + r * DV + lane * PER);
-    float2 v[PER / 2];
-#pragma unroll
-    for (int e = 0; e < PER / 2; ++e) v[e] = po[e];
-    if (ml.x == NEG_INF) continue;  // a piece that saw no token
-    const float mn = fmaxf(M, ml.x);
-    const float a = ex2(M - mn), wgt = ex2(ml.x - mn);  // ex2(-inf) = 0
-    M = mn;
-    L = L * a + wgt * ml.y;
-#pragma unroll
-    for (int e = 0; e < PER / 2; ++e) {
-      acc[2 * e] = acc[2 * e] * a + wgt * v[e].x;
-      acc[2 * e + 1] = acc[2 * e + 1] * a + wgt * v[e].y;
-    }
-  }
-#pragma unroll
-  for (int e = 0; e < PER; ++e) s_acc[warp][lane * PER + e] = acc[e];
-  if (lane == 0) {
-    s_ml[warp][0] = M;
-    s_ml[warp][1] = L;
-  }
-  __syncthreads();
-  if (warp != 0) return;
-  float Mt = NEG_INF;
-#pragma unroll
-  for (int w = 0; w < kMergeWarps; ++w) Mt = fmaxf(Mt, s_ml[w][0]);
-  float f[kMergeWarps], Lt = 0.f;
-#pragma unroll
-  for (int w = 0; w < kMergeWarps; ++w) {
-    f[w] = Mt == NEG_INF ? 0.f : ex2(s_ml[w][0] - Mt);
-    Lt += f[w] * s_ml[w][1];
-  }
-#pragma unroll
-  for (int e = 0; e < PER; ++e) {
-    float v = 0.f;
-#pragma unroll
-    for (int w = 0; w < kMergeWarps; ++w) v += f[w] * s_acc[w][lane * PER + e];
-    acc[e] = v;
-  }
-  const float inv = Lt > 0.f ? 1.0f / Lt : 0.f;
-  const long ob = (static_cast<long>(b) * p.hq + h) * DV + lane * PER;
-  if (p.out_f32) {
-    float* o = reinterpret_cast<float*>(p.out) + ob;
-#pragma unroll
-    for (int e = 0; e < PER; ++e) o[e] = acc[e] * inv;
-  } else {
-    __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(p.out) + ob;
-#pragma unroll
-    for (int e = 0; e < PER; e += 2)
-      *reinterpret_cast<__nv_bfloat162*>(o + e) =
-          __floats2bfloat162_rn(acc[e] * inv, acc[e + 1] * inv);
-  }
-}
-
 // ---------------------------------------------------------------- host side
 // Stages of one warp's ring: 8 KB of K+V pages (2 stages at head_dim 128,
 // block 16).  Registers hold 16 warps per SM; one page in flight per warp
@@ -686,9 +586,7 @@ cudaEvent_t g_split_ev_start = nullptr, g_split_ev_stop = nullptr;
 // Number of page ranges the planner cuts (GQA: one per resident CTA over the
 // head sets; MLA: one per SM over the head groups, times the head groups).
 int decode_workers(const DecodeShape& s, int fmt, int mode, int device) {
-  int sms = 0;
-  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess || sms <= 0)
-    sms = 1;
+  const int sms = sm_count(device);
   if (s.mla) {
     // one 202 KB CTA per SM; a whole number of head-group sets (H = Hq / 32)
     const int H = s.hq / 32;
@@ -698,13 +596,7 @@ int decode_workers(const DecodeShape& s, int fmt, int mode, int device) {
   if (g_decode_workers_override > 0) return g_decode_workers_override;
   const int wpc = gqa_wpc(s.hkv), hsets = s.hkv / wpc;
   const SplitKernel k = pick(s.d, s.bs, fmt, mode);
-  cudaFuncSetAttribute(reinterpret_cast<const void*>(k.fn),
-                       cudaFuncAttributeMaxDynamicSharedMemorySize, k.smem(wpc));
-  int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, reinterpret_cast<const void*>(k.fn),
-                                                    wpc * 32, k.smem(wpc)) != cudaSuccess ||
-      per_sm <= 0)
-    per_sm = 1;
+  const int per_sm = ctas_per_sm(reinterpret_cast<const void*>(k.fn), wpc * 32, k.smem(wpc));
   const int ranges = sms * per_sm / hsets;
   return ranges < 1 ? 1 : ranges;
 }
@@ -728,8 +620,7 @@ cudaError_t launch_decode_gqa(const DecodeShape& s, const DecodeArgs& a, cudaStr
   const int wpc = gqa_wpc(s.hkv), hsets = s.hkv / wpc;
   const SplitKernel k = pick(s.d, s.bs, a.fmt, a.mode);
   const int smem = k.smem(wpc);
-  cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(k.fn),
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(k.fn), smem);
   if (e != cudaSuccess) return e;
 
   CUtensorMap tmk, tmv;
@@ -806,31 +697,6 @@ cudaError_t launch_plan(const int32_t* seq_lens, int batch, int qlen, int groups
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, plan_kernel, seq_lens, batch, qlen, groups, bs, max_blocks,
                             workers, plan, err);
-}
-
-cudaError_t launch_merge(const int* plan, const float* part_ml, const float* part_o, void* out,
-                         int batch, int hq, int groups, int G, int dv, int out_dtype,
-                         bool pieces_per_request, cudaStream_t stream) {
-  cudaLaunchAttribute pdl[1];
-  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  pdl[0].val.programmaticStreamSerializationAllowed = 1;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(batch * hq);
-  cfg.blockDim = dim3(kMergeWarps * 32);
-  cfg.stream = stream;
-  cfg.attrs = pdl;
-  cfg.numAttrs = 1;
-  MergeParams mp{plan,      part_ml, part_o, out, batch, hq, groups, G, dv, out_dtype,
-                 pieces_per_request ? 1 : 0};
-  cudaError_t e;
-  if (dv == 128)
-    e = cudaLaunchKernelEx(&cfg, merge_kernel<128>, mp);
-  else if (dv == 64)
-    e = cudaLaunchKernelEx(&cfg, merge_kernel<64>, mp);
-  else
-    e = cudaLaunchKernelEx(&cfg, merge_kernel<512>, mp);
-  if (e != cudaSuccess) return e;
-  return cudaGetLastError();
 }
 
 }  // namespace fp8pa

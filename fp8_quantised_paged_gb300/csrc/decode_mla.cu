@@ -479,9 +479,7 @@ cudaError_t launch_decode_mla(const DecodeShape& s, const DecodeArgs& a, cudaStr
   const int ranges = s.workers / H;
   const int smem = MlaSmem::kBytes;
   auto kfn = a.fmt == FP8PA_E4M3 ? mla_split_kernel<FP8PA_E4M3> : mla_split_kernel<FP8PA_E5M2>;
-  cudaError_t e =
-      cudaFuncSetAttribute(reinterpret_cast<const void*>(kfn),
-                           cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kfn), smem);
   if (e != cudaSuccess) return e;
   char* ws = static_cast<char*>(a.workspace);
   int* plan = reinterpret_cast<int*>(ws);

@@ -85,6 +85,12 @@ cudaError_t launch_merge(const int* plan, const float* part_ml, const float* par
 cudaError_t launch_decode_gqa(const DecodeShape& s, const DecodeArgs& a, cudaStream_t stream);
 cudaError_t launch_decode_mla(const DecodeShape& s, const DecodeArgs& a, cudaStream_t stream);
 
+// Cached launch set-up (per device): SM count, the dynamic shared-memory
+// opt-in of a kernel (made once), and a kernel's resident CTAs per SM.
+int sm_count(int device);
+cudaError_t ensure_smem_attr(const void* fn, int smem);
+int ctas_per_sm(const void* fn, int threads, int smem);
+
 // Tensor-map encoder from the driver (resolved once through the runtime).
 bool encode_tensor_map_2d_u8(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows,
                              uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle swz);
