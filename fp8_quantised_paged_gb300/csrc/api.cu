@@ -175,7 +175,7 @@ DecodePath decode_path(int batch, int hq, int hkv, int d, int dv, int bs, int ma
     return r;
   }
   if ((d != 64 && d != 128) || dv != d || (bs != 16 && bs != 32 && bs != 64) || hq / hkv > 8 ||
-      mode == FP8PA_SCALE_TOKEN_GROUP || (hkv > 8 && hkv % 8 != 0))
+      mode == FP8PA_SCALE_TOKEN_GROUP)
     r.status = FP8PA_ERR_UNSUPPORTED;
   return r;
 }

@@ -575,8 +575,24 @@ SplitKernel pick(int d, int bs, int fmt, int mode) {
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
-// Warps per CTA (one per KV head of the CTA's head set) and head sets.
-int gqa_wpc(int hkv) { return hkv <= kMaxWarps ? hkv : kMaxWarps; }
+// Warps per CTA, one per KV head of the CTA's head set: the divisor of
+// Hkv (at most 8) that keeps the most warps resident per SM -- large pages
+// make a warp's ring big enough that 8 warps would not fit in one CTA's
+// shared memory, or would leave one CTA per SM.  Ties go to the larger
+// head set (its warps share each page's block-table entry and DRAM rows).
+constexpr int kMaxCtaSmem = 227 * 1024;
+int gqa_wpc(int hkv, const SplitKernel& k) {
+  int best = 1, best_warps = 0;
+  for (int w = 1; w <= kMaxWarps; ++w) {
+    if (hkv % w != 0 || k.smem(w) > kMaxCtaSmem) continue;
+    const int warps = w * ctas_per_sm(reinterpret_cast<const void*>(k.fn), w * 32, k.smem(w));
+    if (warps >= best_warps) {
+      best = w;
+      best_warps = warps;
+    }
+  }
+  return best;
+}
 
 }  // namespace
 
@@ -594,8 +610,8 @@ int decode_workers(const DecodeShape& s, int fmt, int mode, int device) {
     return (ranges < 1 ? 1 : ranges) * H;
   }
   if (g_decode_workers_override > 0) return g_decode_workers_override;
-  const int wpc = gqa_wpc(s.hkv), hsets = s.hkv / wpc;
   const SplitKernel k = pick(s.d, s.bs, fmt, mode);
+  const int wpc = gqa_wpc(s.hkv, k), hsets = s.hkv / wpc;
   const int per_sm = ctas_per_sm(reinterpret_cast<const void*>(k.fn), wpc * 32, k.smem(wpc));
   const int ranges = sms * per_sm / hsets;
   return ranges < 1 ? 1 : ranges;
@@ -617,8 +633,8 @@ size_t decode_workspace_bytes(const DecodeShape& s) {
 
 cudaError_t launch_decode_gqa(const DecodeShape& s, const DecodeArgs& a, cudaStream_t stream) {
   const int G = s.hq / s.hkv;
-  const int wpc = gqa_wpc(s.hkv), hsets = s.hkv / wpc;
   const SplitKernel k = pick(s.d, s.bs, a.fmt, a.mode);
+  const int wpc = gqa_wpc(s.hkv, k), hsets = s.hkv / wpc;
   const int smem = k.smem(wpc);
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(k.fn), smem);
   if (e != cudaSuccess) return e;

@@ -187,6 +187,27 @@ def make_workload(index: int, size: str = "full", seed: int | None = None) -> Wo
                     mla=(index == 5), params=params)
 
 
+def make_shape_case(name: str, batch_lens, hq: int, hkv: int, d: int, bs: int, fmt: int,
+                    scale_mode: int, seed: int, dv: int | None = None,
+                    group_size: int | None = None) -> Workload:
+    """A small seeded workload of any supported shape (parity matrix cases):
+    the given ragged lengths, a permuted pool with 2 spare blocks, values
+    N(0, 1) times a per-(K/V, kv head) spread U(0.5, 2) with 0.5% outliers x20.
+    d = 576 builds the shared-latent layout (one latent, 64-dim groups)."""
+    g = _rng(seed, 0)
+    lens = np.asarray(batch_lens, dtype=np.int32)
+    mla = d == 576
+    pool = int(sum(math.ceil(int(L) / bs) for L in lens)) + 2
+    bt = _tables(g, lens, bs, pool, "perm")
+    params = {"std": g.uniform(0.5, 2.0, size=(2, hkv)), "outlier_p": 0.005, "outlier_x": 20.0}
+    dk_eff = 192.0 if mla else float(d)
+    return Workload(index=0, name=name, batch=len(lens), n_q_heads=hq, n_kv_heads=hkv,
+                    head_dim=d, head_dim_v=(dv or (512 if mla else d)), block_size=bs, fmt=fmt,
+                    scale_mode=scale_mode, group_size=group_size or (64 if mla else d),
+                    sm_scale=1.0 / math.sqrt(dk_eff), seq_lens=lens, block_tables=bt,
+                    num_blocks=pool, seed=seed, mla=mla, params=params)
+
+
 def request_kv(w: Workload, b: int):
     """bf16 bits of request b's K and V rows, [L_b, Hkv, D] each (V is None
     for the MLA workload, whose single latent serves as K and V)."""
@@ -201,7 +222,7 @@ def request_kv(w: Workload, b: int):
             hot = w.params["hot_channels"][which]
             for h in range(hkv):
                 x[:, h, hot[h]] *= 20.0
-        elif w.index in (2, 3):
+        elif w.index in (0, 2, 3):
             x = rng.standard_normal(shape, dtype=np.float32)
             x *= w.params["std"][which].astype(np.float32)[None, :, None]
             n = x.size

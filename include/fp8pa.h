@@ -172,8 +172,7 @@ size_t fp8pa_decode_workspace_bytes(int batch, int n_q_heads, int n_kv_heads, in
  * pass; the result does not depend on the split beyond fp32 rounding.
  *
  * Two layouts are served:
- *  GQA  n_q_heads % n_kv_heads == 0, n_q_heads/n_kv_heads <= 8, n_kv_heads <= 8
- *       or a multiple of 8, head_dim in
+ *  GQA  n_q_heads % n_kv_heads == 0, n_q_heads/n_kv_heads <= 8, head_dim in
  *       {64, 128}, head_dim_v == head_dim, block_size in {16, 32, 64},
  *       scale_mode TOKEN_HEAD or CHANNEL_STATIC, separate v_cache/v_scale.
  *  MLA  n_kv_heads == 1, head_dim 576 (512 latent + 64 rope), head_dim_v
