@@ -35,7 +35,7 @@ from dataclasses import dataclass, field
 import numpy as np
 
 E4M3, E5M2 = 0, 1
-SCALE_TOKEN_HEAD, SCALE_CHANNEL_STATIC, SCALE_TOKEN_GROUP = 0, 1, 2
+SCALE_TOKEN_HEAD, SCALE_CHANNEL_STATIC, SCALE_TOKEN_GROUP, SCALE_MX_BLOCK = 0, 1, 2, 3
 
 
 def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:

@@ -23,7 +23,7 @@ _SRC = os.path.join(_HERE, "fp8pa_oracle.c")
 _LIB_PATH = os.path.join(_HERE, "liboracle.so")
 
 E4M3, E5M2 = 0, 1
-SCALE_TOKEN_HEAD, SCALE_CHANNEL_STATIC, SCALE_TOKEN_GROUP = 0, 1, 2
+SCALE_TOKEN_HEAD, SCALE_CHANNEL_STATIC, SCALE_TOKEN_GROUP, SCALE_MX_BLOCK = 0, 1, 2, 3
 
 _lib = None
 
@@ -58,6 +58,8 @@ def _load():
     lib.or_fp8_decode_array.argtypes = [P, L, i, P]
     lib.or_absmax_scale_bf16.argtypes = [P, i, i]
     lib.or_absmax_scale_bf16.restype = ctypes.c_float
+    lib.or_mx_exponent.argtypes = [ctypes.c_float, i]
+    lib.or_mx_exponent.restype = i
     lib.or_kv_append_quant.argtypes = [P, P, P, i, i, i, i, i, i, P, P, P, P, i, i]
     lib.or_kv_append_quant.restype = i
     lib.or_kv_channel_scales.argtypes = [P, i, i, i, i, P]
@@ -106,6 +108,11 @@ def fp8_encode_bruteforce(x, fmt: int) -> np.ndarray:
     return out.reshape(np.shape(x))
 
 
+def mx_exponent(amax: float, fmt: int) -> int:
+    """The MX block exponent e (scale 2^e) for a block absmax."""
+    return int(_load().or_mx_exponent(ctypes.c_float(amax), fmt))
+
+
 def absmax_scale(x_bf16, fmt: int) -> float:
     a = _c(np.asarray(x_bf16), np.uint16).reshape(-1)
     return float(_load().or_absmax_scale_bf16(_ptr(a), a.size, fmt))
@@ -118,11 +125,12 @@ def kv_append_quant(k, v, slot_mapping, fmt, scale_mode, group_size, k_cache, v_
     k = _c(k, np.uint16)
     v = _c(v, np.uint16)
     sm = _c(slot_mapping, np.int32)
-    for arr, dt in ((k_cache, np.uint8), (k_scale, np.float32)):
+    sdt = np.uint8 if scale_mode == SCALE_MX_BLOCK else np.float32  # E8M0 bytes
+    for arr, dt in ((k_cache, np.uint8), (k_scale, sdt)):
         assert arr.dtype == dt and arr.flags.c_contiguous
     if v is not None:
         assert v_cache.dtype == np.uint8 and v_cache.flags.c_contiguous
-        assert v_scale.dtype == np.float32 and v_scale.flags.c_contiguous
+        assert v_scale.dtype == sdt and v_scale.flags.c_contiguous
     n, hkv, d = k.shape
     num_blocks = k_cache.shape[0]
     return int(_load().or_kv_append_quant(_ptr(k), _ptr(v), _ptr(sm), n, hkv, d, fmt, scale_mode,

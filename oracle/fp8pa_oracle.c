@@ -33,6 +33,15 @@
  * overflow to +-max; the scale is fp32 absmax / FMAX with IEEE division,
  * clamped below at 1e-12, and codes are fp32 x / scale (a division, not a
  * multiply by the reciprocal); query head h reads KV head h / (Hq / Hkv).
+ *
+ * The block-scaled mode follows the Microscaling (MX) format that [P4]
+ * sec. 7.1 names for Blackwell's FP8 (the page gives only "per-16-element
+ * block scaling"): every block of 16 or 32 values along the head dimension
+ * shares one power-of-two scale X = 2^e, stored as its biased exponent
+ * byte e + 127 (E8M0), with e = floor(log2(block absmax)) - emax, emax the
+ * exponent of the format's largest normal (8 for E4M3, 15 for E5M2), held in
+ * [-127, 127] (an all-zero block takes e = -127); codes are the FP8 rounding
+ * of x / X, saturated.
  */
 #include <math.h>
 #include <stdint.h>
@@ -48,6 +57,7 @@
 #define OR_SCALE_TOKEN_HEAD 0
 #define OR_SCALE_CHANNEL_STATIC 1
 #define OR_SCALE_TOKEN_GROUP 2
+#define OR_SCALE_MX_BLOCK 3
 
 /* ------------------------------------------------------------------ */
 /* FP8 formats: [P2] sec. 1.1, [P4] sec. 1.1, [P1] sec. 2.1.           */
@@ -194,27 +204,52 @@ float or_absmax_scale_bf16(const uint16_t* x, int n, int fmt) {
   return s;
 }
 
+/* The block exponent e of the MX mode: floor(log2(amax)) - emax, in
+ * [-127, 127]; -127 for amax = 0.  frexp gives amax = m * 2^E, m in
+ * [0.5, 1), so floor(log2(amax)) = E - 1 exactly. */
+int or_mx_exponent(float amax, int fmt) {
+  if (!(amax > 0.0f)) return -127;
+  int E = 0;
+  (void)frexp((double)amax, &E);
+  int e = (E - 1) - (fmt == OR_E4M3 ? 8 : 15);
+  if (e < -127) e = -127;
+  if (e > 127) e = 127;
+  return e;
+}
+
 /* Quantise one row of `d` values and store codes (and scales) in the
  * paged layout:
  *   codes  [num_blocks][Hkv][bs][D]        u8
  *   TOKEN_HEAD  scale [num_blocks][Hkv][bs]           f32 (written)
  *   TOKEN_GROUP scale [num_blocks][Hkv][bs][D / gs]   f32 (written)
- *   CHANNEL_STATIC scale [Hkv][D]                     f32 (read)      */
+ *   CHANNEL_STATIC scale [Hkv][D]                     f32 (read)
+ *   MX_BLOCK scale [num_blocks][Hkv][bs][D / gs]      u8 E8M0 (written) */
 static void or_quant_row(const uint16_t* src, int d, int fmt, int mode, int gs,
                          const float* chan_scale, uint8_t* dst_codes,
-                         float* dst_scale) {
+                         void* dst_scale) {
   float* x = (float*)malloc(sizeof(float) * (size_t)d);
   for (int i = 0; i < d; ++i) x[i] = bf16_to_f32(src[i]);
   if (mode == OR_SCALE_TOKEN_HEAD) {
     const float s = or_absmax_scale(x, d, fmt);
     for (int i = 0; i < d; ++i) dst_codes[i] = or_fp8_encode(x[i] / s, fmt);
-    *dst_scale = s;
+    *(float*)dst_scale = s;
   } else if (mode == OR_SCALE_TOKEN_GROUP) {
     for (int g = 0; g < d / gs; ++g) {
       const float s = or_absmax_scale(x + g * gs, gs, fmt);
       for (int i = 0; i < gs; ++i)
         dst_codes[g * gs + i] = or_fp8_encode(x[g * gs + i] / s, fmt);
-      dst_scale[g] = s;
+      ((float*)dst_scale)[g] = s;
+    }
+  } else if (mode == OR_SCALE_MX_BLOCK) {
+    for (int g = 0; g < d / gs; ++g) {
+      float amax = 0.0f;
+      for (int i = 0; i < gs; ++i) amax = fmaxf(amax, fabsf(x[g * gs + i]));
+      const int e = or_mx_exponent(amax, fmt);
+      /* x / 2^e is exact in FP64; the float conversion rounds only below
+       * the fp32 normal range, where every such value encodes to zero. */
+      for (int i = 0; i < gs; ++i)
+        dst_codes[g * gs + i] = or_fp8_encode((float)ldexp((double)x[g * gs + i], -e), fmt);
+      ((uint8_t*)dst_scale)[g] = (uint8_t)(e + 127);
     }
   } else {
     for (int i = 0; i < d; ++i) dst_codes[i] = or_fp8_encode(x[i] / chan_scale[i], fmt);
@@ -230,7 +265,9 @@ int or_kv_append_quant(const uint16_t* k, const uint16_t* v, const int32_t* slot
                        int group_size, uint8_t* k_cache, uint8_t* v_cache, float* k_scale,
                        float* v_scale, int num_blocks, int block_size) {
   int bad = 0;
-  const int ngroups = (scale_mode == OR_SCALE_TOKEN_GROUP) ? head_dim / group_size : 1;
+  const int ngroups = (scale_mode == OR_SCALE_TOKEN_GROUP || scale_mode == OR_SCALE_MX_BLOCK)
+                          ? head_dim / group_size
+                          : 1;
   for (int t = 0; t < num_tokens; ++t) {
     const int slot = slot_mapping[t];
     if (slot < 0) continue;
@@ -247,10 +284,12 @@ int or_kv_append_quant(const uint16_t* k, const uint16_t* v, const int32_t* slot
         uint8_t* cache = which == 0 ? k_cache : v_cache;
         float* sc = which == 0 ? k_scale : v_scale;
         const uint16_t* x = src + ((long)t * n_kv_heads + h) * head_dim;
-        float* dst_scale = NULL;
+        void* dst_scale = NULL;
         const float* chan = NULL;
         if (scale_mode == OR_SCALE_CHANNEL_STATIC)
           chan = sc + (long)h * head_dim;
+        else if (scale_mode == OR_SCALE_MX_BLOCK)
+          dst_scale = (uint8_t*)sc + row * ngroups;  /* E8M0 bytes */
         else
           dst_scale = sc + row * ngroups;
         or_quant_row(x, head_dim, fmt, scale_mode, group_size, chan, cache + row * head_dim,
@@ -311,6 +350,8 @@ static double or_deq(const or_attn_t* a, const uint8_t* cache, const float* sc, 
     s = (double)sc[row];
   else if (a->mode == OR_SCALE_TOKEN_GROUP)
     s = (double)sc[row * (a->dk / a->gs) + d / a->gs];
+  else if (a->mode == OR_SCALE_MX_BLOCK)
+    s = ldexp(1.0, (int)((const uint8_t*)sc)[row * (a->dk / a->gs) + d / a->gs] - 127);
   else
     s = (double)sc[(long)g * a->dk + d];
   return code * s;

@@ -141,3 +141,57 @@ def test_channel_calibration():
     assert s[i] == np.abs(xf[:, i[0], i[1]]).max() / np.float32(57344.0)
     z = oracle.kv_channel_scales(np.zeros((4, 1, 16), np.uint16), oracle.E4M3)
     assert (z == np.float32(1e-12)).all()
+
+
+# ---------------------------------------------------------------- MX block mode
+def _mx_append(x_rows, fmt, gs):
+    """Append rows [n, d] (bf16 bits) for one KV head with MX block scales."""
+    n, d = x_rows.shape
+    kc = np.zeros((n, 1, 1, d), np.uint8)
+    ks = np.zeros((n, 1, 1, d // gs), np.uint8)
+    assert oracle.kv_append_quant(x_rows.reshape(n, 1, d), None, np.arange(n, dtype=np.int32),
+                                  fmt, oracle.SCALE_MX_BLOCK, gs, kc, None, ks, None, 1) == 0
+    return kc.reshape(n, d), ks.reshape(n, d // gs)
+
+
+def test_mx_block_hand_worked():
+    """E4M3, blocks of 32: absmax 448 -> e = 0, codes are the plain cast;
+    absmax 500 -> e = 0 too and 500 saturates to 448 (0x7E); absmax 1 ->
+    e = -8, so 1.0 -> 256 (0x78) and 0.5 -> 128 (0x70); an all-zero block
+    takes e = -127 (byte 0) and zero codes."""
+    x = np.zeros((1, 128), np.float32)
+    x[0, 0], x[0, 1] = 448.0, -2.0           # block 0
+    x[0, 32], x[0, 33] = 500.0, -1.0         # block 1
+    x[0, 64], x[0, 65] = 1.0, 0.5            # block 2
+    kc, ks = _mx_append(_bf16(x), oracle.E4M3, 32)
+    assert list(ks[0]) == [127, 127, 119, 0]
+    assert kc[0, 0] == 0x7E and kc[0, 1] == 0xC0      # 448, -2.0
+    assert kc[0, 32] == 0x7E and kc[0, 33] == 0xB8    # 500 -> 448, -1.0
+    assert kc[0, 64] == 0x78 and kc[0, 65] == 0x70    # 256, 128
+    assert not kc[0, 96:].any()
+
+
+def test_mx_block_matches_numpy_torch_restatement():
+    """Every block of seeded heavy-tailed rows against an independent
+    restatement: e from numpy's frexp, codes from torch's float8 cast of
+    x * 2^-e (clamped to the finite range first: torch's e4m3fn cast does not
+    saturate)."""
+    import torch
+    rng = np.random.default_rng(7)
+    for fmt, tdt, fmax, emax in ((oracle.E4M3, torch.float8_e4m3fn, 448.0, 8),
+                                 (oracle.E5M2, torch.float8_e5m2, 57344.0, 15)):
+        for gs in (16, 32):
+            x = rng.standard_t(2.0, size=(64, 128)).astype(np.float32)
+            x *= np.exp2(rng.integers(-20, 20, size=(64, 1))).astype(np.float32)
+            x[3, :gs] = 0.0                                  # an all-zero block
+            xb = f32_to_bf16_bits(x)
+            kc, ks = _mx_append(xb, fmt, gs)
+            xf = (xb.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+            blocks = xf.reshape(64, 128 // gs, gs)
+            amax = np.abs(blocks).max(axis=2)
+            _, E = np.frexp(amax)
+            e = np.where(amax > 0, E - 1 - emax, -127).clip(-127, 127)
+            assert np.array_equal(ks.astype(np.int64) - 127, e)
+            scaled = np.clip(blocks * np.exp2(-e)[..., None], -fmax, fmax)
+            want = torch.from_numpy(scaled.astype(np.float32)).to(tdt).view(torch.uint8).numpy()
+            assert np.array_equal(kc.reshape(64, 128 // gs, gs), want), (fmt, gs)

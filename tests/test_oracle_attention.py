@@ -19,7 +19,7 @@ def build_cache(w):
     """Fill a cache for every token of every request through the oracle's
     append (static channel scales calibrated by the oracle when needed)."""
     nb, hkv, bs, d = w.num_blocks, w.n_kv_heads, w.block_size, w.head_dim
-    ng = d // w.group_size if w.scale_mode == W.SCALE_TOKEN_GROUP else 1
+    ng = d // w.group_size if w.scale_mode in (W.SCALE_TOKEN_GROUP, W.SCALE_MX_BLOCK) else 1
     kc = np.zeros((nb, hkv, bs, d), np.uint8)
     vc = None if w.mla else np.zeros_like(kc)
     kvs = [W.request_kv(w, b) for b in range(w.batch)]
@@ -27,7 +27,8 @@ def build_cache(w):
         ks = oracle.kv_channel_scales(np.concatenate([k for k, _ in kvs]), w.fmt)
         vs = oracle.kv_channel_scales(np.concatenate([v for _, v in kvs]), w.fmt)
     else:
-        ks = np.zeros((nb, hkv, bs, ng), np.float32)
+        sdt = np.uint8 if w.scale_mode == W.SCALE_MX_BLOCK else np.float32
+        ks = np.zeros((nb, hkv, bs, ng), sdt)
         vs = None if w.mla else np.zeros_like(ks)
     for b, (k, v) in enumerate(kvs):
         slots = W.token_slots(w, b, 0, int(w.seq_lens[b]))
@@ -50,6 +51,9 @@ def dequant_request(w, cache, scale, b):
         s = torch.from_numpy(scale[blk, :, off, 0].astype(np.float64))[..., None]
     elif w.scale_mode == W.SCALE_TOKEN_GROUP:
         s = torch.from_numpy(scale[blk, :, off, :].astype(np.float64))
+        s = s.repeat_interleave(w.group_size, dim=-1)
+    elif w.scale_mode == W.SCALE_MX_BLOCK:   # E8M0 bytes: 2^(byte - 127)
+        s = torch.from_numpy(np.exp2(scale[blk, :, off, :].astype(np.float64) - 127.0))
         s = s.repeat_interleave(w.group_size, dim=-1)
     else:
         s = torch.from_numpy(scale.astype(np.float64))[None]
@@ -231,3 +235,17 @@ def test_multiquery_rows_are_a_causal_chunk(idx, q_len):
         ref = o.permute(1, 0, 2).numpy()
         assert np.allclose(got[b], ref, rtol=1e-10, atol=1e-10), np.abs(got[b] - ref).max()
     assert checked >= w.batch - 1
+
+
+@pytest.mark.parametrize("fmt,gs", [(W.E4M3, 32), (W.E5M2, 16)])
+def test_mx_block_attention_matches_torch_sdpa(fmt, gs):
+    """Block-scaled (MX) cache: attention over the dequantised cache,
+    decode(code) * 2^(byte - 127), against float64 SDPA."""
+    w = W.make_shape_case("mx", [1, 15, 16, 17, 53], 16, 4, 128, 16, fmt, W.SCALE_MX_BLOCK,
+                          seed=31, group_size=gs)
+    kc, vc, ks, vs = build_cache(w)
+    assert ks.dtype == np.uint8 and ks.shape[-1] == 128 // gs
+    q = W.queries(w)
+    got = run_oracle(w, q, kc, vc, ks, vs)
+    ref = sdpa_reference(w, q, kc, vc, ks, vs)
+    assert np.allclose(got, ref, rtol=1e-10, atol=1e-10), np.abs(got - ref).max()
