@@ -18,6 +18,7 @@ _API = ("kv_append_quant", "kv_channel_scales", "kv_channel_absmax_update",
         "decode_step",
         "decode_workspace_bytes", "get_device_error", "set_decode_workers", "version",
         "E4M3", "E5M2", "SCALE_TOKEN_HEAD", "SCALE_CHANNEL_STATIC", "SCALE_TOKEN_GROUP",
+        "SCALE_MX_BLOCK",
         "OUT_BF16", "OUT_F32", "Fp8paError")
 
 __all__ = list(_API)

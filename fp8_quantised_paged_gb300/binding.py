@@ -19,14 +19,14 @@ import ctypes
 import torch
 
 from . import _native as N
-from ._native import (E4M3, E5M2, OUT_BF16, OUT_F32, SCALE_CHANNEL_STATIC, SCALE_TOKEN_GROUP,
-                      SCALE_TOKEN_HEAD, Fp8paError)
+from ._native import (E4M3, E5M2, OUT_BF16, OUT_F32, SCALE_CHANNEL_STATIC, SCALE_MX_BLOCK,
+                      SCALE_TOKEN_GROUP, SCALE_TOKEN_HEAD, Fp8paError)
 
 __all__ = ["kv_append_quant", "kv_channel_scales", "kv_channel_absmax_update",
-           "kv_scales_from_absmax", "paged_decode_attention", "paged_multiquery_attention", "decode_step",
-           "decode_workspace_bytes", "get_device_error", "set_decode_workers", "version",
-           "E4M3", "E5M2", "SCALE_TOKEN_HEAD", "SCALE_CHANNEL_STATIC", "SCALE_TOKEN_GROUP",
-           "OUT_BF16", "OUT_F32", "Fp8paError"]
+           "kv_scales_from_absmax", "paged_decode_attention", "paged_multiquery_attention",
+           "decode_step", "decode_workspace_bytes", "get_device_error", "set_decode_workers",
+           "version", "E4M3", "E5M2", "SCALE_TOKEN_HEAD", "SCALE_CHANNEL_STATIC",
+           "SCALE_TOKEN_GROUP", "SCALE_MX_BLOCK", "OUT_BF16", "OUT_F32", "Fp8paError"]
 
 
 def _ptr(t):
@@ -47,6 +47,11 @@ _NOP = _Nop()
 def _on(dev):
     """Make `dev` current for a call (a no-op when it already is)."""
     return _NOP if dev.index == torch.cuda.current_device() else torch.cuda.device(dev)
+
+
+def _scale_dtype(scale_mode):
+    """fp32 scales, or E8M0 exponent bytes for the MX block mode."""
+    return torch.uint8 if scale_mode == SCALE_MX_BLOCK else torch.float32
 
 
 def _need(t, dtype, name, device=None):
@@ -79,15 +84,16 @@ def kv_append_quant(k, v, slot_mapping, k_cache, v_cache, k_scale, v_scale, fmt=
                     scale_mode=SCALE_TOKEN_HEAD, group_size=64, stream=None):
     """k, v: bf16 [num_tokens, Hkv, D] (v may be None for the MLA latent);
     slot_mapping: int32 [num_tokens]; caches: uint8 [num_blocks, Hkv, bs, D];
-    scales: float32 per the scale mode (see include/fp8pa.h)."""
+    scales: float32 per the scale mode, uint8 E8M0 exponents for SCALE_MX_BLOCK
+    (see include/fp8pa.h)."""
     _need(k, torch.bfloat16, "k")
     dev = k.device
     _need(v, torch.bfloat16, "v", dev)
     _need(slot_mapping, torch.int32, "slot_mapping", dev)
     _need(k_cache, torch.uint8, "k_cache", dev)
     _need(v_cache, torch.uint8, "v_cache", dev)
-    _need(k_scale, torch.float32, "k_scale", dev)
-    _need(v_scale, torch.float32, "v_scale", dev)
+    _need(k_scale, _scale_dtype(scale_mode), "k_scale", dev)
+    _need(v_scale, _scale_dtype(scale_mode), "v_scale", dev)
     n, hkv, d = k.shape
     nb, _, bs, _ = k_cache.shape
     with _on(dev):
@@ -159,7 +165,8 @@ def paged_decode_attention(q, k_cache, v_cache, k_scale, v_scale, block_tables, 
     _need(q, torch.bfloat16, "q")
     dev = q.device
     for t, dt, name in ((k_cache, torch.uint8, "k_cache"), (v_cache, torch.uint8, "v_cache"),
-                        (k_scale, torch.float32, "k_scale"), (v_scale, torch.float32, "v_scale"),
+                        (k_scale, _scale_dtype(scale_mode), "k_scale"),
+                        (v_scale, _scale_dtype(scale_mode), "v_scale"),
                         (block_tables, torch.int32, "block_tables"),
                         (seq_lens, torch.int32, "seq_lens")):
         _need(t, dt, name, dev)
@@ -202,7 +209,8 @@ def paged_multiquery_attention(q, k_cache, v_cache, k_scale, v_scale, block_tabl
     _need(q, torch.bfloat16, "q")
     dev = q.device
     for t, dt, name in ((k_cache, torch.uint8, "k_cache"), (v_cache, torch.uint8, "v_cache"),
-                        (k_scale, torch.float32, "k_scale"), (v_scale, torch.float32, "v_scale"),
+                        (k_scale, _scale_dtype(scale_mode), "k_scale"),
+                        (v_scale, _scale_dtype(scale_mode), "v_scale"),
                         (block_tables, torch.int32, "block_tables"),
                         (seq_lens, torch.int32, "seq_lens")):
         _need(t, dt, name, dev)
@@ -245,7 +253,8 @@ def decode_step(k_new, v_new, slot_mapping, q, k_cache, v_cache, k_scale, v_scal
     _need(k_new, torch.bfloat16, "k_new", dev)
     _need(v_new, torch.bfloat16, "v_new", dev)
     for t, dt, name in ((k_cache, torch.uint8, "k_cache"), (v_cache, torch.uint8, "v_cache"),
-                        (k_scale, torch.float32, "k_scale"), (v_scale, torch.float32, "v_scale"),
+                        (k_scale, _scale_dtype(scale_mode), "k_scale"),
+                        (v_scale, _scale_dtype(scale_mode), "v_scale"),
                         (block_tables, torch.int32, "block_tables"),
                         (seq_lens, torch.int32, "seq_lens"),
                         (slot_mapping, torch.int32, "slot_mapping")):

@@ -151,7 +151,7 @@ DecodePath decode_path(int batch, int hq, int hkv, int d, int dv, int bs, int ma
   s.qlen = 1;
   if ((fmt != FP8PA_E4M3 && fmt != FP8PA_E5M2) ||
       (mode != FP8PA_SCALE_TOKEN_HEAD && mode != FP8PA_SCALE_CHANNEL_STATIC &&
-       mode != FP8PA_SCALE_TOKEN_GROUP) ||
+       mode != FP8PA_SCALE_TOKEN_GROUP && mode != FP8PA_SCALE_MX_BLOCK) ||
       (out_dtype != FP8PA_OUT_BF16 && out_dtype != FP8PA_OUT_F32)) {
     r.status = FP8PA_ERR_BAD_ENUM;
     return r;
@@ -175,7 +175,8 @@ DecodePath decode_path(int batch, int hq, int hkv, int d, int dv, int bs, int ma
     return r;
   }
   if ((d != 64 && d != 128) || dv != d || (bs != 16 && bs != 32 && bs != 64) || hq / hkv > 8 ||
-      mode == FP8PA_SCALE_TOKEN_GROUP)
+      mode == FP8PA_SCALE_TOKEN_GROUP ||
+      (mode == FP8PA_SCALE_MX_BLOCK && gs != 16 && gs != 32))
     r.status = FP8PA_ERR_UNSUPPORTED;
   return r;
 }
@@ -267,11 +268,14 @@ int append_prepare(const void* k, const void* v, const int32_t* slot_mapping, in
     return FP8PA_ERR_BAD_SHAPE;
   if ((fmt != FP8PA_E4M3 && fmt != FP8PA_E5M2) ||
       (scale_mode != FP8PA_SCALE_TOKEN_HEAD && scale_mode != FP8PA_SCALE_CHANNEL_STATIC &&
-       scale_mode != FP8PA_SCALE_TOKEN_GROUP))
+       scale_mode != FP8PA_SCALE_TOKEN_GROUP && scale_mode != FP8PA_SCALE_MX_BLOCK))
     return FP8PA_ERR_BAD_ENUM;
   if (head_dim % 16 != 0 || head_dim > 768) return FP8PA_ERR_UNSUPPORTED;
   if (scale_mode == FP8PA_SCALE_TOKEN_GROUP &&
       (!pow2(group_size) || group_size < 16 || group_size > 256 || head_dim % group_size != 0))
+    return FP8PA_ERR_UNSUPPORTED;
+  if (scale_mode == FP8PA_SCALE_MX_BLOCK &&
+      ((group_size != 16 && group_size != 32) || head_dim % group_size != 0))
     return FP8PA_ERR_UNSUPPORTED;
   if (static_cast<long long>(num_blocks) * block_size >= (1ll << 31)) return FP8PA_ERR_UNSUPPORTED;
   *a = AppendArgs{};
@@ -292,7 +296,9 @@ int append_prepare(const void* k, const void* v, const int32_t* slot_mapping, in
   a->hkv = n_kv_heads;
   a->d = head_dim;
   a->ntens = v ? 2 : 1;
-  a->gs = scale_mode == FP8PA_SCALE_TOKEN_GROUP ? group_size : head_dim;
+  a->gs = (scale_mode == FP8PA_SCALE_TOKEN_GROUP || scale_mode == FP8PA_SCALE_MX_BLOCK)
+              ? group_size
+              : head_dim;
   a->num_blocks = num_blocks;
   a->bs = block_size;
   return FP8PA_OK;

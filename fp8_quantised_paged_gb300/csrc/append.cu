@@ -73,6 +73,7 @@ __device__ __forceinline__ void append_row(const AppendArgs& a, long row, int la
   }
 
   constexpr float kFmax = fp8_max<FMT>();
+  constexpr int kEmax = FMT == FP8PA_E4M3 ? 8 : 15;  // exponent of the largest normal
   float s[R];
   if constexpr (MODE == FP8PA_SCALE_TOKEN_HEAD) {
     float m = 0.0f;
@@ -96,6 +97,24 @@ __device__ __forceinline__ void append_row(const AppendArgs& a, long row, int la
       if (ci < nch && (lane & (lpg - 1)) == 0)
         a.scale[which][crow * ngroups + (ci * 8) / a.gs] = s[r];
     }
+  } else if constexpr (MODE == FP8PA_SCALE_MX_BLOCK) {
+    // s = 2^e with e = floor(log2(block absmax)) - emax, read off the fp32
+    // exponent field (a zero or subnormal absmax gives the floor, -127); the
+    // codes below multiply by 2^-e, which is exact.
+    const int lpg = a.gs / 8;
+    const int ngroups = a.d / a.gs;
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      float m = cmax[r];
+      for (int o = 1; o < lpg; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+      const int ef = (__float_as_int(m) >> 23) & 0xFF;
+      const int e = ef == 0 ? -127 : min(127, max(-127, ef - 127 - kEmax));
+      s[r] = exp2i(-e);  // the multiplier 2^-e (e <= 119 for bf16 inputs)
+      const int ci = lane + 32 * r;
+      if (ci < nch && (lane & (lpg - 1)) == 0)
+        reinterpret_cast<uint8_t*>(a.scale[which])[crow * ngroups + (ci * 8) / a.gs] =
+            static_cast<uint8_t>(e + 127);
+    }
   }
 
 #pragma unroll
@@ -109,6 +128,9 @@ __device__ __forceinline__ void append_row(const AppendArgs& a, long row, int la
       const float sc[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
 #pragma unroll
       for (int e = 0; e < 8; ++e) q[e] = __fdiv_rn(v[r][e], sc[e]);
+    } else if constexpr (MODE == FP8PA_SCALE_MX_BLOCK) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) q[e] = v[r][e] * s[r];
     } else {
 #pragma unroll
       for (int e = 0; e < 8; ++e) q[e] = __fdiv_rn(v[r][e], s[r]);
@@ -180,6 +202,8 @@ cudaError_t launch_append_m(const AppendArgs& a, int mode, const PlanArgs* pl,
       return launch_append_r<FMT, FP8PA_SCALE_TOKEN_HEAD>(a, pl, stream);
     case FP8PA_SCALE_CHANNEL_STATIC:
       return launch_append_r<FMT, FP8PA_SCALE_CHANNEL_STATIC>(a, pl, stream);
+    case FP8PA_SCALE_MX_BLOCK:
+      return launch_append_r<FMT, FP8PA_SCALE_MX_BLOCK>(a, pl, stream);
     default:
       return launch_append_r<FMT, FP8PA_SCALE_TOKEN_GROUP>(a, pl, stream);
   }

@@ -66,15 +66,59 @@ struct GqaParams {
   uint32_t* err;
   int B, hq, hkv, G, max_blocks, num_blocks;
   int qlen;  // queries per request: B counts (request, query) pairs
+  int gs;    // dims per block exponent (MX block mode)
   float qk_scale_log2;
 };
 
-// Shared-memory layout for `w` warps (each with its own NST-stage ring).
-template <int D, int BS, int NST>
+// MX block mode helpers.  2^k for an integer k <= 0 as an f16 bit pattern in
+// both halves (f16 subnormals down to 2^-24, then 0).
+__device__ __forceinline__ uint32_t h2_pow2(int k) {
+  const uint32_t h =
+      k >= -14 ? static_cast<uint32_t>(k + 15) << 10 : (k >= -24 ? 1u << (k + 24) : 0u);
+  return h | (h << 16);
+}
+__device__ __forceinline__ uint32_t hmul2_bits(uint32_t a, uint32_t b) {
+  const __half2 r = __hmul2(*reinterpret_cast<const __half2*>(&a),
+                            *reinterpret_cast<const __half2*>(&b));
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
+// The E8M0 exponent bytes of one token (nb = 2, 4 or 8 of them).
+struct ExpRow {
+  uint32_t w0, w1;
+  __device__ __forceinline__ int byte(int k) const {
+    return static_cast<int>(((k < 4 ? w0 : w1) >> (8 * (k & 3))) & 0xFFu);
+  }
+  __device__ __forceinline__ int max_byte() const {
+    uint32_t m = __vmaxu4(w0, w1);
+    m = __vmaxu4(m, m >> 16);
+    m = __vmaxu4(m, m >> 8);
+    return static_cast<int>(m & 0xFFu);
+  }
+};
+__device__ __forceinline__ ExpRow exp_row(const uint8_t* base, int t, int nb) {
+  ExpRow r;
+  if (nb == 8) {
+    const uint2 x = *reinterpret_cast<const uint2*>(base + t * 8);
+    r.w0 = x.x;
+    r.w1 = x.y;
+  } else if (nb == 4) {
+    r.w0 = *reinterpret_cast<const uint32_t*>(base + t * 4);
+    r.w1 = 0u;
+  } else {
+    r.w0 = *reinterpret_cast<const uint16_t*>(base + t * 2);
+    r.w1 = 0u;
+  }
+  return r;
+}
+
+// Shared-memory layout for `w` warps (each with its own NST-stage ring);
+// SCB = scale bytes per token per tensor in the ring (4 for one fp32 scale,
+// D/16 for the largest count of E8M0 block exponents, 0 for static scales).
+template <int D, int BS, int NST, int SCB>
 struct GqaSmem {
   static constexpr int kPage = BS * D;
   __host__ __device__ static constexpr int pages(int w) { return w * NST * 2 * kPage; }
-  __host__ __device__ static constexpr int scales(int w) { return w * NST * 2 * BS * 4; }
+  __host__ __device__ static constexpr int scales(int w) { return w * NST * 2 * BS * SCB; }
   __host__ __device__ static constexpr int ps(int w) { return w * 512; }
   __host__ __device__ static constexpr int bars(int w) { return w * NST * 8; }
   __host__ __device__ static constexpr int oks(int w) { return w * NST * 4; }
@@ -103,15 +147,19 @@ template <int D, int BS, int FMT, int MODE, int NST>
 __global__ void __launch_bounds__(kMaxWarps * 32)
     gqa_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                      const GqaParams p) {
-  using SM = GqaSmem<D, BS, NST>;
+  constexpr bool TOKSC = (MODE == FP8PA_SCALE_TOKEN_HEAD);
+  constexpr bool MX = (MODE == FP8PA_SCALE_MX_BLOCK);
+  constexpr bool DYN = TOKSC || MX;  // per-token scales: q stays exact in f16
+  using SM = GqaSmem<D, BS, NST, TOKSC ? 4 : (MX ? D / 16 : 0)>;
   constexpr int PAGE = SM::kPage;
+  constexpr int SCB = TOKSC ? 4 : (MX ? D / 16 : 0);
   constexpr int TILES = BS / 16;
   constexpr int KW = D / 16;   // K words per row per thread = k-steps
   constexpr int KCH = D / 64;  // 16-byte K chunks per row per thread
   constexpr int VW = D / 32;   // V words per token per thread
   constexpr int MT = D / 16;   // dv tiles of 16
-  constexpr bool TOKSC = (MODE == FP8PA_SCALE_TOKEN_HEAD);
-  constexpr uint32_t TX = 2 * PAGE + (TOKSC ? 2 * BS * 4 : 0);
+  const int nbx = MX ? D / p.gs : 0;  // exponent bytes per token (MX)
+  const uint32_t TX = 2 * PAGE + (TOKSC ? 2 * BS * 4 : (MX ? 2 * BS * nbx : 0));
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -120,7 +168,8 @@ __global__ void __launch_bounds__(kMaxWarps * 32)
   const int g = lane >> 2, c = lane & 3;
   const int W = blockDim.x >> 5;  // warps in this CTA
   uint8_t* pages = smem + warp * (NST * 2 * PAGE);
-  float* scl = reinterpret_cast<float*>(smem + SM::pages(W)) + warp * (NST * 2 * BS);
+  uint8_t* sclb = smem + SM::pages(W) + warp * (NST * 2 * BS * SCB);
+  float* scl = reinterpret_cast<float*>(sclb);
   // P^T for the PV MMA as two f16 planes (hi + lo carry ~22 significant bits)
   uint16_t* ps = reinterpret_cast<uint16_t*>(smem + SM::pages(W) + SM::scales(W)) + warp * 256;
   uint64_t* bars =
@@ -190,6 +239,13 @@ __global__ void __launch_bounds__(kMaxWarps * 32)
         if constexpr (TOKSC) {
           bulk_load(scl + s * 2 * BS, p.k_scale + row, BS * 4, &bars[s]);
           bulk_load(scl + s * 2 * BS + BS, p.v_scale + row, BS * 4, &bars[s]);
+        } else if constexpr (MX) {
+          const uint8_t* ke = reinterpret_cast<const uint8_t*>(p.k_scale);
+          const uint8_t* ve = reinterpret_cast<const uint8_t*>(p.v_scale);
+          bulk_load(sclb + s * 2 * BS * SCB, ke + static_cast<long>(row) * nbx, BS * nbx,
+                    &bars[s]);
+          bulk_load(sclb + s * 2 * BS * SCB + BS * SCB, ve + static_cast<long>(row) * nbx,
+                    BS * nbx, &bars[s]);
         }
       } else {
         raise_error(p.err, FP8PA_DEVERR_BLOCK_RANGE);
@@ -227,7 +283,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32)
   // ---- per-segment state.  Q enters the MMA as f16; with static channel
   // scales folded in it is no longer exact in f16, so it is split into a
   // high and a low f16 part and the contraction runs twice.
-  constexpr int QP = TOKSC ? 1 : 2;
+  constexpr int QP = DYN ? 1 : 2;
   uint32_t qb[QP][KW][2];
   float O[MT][4];
   float m0 = -FLT_MAX, m1 = -FLT_MAX, l0 = 0.f, l1 = 0.f, zs = 0.f;
@@ -258,7 +314,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32)
             qv[8 * x + 2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
           }
         }
-        if constexpr (!TOKSC) {
+        if constexpr (!DYN) {  // static channel scales fold into q
           const float* ksc = p.k_scale + kvh * D + c * (D / 4);
 #pragma unroll
           for (int e = 0; e < D / 4; ++e) qv[e] *= __ldg(ksc + e);
@@ -292,7 +348,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32)
       zs = p.qk_scale_log2 * exp2i(eq - 14);
       m0 = m1 = NEG_INF;
       l0 = l1 = 0.f;
-      erun = TOKSC ? -127 : 1;
+      erun = DYN ? -127 : 1;
 #pragma unroll
       for (int t = 0; t < MT; ++t) O[t][0] = O[t][1] = O[t][2] = O[t][3] = 0.f;
     }
@@ -308,6 +364,8 @@ __global__ void __launch_bounds__(kMaxWarps * 32)
     const uint32_t vbase = kbase + PAGE;
     const float* sks = scl + s * 2 * BS;
     const float* svs = sks + BS;
+    const uint8_t* kex = sclb + s * 2 * BS * SCB;  // MX: exponent bytes of K, V
+    const uint8_t* vex = kex + BS * SCB;
 
 #pragma unroll
     for (int tt = 0; tt < TILES; ++tt) {
@@ -330,11 +388,27 @@ __global__ void __launch_bounds__(kMaxWarps * 32)
       }
       const bool v0 = full || g < tv, v1 = full || g + 8 < tv;
       float sk0 = 1.f, sk1 = 1.f, sv0 = 1.f, sv1 = 1.f;
+      // MX: each K row's f16 codes are multiplied by 2^(e_block - e_max of
+      // the token) (exact), and 2^e_max becomes the row's scale; this lane's
+      // K words cover block kb0 (words with 4j < gs) and kb1.
+      uint32_t fk0a = 0u, fk0b = 0u, fk1a = 0u, fk1b = 0u;
       if constexpr (TOKSC) {
         sk0 = sks[r0 + g];
         sk1 = sks[r0 + g + 8];
         sv0 = v0 ? svs[r0 + g] : 0.f;
         sv1 = v1 ? svs[r0 + g + 8] : 0.f;
+      } else if constexpr (MX) {
+        const int kb0 = (c * (D / 4)) / p.gs, kb1 = (c * (D / 4) + D / 4 - 1) / p.gs;
+        const ExpRow e0 = exp_row(kex, r0 + g, nbx), e1 = exp_row(kex, r0 + g + 8, nbx);
+        const int m0e = e0.max_byte(), m1e = e1.max_byte();
+        fk0a = h2_pow2(e0.byte(kb0) - m0e);
+        fk0b = h2_pow2(e0.byte(kb1) - m0e);
+        fk1a = h2_pow2(e1.byte(kb0) - m1e);
+        fk1b = h2_pow2(e1.byte(kb1) - m1e);
+        sk0 = exp2i(m0e - 127);
+        sk1 = exp2i(m1e - 127);
+        sv0 = v0 ? exp2i(exp_row(vex, r0 + g, nbx).max_byte() - 127) : 0.f;
+        sv1 = v1 ? exp2i(exp_row(vex, r0 + g + 8, nbx).max_byte() - 127) : 0.f;
       }
       // two independent accumulator chains (even / odd k-steps)
       float acc[4] = {0.f, 0.f, 0.f, 0.f}, acc2[4] = {0.f, 0.f, 0.f, 0.f};
@@ -343,6 +417,14 @@ __global__ void __launch_bounds__(kMaxWarps * 32)
         uint32_t a0, a1, a2, a3;
         fp8x4_to_f16x2x2<FMT>(kw[0][j], a0, a2);
         fp8x4_to_f16x2x2<FMT>(kw[1][j], a1, a3);
+        if constexpr (MX) {
+          const bool hb = 4 * j >= p.gs;
+          const uint32_t f0 = hb ? fk0b : fk0a, f1 = hb ? fk1b : fk1a;
+          a0 = hmul2_bits(a0, f0);
+          a2 = hmul2_bits(a2, f0);
+          a1 = hmul2_bits(a1, f1);
+          a3 = hmul2_bits(a3, f1);
+        }
 #pragma unroll
         for (int qp = 0; qp < QP; ++qp)
           mma_16816((j & 1) ? acc2 : acc, a0, a1, a2, a3, qb[qp][j][0], qb[qp][j][1]);
@@ -373,7 +455,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32)
       m1 = mn1;
       // ---- fold the V scale into P, normalised by a running power of two
       float rs = 1.f, q00, q01, q10, q11;
-      if constexpr (TOKSC) {
+      if constexpr (DYN) {
         float svm = fmaxf(sv0, sv1);
 #pragma unroll
         for (int o = 4; o < 32; o <<= 1) svm = fmaxf(svm, __shfl_xor_sync(0xffffffffu, svm, o));
@@ -452,6 +534,20 @@ __global__ void __launch_bounds__(kMaxWarps * 32)
           for (int e = 0; e < VW; ++e) vw[u][e] = 0u;
         }
       }
+      // MX: the V codes of token tau_u, in this lane's block vb, times
+      // 2^(e_block - e_max of the token); 2^e_max went into P above.
+      uint32_t fv01 = 0u, fv23 = 0u;
+      if constexpr (MX) {
+        const int vb = ((D == 128 ? 16 : 8) * g) / p.gs;
+        uint32_t f[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const ExpRow e = exp_row(vex, r0 + 4 * c + ((u + c) & 3), nbx);
+          f[u] = h2_pow2(e.byte(vb) - e.max_byte());
+        }
+        fv01 = (f[0] & 0xFFFFu) | (f[1] & 0xFFFF0000u);
+        fv23 = (f[2] & 0xFFFFu) | (f[3] & 0xFFFF0000u);
+      }
 #pragma unroll
       for (int t = 0; t < MT; ++t) {
         const uint32_t sel = (t & 1) ? 0x7362u : 0x5140u;
@@ -460,6 +556,12 @@ __global__ void __launch_bounds__(kMaxWarps * 32)
         uint32_t a0, a1, a2, a3;
         fp8x4_to_f16x2x2<FMT>(x01, a0, a1);
         fp8x4_to_f16x2x2<FMT>(x23, a2, a3);
+        if constexpr (MX) {
+          a0 = hmul2_bits(a0, fv01);
+          a1 = hmul2_bits(a1, fv01);
+          a2 = hmul2_bits(a2, fv23);
+          a3 = hmul2_bits(a3, fv23);
+        }
         mma_16816(O[t], a0, a1, a2, a3, pb.x, pb.y);
         mma_16816(O[t], a0, a1, a2, a3, pl.x, pl.y);
       }
@@ -483,7 +585,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32)
       }
       // piece rows: (piece of request b) x KV head x query head of the group
       const long seg = (segbase[cc.b] + (wid - uprefix[cc.b] / upw)) * p.hkv + kvh;
-      const float fin = TOKSC ? exp2i(erun - 15) : (1.0f / 16384.f);
+      const float fin = DYN ? exp2i(erun - 15) : (1.0f / 16384.f);
 #pragma unroll
       for (int hsel = 0; hsel < 2; ++hsel) {
         const int hh = 2 * c + hsel;
@@ -495,7 +597,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32)
           vals[2 * t + 1] = O[t][2 + hsel] * fin;
         }
         const int dv0 = (D / 8) * g;
-        if constexpr (!TOKSC) {
+        if constexpr (!DYN) {
           const float* vsc = p.v_scale + kvh * D + dv0;
 #pragma unroll
           for (int e = 0; e < D / 8; ++e) vals[e] *= __ldg(vsc + e);
@@ -545,14 +647,19 @@ struct SplitKernel {
 template <int D, int BS, int FMT, int MODE>
 SplitKernel pick4() {
   constexpr int NST = stages_for<D, BS>();
-  using SM = GqaSmem<D, BS, NST>;
+  constexpr int SCB =
+      MODE == FP8PA_SCALE_TOKEN_HEAD ? 4 : (MODE == FP8PA_SCALE_MX_BLOCK ? D / 16 : 0);
+  using SM = GqaSmem<D, BS, NST, SCB>;
   return {gqa_split_kernel<D, BS, FMT, MODE, NST>, SM::bytes(1) - 1024};
 }
 
 template <int D, int BS, int FMT>
 SplitKernel pick3(int mode) {
-  return mode == FP8PA_SCALE_TOKEN_HEAD ? pick4<D, BS, FMT, FP8PA_SCALE_TOKEN_HEAD>()
-                                        : pick4<D, BS, FMT, FP8PA_SCALE_CHANNEL_STATIC>();
+  switch (mode) {
+    case FP8PA_SCALE_TOKEN_HEAD: return pick4<D, BS, FMT, FP8PA_SCALE_TOKEN_HEAD>();
+    case FP8PA_SCALE_MX_BLOCK: return pick4<D, BS, FMT, FP8PA_SCALE_MX_BLOCK>();
+    default: return pick4<D, BS, FMT, FP8PA_SCALE_CHANNEL_STATIC>();
+  }
 }
 
 template <int D, int BS>
@@ -686,6 +793,7 @@ cudaError_t launch_decode_gqa(const DecodeShape& s, const DecodeArgs& a, cudaStr
   p.max_blocks = s.max_blocks;
   p.num_blocks = a.num_blocks;
   p.qlen = s.qlen;
+  p.gs = a.gs;
   p.qk_scale_log2 = a.sm_scale * 1.4426950408889634f;
   cfg.gridDim = dim3(static_cast<unsigned>(s.workers) * hsets);
   cfg.blockDim = dim3(wpc * 32);

@@ -40,6 +40,9 @@
  *   TOKEN_HEAD scale f32 [num_blocks][n_kv_heads][block_size]
  *   TOKEN_GROUP scale f32 [num_blocks][n_kv_heads][block_size][head_dim/group_size]
  *   CHANNEL_STATIC scale f32 [n_kv_heads][head_dim]   (caller-given, read only)
+ *   MX_BLOCK scale   u8  [num_blocks][n_kv_heads][block_size][head_dim/group_size]
+ *                        (E8M0: byte b is the power of two 2^(b - 127); the
+ *                        float* scale arguments then carry this byte buffer)
  *   slot s           -> block s / block_size, offset s % block_size
  *   block_tables     i32 [batch][max_blocks_per_seq]; token t of request b
  *                        lives in block block_tables[b][t / block_size]
@@ -81,6 +84,7 @@ extern "C" {
 #define FP8PA_SCALE_TOKEN_HEAD 0     /* dynamic: one f32 per (token, kv head), written by append */
 #define FP8PA_SCALE_CHANNEL_STATIC 1 /* static: caller-given f32 per (kv head, dim), read only   */
 #define FP8PA_SCALE_TOKEN_GROUP 2    /* dynamic: one f32 per (token, kv head, group of dims)     */
+#define FP8PA_SCALE_MX_BLOCK 3       /* dynamic: one E8M0 byte per (token, kv head, 16/32 dims)  */
 
 /* Output element types of the decode. */
 #define FP8PA_OUT_BF16 0
@@ -101,11 +105,19 @@ extern "C" {
  * scale_mode    TOKEN_HEAD: s = max(absmax(row)/FMAX, 1e-12), written to
  *               k_scale/v_scale.  TOKEN_GROUP: the same per group of
  *               group_size dims.  CHANNEL_STATIC: s = k_scale[h][d] given
- *               by the caller, not written.
+ *               by the caller, not written.  MX_BLOCK: per block of
+ *               group_size (16 or 32) dims the power of two s = 2^e,
+ *               e = floor(log2(absmax)) - emax (emax 8 for E4M3, 15 for
+ *               E5M2) held in [-127, 127] (-127 for an all-zero block),
+ *               written as the byte e + 127 -- the Microscaling block format
+ *               that "FP8混合精度推理全链路部署实战"
+ *               (ybb.press/ai-applications/14145.html) sec. 7.1 names for
+ *               Blackwell; codes = fp8_rne_satfinite(x * 2^-e), exact scaling.
  * code          = fp8_rne_satfinite(x / s), IEEE fp32 division; codes are
  *               bit-exact with the definition above.
  * Requirements  head_dim % 16 == 0, head_dim <= 768; group_size in
- *               {16,32,64,128,256} dividing head_dim; block_size > 0;
+ *               {16,32,64,128,256} dividing head_dim ({16,32} for MX_BLOCK);
+ *               block_size > 0;
  *               16-byte aligned k, v, caches and scales.
  * Errors        negative code, nothing launched.  A slot past the pool is
  *               skipped and sets FP8PA_DEVERR_SLOT_RANGE.

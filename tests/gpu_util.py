@@ -56,7 +56,15 @@ def to_dev_bf16(bits: np.ndarray) -> torch.Tensor:
 
 
 def n_scale_groups(w):
-    return w.head_dim // w.group_size if w.scale_mode == W.SCALE_TOKEN_GROUP else 1
+    grouped = (W.SCALE_TOKEN_GROUP, W.SCALE_MX_BLOCK)
+    return w.head_dim // w.group_size if w.scale_mode in grouped else 1
+
+
+def scale_dtype(w, torch_side=True):
+    """E8M0 bytes for the MX block mode, fp32 scales otherwise."""
+    if w.scale_mode == W.SCALE_MX_BLOCK:
+        return torch.uint8 if torch_side else np.uint8
+    return torch.float32 if torch_side else np.float32
 
 
 def gpu_cache(w, F, kvs=None, step=True, back=1):
@@ -73,7 +81,7 @@ def gpu_cache(w, F, kvs=None, step=True, back=1):
         ks = F.kv_channel_scales(to_dev_bf16(np.concatenate([k for k, _ in kvs])), w.fmt)
         vs = F.kv_channel_scales(to_dev_bf16(np.concatenate([v for _, v in kvs])), w.fmt)
     else:
-        ks = torch.zeros((nb, hkv, bs, n_scale_groups(w)), dtype=torch.float32, device=DEV)
+        ks = torch.zeros((nb, hkv, bs, n_scale_groups(w)), dtype=scale_dtype(w), device=DEV)
         vs = None if w.mla else torch.zeros_like(ks)
     pk, pv, ps = [], [], []
     for b, (k, v) in enumerate(kvs):
@@ -111,7 +119,7 @@ def oracle_cache(w, kvs=None, requests=None):
         ks = oracle.kv_channel_scales(np.concatenate([k for k, _ in kvs]), w.fmt)
         vs = oracle.kv_channel_scales(np.concatenate([v for _, v in kvs]), w.fmt)
     else:
-        ks = np.zeros((nb, hkv, bs, n_scale_groups(w)), np.float32)
+        ks = np.zeros((nb, hkv, bs, n_scale_groups(w)), scale_dtype(w, torch_side=False))
         vs = None if w.mla else np.zeros_like(ks)
     for b, (k, v) in enumerate(kvs):
         if requests is not None and b not in requests:

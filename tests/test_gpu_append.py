@@ -157,3 +157,32 @@ def test_running_absmax_calibration_matches_oracle(F):
         amax2 = amax.clone()
         F.kv_scales_from_absmax(amax2, fmt, out=amax2)
         assert np.array_equal(amax2.cpu().numpy().view(np.uint32), want.view(np.uint32))
+
+
+@pytest.mark.parametrize("fmt", [W.E4M3, W.E5M2])
+@pytest.mark.parametrize("gs", [16, 32])
+def test_every_finite_bf16_pattern_mx_blocks(F, fmt, gs):
+    """MX block mode over rows that together hold every finite bf16 value:
+    E8M0 block exponents and codes bit-exact with the oracle."""
+    from gpu_util import DEV, to_dev_bf16
+    d = 128
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    xf = W.bf16_bits_to_f32(bits)
+    fin = bits[np.isfinite(xf)]
+    rng = np.random.default_rng(gs + fmt)
+    fin = rng.permutation(fin)
+    pad = (-fin.size) % (2 * d)
+    fin = np.concatenate([fin, np.zeros(pad, np.uint16)])
+    x = fin.reshape(-1, 2, d)
+    n, bs = x.shape[0], 16
+    nb = (n + bs - 1) // bs + 1
+    kc = torch.zeros((nb, 2, bs, d), dtype=torch.uint8, device=DEV)
+    ke = torch.zeros((nb, 2, bs, d // gs), dtype=torch.uint8, device=DEV)
+    slots = rng.permutation(nb * bs)[:n].astype(np.int32)
+    F.kv_append_quant(to_dev_bf16(x), None, torch.from_numpy(slots).to(DEV), kc, None, ke, None,
+                      fmt=fmt, scale_mode=W.SCALE_MX_BLOCK, group_size=gs)
+    okc = np.zeros((nb, 2, bs, d), np.uint8)
+    oke = np.zeros((nb, 2, bs, d // gs), np.uint8)
+    oracle.kv_append_quant(x, None, slots, fmt, W.SCALE_MX_BLOCK, gs, okc, None, oke, None, bs)
+    _assert_codes_equal(kc.cpu().numpy(), okc, "codes")
+    assert np.array_equal(ke.cpu().numpy(), oke), "exponents"

@@ -14,7 +14,7 @@ from fp8_quantised_paged_gb300 import workloads as W
 pytestmark = pytest.mark.gpu
 
 E4, E5 = W.E4M3, W.E5M2
-TH, CS, TG = W.SCALE_TOKEN_HEAD, W.SCALE_CHANNEL_STATIC, W.SCALE_TOKEN_GROUP
+TH, CS, TG, MX = W.SCALE_TOKEN_HEAD, W.SCALE_CHANNEL_STATIC, W.SCALE_TOKEN_GROUP, W.SCALE_MX_BLOCK
 
 # name, hq, hkv, d, bs, fmt, mode
 CASES = [
@@ -77,3 +77,38 @@ def test_shape_multiquery_matches_oracle(F, case):
     check_close(gpu_multiquery(w, F, qc, g, out_dtype=torch.float32),
                 oracle_multiquery(w, qc, o, 3), bf16_out=False, what=f"{name} q_len=3")
     assert F.get_device_error() == 0
+
+
+# MX block-scaled caches: name, hq, hkv, d, bs, fmt, group_size
+MX_CASES = [
+    ("mx32_e4m3_d128_bs16_g8", 64, 8, 128, 16, E4, 32),
+    ("mx16_e5m2_d64_bs32_g4", 16, 4, 64, 32, E5, 16),
+    ("mx16_e4m3_d128_bs64_g8", 16, 2, 128, 64, E4, 16),
+    ("mx32_e5m2_d64_bs16_g8", 8, 1, 64, 16, E5, 32),
+]
+
+
+@pytest.mark.parametrize("case", MX_CASES, ids=[c[0] for c in MX_CASES])
+def test_mx_block_matches_oracle(F, case):
+    """Block exponents and codes bit-exact; attention (bf16 and f32 outputs,
+    and a 3-query chunk) within tolerance of the oracle."""
+    from gpu_util import (check_close, gpu_attention, gpu_cache, gpu_multiquery, oracle_attention,
+                          oracle_cache, oracle_multiquery)
+    name, hq, hkv, d, bs, fmt, gs = case
+    w = W.make_shape_case(name, _lens(bs), hq, hkv, d, bs, fmt, MX,
+                          seed=3000 + MX_CASES.index(case), group_size=gs)
+    kvs = [W.request_kv(w, b) for b in range(w.batch)]
+    g = gpu_cache(w, F, kvs)
+    o = oracle_cache(w, kvs)
+    for got, want, what in zip(g, o, ("K codes", "V codes", "K exponents", "V exponents")):
+        assert np.array_equal(got.cpu().numpy(), want), what
+    q = W.queries(w)
+    ref = oracle_attention(w, q, o)
+    check_close(gpu_attention(w, F, q, g), ref, bf16_out=True, what=f"{name} bf16")
+    check_close(gpu_attention(w, F, q, g, out_dtype=torch.float32), ref, bf16_out=False,
+                what=f"{name} f32")
+    qc = W.chunk_queries(w, 3)
+    short = bool((w.seq_lens < 3).any())
+    check_close(gpu_multiquery(w, F, qc, g, out_dtype=torch.float32),
+                oracle_multiquery(w, qc, o, 3), bf16_out=False, what=f"{name} q_len=3")
+    assert F.get_device_error() == (4 if short else 0)
