@@ -48,6 +48,9 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["fp8pa", "reference"], default="fp8pa")
     ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--mx-block", type=int, default=0, choices=[0, 16, 32],
+                    help="store the GQA workload's cache in the MX block-scaled mode "
+                         "(one E8M0 exponent per block of this many dims)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--traffic-json", default=os.path.join(ROOT, "profiles", "traffic.json"),
@@ -68,9 +71,12 @@ def accounting(w: W.Workload, b_sel=None) -> dict:
         sc_tok = 4 * w.n_kv_heads * ntens
     elif w.scale_mode == W.SCALE_TOKEN_GROUP:
         sc_tok = 4 * w.n_kv_heads * (w.head_dim // w.group_size) * ntens
+    elif w.scale_mode == W.SCALE_MX_BLOCK:  # one E8M0 byte per block
+        sc_tok = w.n_kv_heads * (w.head_dim // w.group_size) * ntens
     else:
         sc_tok = 0
-    static_sc = 4 * w.n_kv_heads * w.head_dim * ntens if w.scale_mode == W.SCALE_CHANNEL_STATIC else 0
+    static_sc = (4 * w.n_kv_heads * w.head_dim * ntens
+                 if w.scale_mode == W.SCALE_CHANNEL_STATIC else 0)
     kv = kv_tokens * (codes + sc_tok) + static_sc
     q = B * w.n_q_heads * w.head_dim * 2
     out = B * w.n_q_heads * w.head_dim_v * 2
@@ -81,6 +87,22 @@ def accounting(w: W.Workload, b_sel=None) -> dict:
     append = B * (codes * 2 + codes + sc_tok) + B * 4
     return {"kv_tokens": kv_tokens, "bytes_per_token": codes + sc_tok, "split": split,
             "decode": decode, "append": append, "step": decode + append}
+
+
+def bench_workload(args) -> W.Workload:
+    """The named full-size workload, optionally with an MX block-scaled cache."""
+    w = W.make_workload(args.workload, "full")
+    if args.mx_block:
+        if w.mla:
+            raise SystemExit("--mx-block applies to the grouped-query workloads")
+        w.scale_mode, w.group_size = W.SCALE_MX_BLOCK, args.mx_block
+        w.name = f"{w.name}_mx{args.mx_block}"
+    return w
+
+
+def scale_groups(w) -> int:
+    grouped = (W.SCALE_TOKEN_GROUP, W.SCALE_MX_BLOCK)
+    return w.head_dim // w.group_size if w.scale_mode in grouped else 1
 
 
 # ---------------------------------------------------------------- clocks
@@ -198,14 +220,15 @@ def oracle_sample(w: W.Workload, b: int, heads=None, threads=None):
     L = int(w.seq_lens[b])
     bs, hkv, d = w.block_size, w.n_kv_heads, w.head_dim
     nbl = (L + bs - 1) // bs
-    ng = d // w.group_size if w.scale_mode == W.SCALE_TOKEN_GROUP else 1
+    ng = scale_groups(w)
     kc = np.zeros((nbl, hkv, bs, d), np.uint8)
     vc = None if w.mla else np.zeros_like(kc)
     if w.scale_mode == W.SCALE_CHANNEL_STATIC:
         ks = oracle.kv_channel_scales(k, w.fmt)
         vs = oracle.kv_channel_scales(v, w.fmt)
     else:
-        ks = np.zeros((nbl, hkv, bs, ng), np.float32)
+        ks = np.zeros((nbl, hkv, bs, ng),
+                      np.uint8 if w.scale_mode == W.SCALE_MX_BLOCK else np.float32)
         vs = None if w.mla else np.zeros_like(ks)
     t = np.arange(L)
     slots = (t // bs * bs + t % bs).astype(np.int32)
@@ -232,7 +255,7 @@ def run_reference(args, rank):
     import oracle
     if rank != 0:
         return
-    w = W.make_workload(args.workload, "full")
+    w = bench_workload(args)
     G = w.n_q_heads // w.n_kv_heads
     threads = oracle.max_threads()
     times, nbytes, toks = [], 0.0, 0.0
@@ -268,11 +291,11 @@ def run_gpu(args, rank, world, local_rank):
 
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
-    w = W.make_workload(args.workload, "full")
+    w = bench_workload(args)
     acc = accounting(w)
     nb, hkv, bs, d = w.num_blocks, w.n_kv_heads, w.block_size, w.head_dim
     ntens = 1 if w.mla else 2
-    ng = d // w.group_size if w.scale_mode == W.SCALE_TOKEN_GROUP else 1
+    ng = scale_groups(w)
 
     # ---- cache: prefill every request's first L-1 tokens through the library
     kc = torch.zeros((nb, hkv, bs, d), dtype=torch.uint8, device=dev)
@@ -284,7 +307,8 @@ def run_gpu(args, rank, world, local_rank):
         vs = F.kv_channel_scales(to_bf16_tensor(np.concatenate([v for _, v in kvs]), dev), w.fmt)
         get = lambda b: kvs[b]
     else:
-        ks = torch.zeros((nb, hkv, bs, ng), dtype=torch.float32, device=dev)
+        sdt = torch.uint8 if w.scale_mode == W.SCALE_MX_BLOCK else torch.float32
+        ks = torch.zeros((nb, hkv, bs, ng), dtype=sdt, device=dev)
         vs = None if w.mla else torch.zeros_like(ks)
         get = lambda b: W.request_kv(w, b)
     for b in range(w.batch):

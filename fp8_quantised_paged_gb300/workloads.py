@@ -83,7 +83,8 @@ class Workload:
                 "n_kv_heads": self.n_kv_heads, "head_dim": self.head_dim,
                 "head_dim_v": self.head_dim_v, "block_size": self.block_size,
                 "kv_fmt": "e4m3" if self.fmt == E4M3 else "e5m2",
-                "scale_mode": ["token_head", "channel_static", "token_group"][self.scale_mode],
+                "scale_mode": ["token_head", "channel_static", "token_group",
+                               f"mx_block_{self.group_size}"][self.scale_mode],
                 "kv_tokens": self.total_tokens, "num_blocks": self.num_blocks}
 
 
