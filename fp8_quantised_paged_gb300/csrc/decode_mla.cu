@@ -285,7 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const MlaParams 
       const int bcol = 8 * ((lane >> 3) & 1);
       const uint32_t aaddr = qs_base + (arow * kStride + acol) * 2;
       const uint32_t baddr = cs_base + (brow * kStride + bcol) * 2;
-#pragma unroll 1
+#pragma unroll 9
       for (int gi = 0; gi < kGroups; ++gi) {
         float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
@@ -389,7 +389,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const MlaParams 
 #pragma unroll
       for (int gg = 0; gg < 2; ++gg) {
         const int gv = 2 * tq + gg;
-#pragma unroll 1
+#pragma unroll 4
         for (int kk = 0; kk < 4; ++kk) {
           const int t0 = 16 * kk + 2 * c;
           const float sa = Ss[t0 * kGroups + gv] * pf, sb = Ss[(t0 + 1) * kGroups + gv] * pf;
