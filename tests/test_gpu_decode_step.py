@@ -94,3 +94,64 @@ def test_decode_step_with_nothing_to_append(F):
                         bt, sl, w.n_kv_heads, w.sm_scale, **kw)
     assert torch.equal(ref, got)
     assert F.get_device_error() == 0
+
+
+def test_decode_step_replays_from_a_cuda_graph(F):
+    """The step captured once in a CUDA graph (with its host-to-device input
+    copy and device-to-host output copy) and replayed: the output equals an
+    eager call's bit for bit, and replays pick up new inputs."""
+    from gpu_util import DEV, gpu_cache, to_dev_bf16
+    w = W.make_workload(2, "small")
+    kvs = [W.request_kv(w, b) for b in range(w.batch)]
+    c = gpu_cache(w, F, kvs, step=False)
+    kn = np.stack([k[-1] for k, _ in kvs])
+    vn = np.stack([v[-1] for _, v in kvs])
+    q = W.queries(w)
+    bt = torch.from_numpy(w.block_tables).to(DEV)
+    sl = torch.from_numpy(w.seq_lens).to(DEV)
+    slots = torch.from_numpy(W.step_slots(w)).to(DEV)
+    kw = dict(fmt=w.fmt, scale_mode=w.scale_mode, out_dtype=torch.float32)
+    ws = torch.empty(F.decode_workspace_bytes(w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim,
+                                              w.head_dim, w.block_size, w.max_blocks),
+                     dtype=torch.uint8, device=DEV)
+    # eager reference (on a copy of the cache)
+    ce = tuple(t.clone() for t in c)
+    ref = F.decode_step(to_dev_bf16(kn), to_dev_bf16(vn), slots, to_dev_bf16(q), *ce, bt, sl,
+                        w.n_kv_heads, w.sm_scale, workspace=ws, **kw)
+    # graph: pinned inputs -> device, step, device -> pinned output
+    q_h = torch.from_numpy(q.view(np.int16)).pin_memory()
+    q_d = torch.empty(q_h.shape, dtype=torch.int16, device=DEV)
+    kn_d, vn_d = to_dev_bf16(kn), to_dev_bf16(vn)
+    out = torch.empty_like(ref)
+    out_h = torch.empty(out.shape, dtype=torch.float32).pin_memory()
+
+    def body():
+        q_d.copy_(q_h, non_blocking=True)
+        F.decode_step(kn_d, vn_d, slots, q_d.view(torch.bfloat16), *c, bt, sl, w.n_kv_heads,
+                      w.sm_scale, out=out, workspace=ws, **kw)
+        out_h.copy_(out, non_blocking=True)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        body()                                   # warm-up outside the capture
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        body()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out_h, ref.cpu())
+    assert F.get_device_error() == 0
+    # new query values through the same pinned buffer
+    q_h.copy_(torch.from_numpy((q ^ np.uint16(0x8000)).view(np.int16)))   # q -> -q
+    g.replay()
+    torch.cuda.synchronize()
+    ce2 = tuple(t.clone() for t in c)
+    ref2 = F.decode_step(to_dev_bf16(kn), to_dev_bf16(vn), slots,
+                         to_dev_bf16(q ^ np.uint16(0x8000)), *ce2, bt, sl, w.n_kv_heads,
+                         w.sm_scale, workspace=ws, **kw)
+    assert torch.equal(out_h, ref2.cpu())
+    assert not torch.equal(ref2, ref)
