@@ -44,6 +44,7 @@ _SIGS = {
                                                     _I, _I, _I, _I, _I, _I, ctypes.c_float, _I,
                                                     _P, _I, _P]),
     "fp8pa_get_device_error": (_I, [_P, ctypes.POINTER(ctypes.c_uint32)]),
+    "fp8pa_selftest_bounded_wait": (_I, [ctypes.c_longlong, _P]),
     "fp8pa_set_decode_workers": (_I, [_I]),
     "fp8pa_set_split_events": (_I, [_P, _P]),
     "fp8pa_error_string": (ctypes.c_char_p, [_I]),

@@ -100,6 +100,25 @@ int ctas_per_sm(const void* fn, int threads, int smem) {
   return per_sm;
 }
 
+namespace {
+
+// One warp waits on a barrier that no copy or thread completes; the bounded
+// wait gives up after `limit` cycles and records the timeout.
+__global__ void __launch_bounds__(32) bounded_wait_selftest_kernel(long long limit,
+                                                                  uint32_t* err) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_barrier_init();
+  }
+  __syncwarp();
+  const bool landed = mbar_wait_bounded(&bar, 0, limit);
+  if (!__all_sync(0xffffffffu, landed) && threadIdx.x == 0)
+    raise_error(err, FP8PA_DEVERR_TIMEOUT);
+}
+
+}  // namespace
+
 bool encode_tensor_map_2d_u8(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows,
                              uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle swz) {
   static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
@@ -462,6 +481,15 @@ int fp8pa_decode_step(const void* k_new, const void* v_new, const int32_t* slot_
   if (e != cudaSuccess) return FP8PA_ERR_CUDA;
   a.plan_ready = true;
   return cuda_status(launch_decode(path, a, cs));
+}
+
+int fp8pa_selftest_bounded_wait(long long limit_cycles, void* stream) {
+  const long long limit =
+      limit_cycles < 1000 ? 1000 : (limit_cycles > kWaitLimitCycles ? kWaitLimitCycles : limit_cycles);
+  uint32_t* err = device_error_ptr(nullptr);
+  if (!err) return FP8PA_ERR_CUDA;
+  bounded_wait_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(limit, err);
+  return cuda_status(cudaGetLastError());
 }
 
 int fp8pa_get_device_error(void* stream, uint32_t* flags) {

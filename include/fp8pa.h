@@ -311,6 +311,16 @@ int fp8pa_paged_decode_attention_static_ws(const void* q, const uint8_t* k_cache
 int fp8pa_get_device_error(void* stream, uint32_t* flags);
 
 /*
+ * Self-test of the bounded waits every kernel uses on its asynchronous
+ * copies: one warp waits on a shared-memory barrier that nothing completes,
+ * for at most `limit_cycles` SM cycles (clamped to [1e3, 4e9]), then records
+ * FP8PA_DEVERR_TIMEOUT in the device error word and returns -- exactly what
+ * a decode warp does when a copy never lands.  Read the result with
+ * fp8pa_get_device_error().  Nothing is faulted, trapped or left hanging.
+ */
+int fp8pa_selftest_bounded_wait(long long limit_cycles, void* stream);
+
+/*
  * Tuning and testing knob: the number of split workers the decode uses
  * (0 = one per resident warp slot on the device, the default).  It changes
  * how the sequences are cut into partials, never the result beyond fp32

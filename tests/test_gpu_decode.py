@@ -222,3 +222,19 @@ def test_full_ragged_e5m2_sampled(F):
 @pytest.mark.slow
 def test_full_mla_latent_sampled(F):
     _full_size_sampled(F, 5, sample=(0, 31))
+
+
+def test_bounded_wait_gives_up_and_reports(F):
+    """Failure detection without a fault: a warp waiting on a barrier that
+    nothing completes gives up after its cycle limit (here ~1 ms), records
+    the timeout bit and returns; the context stays usable."""
+    import time
+    from fp8_quantised_paged_gb300 import _native as N
+    F.get_device_error()
+    t0 = time.perf_counter()
+    N.check(N.lib.fp8pa_selftest_bounded_wait(2_000_000, None), "selftest")
+    assert F.get_device_error() == N.DEVERR_TIMEOUT
+    assert time.perf_counter() - t0 < 5.0
+    # the device still runs work afterwards
+    x = torch.ones(4, device="cuda:0")
+    assert float((x * 2).sum()) == 8.0
