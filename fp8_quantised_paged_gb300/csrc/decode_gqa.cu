@@ -9,12 +9,14 @@
 //   k^ = decode(code) * scale, query head h reading KV head h / G.
 //
 // GB300 design.
-//  * Work is the flat list of units (request b, kv head, page j).  A planner
-//    kernel cuts it into equal contiguous ranges, one per warp of a grid that
-//    fills every SM; a range that crosses a (b, kv head) boundary yields one
-//    partial per piece.  A merge kernel folds the partials of each output
-//    row with the log-sum-exp rule.  Balance is exact for ragged batches and
-//    a 128K-token request spreads over the whole GPU.
+//  * Work is the flat list of units (request b, page j).  The planner
+//    (plan.cuh) cuts it into equal contiguous ranges, one per resident CTA.
+//    A CTA's warps are the KV heads of one head set and walk the range's
+//    pages together, so they read each block's adjacent per-head slices.  A
+//    range that crosses a request boundary yields one partial per request;
+//    the merge (merge.cu) folds the partials of each output row with the
+//    log-sum-exp rule.  Balance is exact for ragged batches and a
+//    128K-token request spreads over the whole GPU.
 //  * Each warp streams its pages through a private ring of shared-memory
 //    stages filled by the tensor-copy engine (TMA, 2-D boxes of
 //    block_size x head_dim bytes with the 128/64-byte swizzle) plus 1-D bulk
@@ -27,7 +29,8 @@
 //    exactly to f16 in registers.  Scales stay outside the contraction: the
 //    per-token K scale multiplies the score, the per-token V scale folds
 //    into P, per-channel K scales fold into q, per-channel V scales multiply
-//    the output.  Power-of-two normalisers keep q and P inside f16's range.
+//    the output; MX block exponents scale the f16 fragments by exact powers
+//    of two.  Power-of-two normalisers keep q and P inside f16's range.
 //  * Softmax runs in FP32 in the log2 domain with warp-shuffle maxima.
 #include <float.h>
 
@@ -804,7 +807,7 @@ cudaError_t launch_decode_gqa(const DecodeShape& s, const DecodeArgs& a, cudaStr
   if (g_split_ev_stop) cudaEventRecord(g_split_ev_stop, stream);
 
   return launch_merge(plan, part_ml, part_o, a.out, s.batch, s.hq, s.hkv, G, s.dv, a.out_dtype,
-                      /*pieces_per_request=*/true, stream);
+                      stream);
 }
 
 cudaError_t launch_plan(const int32_t* seq_lens, int batch, int qlen, int groups, int bs,

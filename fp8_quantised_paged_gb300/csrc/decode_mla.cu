@@ -526,7 +526,7 @@ cudaError_t launch_decode_mla(const DecodeShape& s, const DecodeArgs& a, cudaStr
   if (e != cudaSuccess) return e;
   if (g_split_ev_stop) cudaEventRecord(g_split_ev_stop, stream);
   return launch_merge(plan, part_ml, part_o, a.out, s.batch, s.hq, H, kHeads, kDv, a.out_dtype,
-                      /*pieces_per_request=*/true, stream);
+                      stream);
 }
 
 }  // namespace fp8pa

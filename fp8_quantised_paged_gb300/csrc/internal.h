@@ -81,7 +81,7 @@ cudaError_t launch_plan(const int32_t* seq_lens, int batch, int qlen, int groups
                         cudaStream_t stream);
 cudaError_t launch_merge(const int* plan, const float* part_ml, const float* part_o, void* out,
                          int batch, int hq, int groups, int G, int dv, int out_dtype,
-                         bool pieces_per_request, cudaStream_t stream);
+                         cudaStream_t stream);
 cudaError_t launch_decode_gqa(const DecodeShape& s, const DecodeArgs& a, cudaStream_t stream);
 cudaError_t launch_decode_mla(const DecodeShape& s, const DecodeArgs& a, cudaStream_t stream);
 

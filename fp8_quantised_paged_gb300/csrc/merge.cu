@@ -20,10 +20,7 @@ struct MergeParams {
   const float* part_ml;
   const float* part_o;
   void* out;
-  int B, hq, hkv, G, dv, out_f32;
-  // 0: pieces are numbered per (request, group) (GQA planner with KV heads as
-  // groups); 1: per request, with the group folded into the piece row (MLA).
-  int per_request;
+  int B, hq, hkv, G, dv, out_f32;  // hkv: head groups (KV heads, or 32-head groups)
 };
 
 // One CTA of kMergeWarps warps per output row (b, h): the warps share the
@@ -42,13 +39,11 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const MergePara
   const int b = row / p.hq, h = row % p.hq;
   const int kvh = h / p.G, hh = h % p.G;
   const int* segbase = p.plan + kPlanHeader + p.B + 1;
-  const int e0 = p.per_request ? b : b * p.hkv + kvh;
-  const int sb = segbase[e0], se = segbase[e0 + 1];
+  // pieces of request b: [segbase[b], segbase[b + 1]); piece s holds one row
+  // per (head group, head of the group)
+  const int sb = segbase[b], se = segbase[b + 1];
   // row of piece s for this head
-  auto prow = [&](int s) -> long {
-    return p.per_request ? (static_cast<long>(s) * p.hkv + kvh) * p.G + hh
-                         : static_cast<long>(s) * p.G + hh;
-  };
+  auto prow = [&](int s) -> long { return (static_cast<long>(s) * p.hkv + kvh) * p.G + hh; };
   const float NEG_INF = __int_as_float(0xff800000);
   // Each warp folds its pieces (s = sb + warp, + kMergeWarps, ...) in chunks
   // of C: every load of a chunk (the pieces' (m, l) and this lane's slice of
@@ -140,7 +135,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const MergePara
 
 cudaError_t launch_merge(const int* plan, const float* part_ml, const float* part_o, void* out,
                          int batch, int hq, int groups, int G, int dv, int out_dtype,
-                         bool pieces_per_request, cudaStream_t stream) {
+                         cudaStream_t stream) {
   cudaLaunchAttribute pdl[1];
   pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   pdl[0].val.programmaticStreamSerializationAllowed = 1;
@@ -150,8 +145,7 @@ cudaError_t launch_merge(const int* plan, const float* part_ml, const float* par
   cfg.stream = stream;
   cfg.attrs = pdl;
   cfg.numAttrs = 1;
-  MergeParams mp{plan,      part_ml, part_o, out, batch, hq, groups, G, dv, out_dtype,
-                 pieces_per_request ? 1 : 0};
+  MergeParams mp{plan, part_ml, part_o, out, batch, hq, groups, G, dv, out_dtype};
   cudaError_t e;
   if (dv == 128)
     e = cudaLaunchKernelEx(&cfg, merge_kernel<128>, mp);

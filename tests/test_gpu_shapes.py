@@ -112,3 +112,19 @@ def test_mx_block_matches_oracle(F, case):
     check_close(gpu_multiquery(w, F, qc, g, out_dtype=torch.float32),
                 oracle_multiquery(w, qc, o, 3), bf16_out=False, what=f"{name} q_len=3")
     assert F.get_device_error() == (4 if short else 0)
+
+
+def test_large_batch_matches_oracle(F):
+    """3,000 requests of 1..64 tokens (the planner's scans run ~100 warp
+    passes; most ranges cross many requests), checked in full."""
+    from gpu_util import check_close, gpu_attention, gpu_cache, oracle_attention, oracle_cache
+    rng = np.random.default_rng(5)
+    lens = rng.integers(1, 65, size=3000)
+    w = W.make_shape_case("large_batch", lens, 8, 2, 64, 16, E4, TH, seed=4242)
+    kvs = [W.request_kv(w, b) for b in range(w.batch)]
+    g = gpu_cache(w, F, kvs)
+    o = oracle_cache(w, kvs)
+    q = W.queries(w)
+    check_close(gpu_attention(w, F, q, g, out_dtype=torch.float32), oracle_attention(w, q, o),
+                bf16_out=False, what="large batch")
+    assert F.get_device_error() == 0
