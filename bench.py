@@ -51,6 +51,9 @@ def parse_args():
     ap.add_argument("--mx-block", type=int, default=0, choices=[0, 16, 32],
                     help="store the GQA workload's cache in the MX block-scaled mode "
                          "(one E8M0 exponent per block of this many dims)")
+    ap.add_argument("--q-len", type=int, default=1,
+                    help="queries per request: a causal chunk (the last q_len tokens of each "
+                         "request are appended, then attend); 1 is plain decode")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--traffic-json", default=os.path.join(ROOT, "profiles", "traffic.json"),
@@ -59,8 +62,9 @@ def parse_args():
 
 
 # ---------------------------------------------------------------- accounting
-def accounting(w: W.Workload, b_sel=None) -> dict:
-    """Algorithmic bytes of one step (or of the requests in b_sel)."""
+def accounting(w: W.Workload, b_sel=None, q_len: int = 1) -> dict:
+    """Algorithmic bytes of one step (or of the requests in b_sel): the cache
+    is read once however many queries a request has in its chunk."""
     bs = w.block_size
     lens = w.seq_lens if b_sel is None else w.seq_lens[list(b_sel)]
     B = len(lens)
@@ -78,13 +82,13 @@ def accounting(w: W.Workload, b_sel=None) -> dict:
     static_sc = (4 * w.n_kv_heads * w.head_dim * ntens
                  if w.scale_mode == W.SCALE_CHANNEL_STATIC else 0)
     kv = kv_tokens * (codes + sc_tok) + static_sc
-    q = B * w.n_q_heads * w.head_dim * 2
-    out = B * w.n_q_heads * w.head_dim_v * 2
+    q = B * q_len * w.n_q_heads * w.head_dim * 2
+    out = B * q_len * w.n_q_heads * w.head_dim_v * 2
     pages = int(sum(math.ceil(int(L) / bs) for L in lens))
     tables = pages * 4 + B * 4
     split = kv + q + tables
     decode = split + out
-    append = B * (codes * 2 + codes + sc_tok) + B * 4
+    append = B * q_len * (codes * 2 + codes + sc_tok + 4)
     return {"kv_tokens": kv_tokens, "bytes_per_token": codes + sc_tok, "split": split,
             "decode": decode, "append": append, "step": decode + append}
 
@@ -292,12 +296,15 @@ def run_gpu(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     w = bench_workload(args)
-    acc = accounting(w)
+    ql = args.q_len
+    if ql > 1:
+        args.no_cpu_baseline = True  # the oracle sample is a one-query decode
+    acc = accounting(w, q_len=ql)
     nb, hkv, bs, d = w.num_blocks, w.n_kv_heads, w.block_size, w.head_dim
     ntens = 1 if w.mla else 2
     ng = scale_groups(w)
 
-    # ---- cache: prefill every request's first L-1 tokens through the library
+    # ---- cache: prefill every request's first L - q_len tokens through the library
     kc = torch.zeros((nb, hkv, bs, d), dtype=torch.uint8, device=dev)
     vc = None if w.mla else torch.zeros_like(kc)
     last_k, last_v = [], []
@@ -314,34 +321,38 @@ def run_gpu(args, rank, world, local_rank):
     for b in range(w.batch):
         k, v = get(b)
         L = int(w.seq_lens[b])
-        if L > 1:
-            F.kv_append_quant(to_bf16_tensor(k[:L - 1], dev),
-                              None if v is None else to_bf16_tensor(v[:L - 1], dev),
-                              torch.from_numpy(W.token_slots(w, b, 0, L - 1)).to(dev), kc, vc,
+        if L > ql:
+            F.kv_append_quant(to_bf16_tensor(k[:L - ql], dev),
+                              None if v is None else to_bf16_tensor(v[:L - ql], dev),
+                              torch.from_numpy(W.token_slots(w, b, 0, L - ql)).to(dev), kc, vc,
                               ks, vs, fmt=w.fmt, scale_mode=w.scale_mode,
                               group_size=w.group_size)
-        last_k.append(k[L - 1])
+        last_k.append(k[L - ql:L])
         if v is not None:
-            last_v.append(v[L - 1])
+            last_v.append(v[L - ql:L])
     if w.mla:
         vc_, vs_ = kc, ks
     else:
         vc_, vs_ = vc, vs
 
     # ---- step inputs, resident
-    q_h = W.queries(w)
-    kn_h = np.stack(last_k)
-    vn_h = None if w.mla else np.stack(last_v)
-    slot_h = W.step_slots(w)
+    q_h = W.queries(w) if ql == 1 else W.chunk_queries(w, ql)
+    kn_h = np.concatenate(last_k)
+    vn_h = None if w.mla else np.concatenate(last_v)
+    slot_h = np.concatenate([W.token_slots(w, b, int(w.seq_lens[b]) - ql, int(w.seq_lens[b]))
+                             for b in range(w.batch)]).astype(np.int32)
     q = to_bf16_tensor(q_h, dev)
     kn = to_bf16_tensor(kn_h, dev)
     vn = None if w.mla else to_bf16_tensor(vn_h, dev)
     slots = torch.from_numpy(slot_h).to(dev)
     bt = torch.from_numpy(w.block_tables).to(dev)
     sl = torch.from_numpy(w.seq_lens).to(dev)
-    out = torch.empty((w.batch, w.n_q_heads, w.head_dim_v), dtype=torch.bfloat16, device=dev)
+    oshape = (w.batch, w.n_q_heads, w.head_dim_v) if ql == 1 else \
+        (w.batch, ql, w.n_q_heads, w.head_dim_v)
+    out = torch.empty(oshape, dtype=torch.bfloat16, device=dev)
     ws = torch.empty(F.decode_workspace_bytes(w.batch, w.n_q_heads, hkv, d, w.head_dim_v, bs,
-                                              w.max_blocks, dev), dtype=torch.uint8, device=dev)
+                                              w.max_blocks, dev, q_len=ql),
+                     dtype=torch.uint8, device=dev)
 
     def step(q_, kn_, vn_, slots_, sl_):
         # one call: append (with the split planner in the same launch),
@@ -502,7 +513,9 @@ def run_gpu(args, rank, world, local_rank):
                            compute="fp8 codes -> exact f16, warp MMA (m16n8k16), f32 accumulate "
                                    "and softmax",
                            l2="no flush: every step reads the whole cache, larger than L2",
-                           step="fp8pa_decode_step: append (1 token/request) and plan, split, merge",
+                           step=f"fp8pa_decode_step: append ({ql} token(s)/request) and plan, "
+                                "split, merge",
+                           q_len=ql,
                            bytes_per_step=acc["step"]),
             "roofline": roof,
             "gpu_launches": 3 * args.steps,

@@ -31,6 +31,7 @@ _SIGS = {
     "fp8pa_kv_channel_absmax_update": (_I, [_P, _I, _I, _I, _P, _P]),
     "fp8pa_kv_scales_from_absmax": (_I, [_P, _I, _I, _P, _P]),
     "fp8pa_decode_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I, _I, _I, _I, _I]),
+    "fp8pa_multiquery_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I, _I, _I, _I, _I, _I]),
     "fp8pa_paged_decode_attention": (_I, [_P, _P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I,
                                           _I, _I, _I, ctypes.c_float, _I, _P, _I, _P,
                                           ctypes.c_size_t, _P]),

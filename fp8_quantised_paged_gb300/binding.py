@@ -144,11 +144,13 @@ def kv_scales_from_absmax(absmax, fmt=E5M2, out=None, stream=None):
 
 
 def decode_workspace_bytes(batch, n_q_heads, n_kv_heads, head_dim, head_dim_v, block_size,
-                           max_blocks_per_seq, device=None) -> int:
+                           max_blocks_per_seq, device=None, q_len=1) -> int:
+    """Workspace bytes for the decode (q_len = 1) or a causal chunk of q_len
+    queries per request (paged_multiquery_attention, decode_step)."""
     with torch.cuda.device(device if device is not None else torch.cuda.current_device()):
-        nbytes = int(N.lib.fp8pa_decode_workspace_bytes(batch, n_q_heads, n_kv_heads, head_dim,
-                                                        head_dim_v, block_size,
-                                                        max_blocks_per_seq))
+        nbytes = int(N.lib.fp8pa_multiquery_workspace_bytes(batch, q_len, n_q_heads, n_kv_heads,
+                                                            head_dim, head_dim_v, block_size,
+                                                            max_blocks_per_seq))
     if nbytes == 0:
         raise Fp8paError(N.ERR_UNSUPPORTED, "decode_workspace_bytes")
     return nbytes
@@ -226,8 +228,8 @@ def paged_multiquery_attention(q, k_cache, v_cache, k_scale, v_scale, block_tabl
     _need(out, out.dtype, "out", dev)
     with _on(dev):
         if workspace is None:
-            need = int(N.lib.fp8pa_decode_workspace_bytes(B * qlen, hq, n_kv_heads, dk, dv, bs,
-                                                          max_blocks))
+            need = int(N.lib.fp8pa_multiquery_workspace_bytes(B, qlen, hq, n_kv_heads, dk, dv,
+                                                              bs, max_blocks))
             if need > 0:
                 workspace = torch.empty(need, dtype=torch.uint8, device=dev)
         _need(workspace, torch.uint8, "workspace", dev)
@@ -274,8 +276,8 @@ def decode_step(k_new, v_new, slot_mapping, q, k_cache, v_cache, k_scale, v_scal
     _need(out, out.dtype, "out", dev)
     with _on(dev):
         if workspace is None:
-            need = int(N.lib.fp8pa_decode_workspace_bytes(B * qlen, hq, n_kv_heads, dk, dv, bs,
-                                                          max_blocks))
+            need = int(N.lib.fp8pa_multiquery_workspace_bytes(B, qlen, hq, n_kv_heads, dk, dv,
+                                                              bs, max_blocks))
             if need > 0:
                 workspace = torch.empty(need, dtype=torch.uint8, device=dev)
         _need(workspace, torch.uint8, "workspace", dev)

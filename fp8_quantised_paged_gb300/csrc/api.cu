@@ -402,16 +402,36 @@ int fp8pa_kv_scales_from_absmax(const float* absmax, int n, int fmt, float* scal
       launch_scales_from_absmax(absmax, n, fmt, scale_out, static_cast<cudaStream_t>(stream)));
 }
 
-size_t fp8pa_decode_workspace_bytes(int batch, int n_q_heads, int n_kv_heads, int head_dim,
-                                    int head_dim_v, int block_size, int max_blocks_per_seq) {
-  const int mode = head_dim == 576 ? FP8PA_SCALE_TOKEN_GROUP : FP8PA_SCALE_TOKEN_HEAD;
-  DecodePath path = decode_path(batch, n_q_heads, n_kv_heads, head_dim, head_dim_v, block_size,
-                                max_blocks_per_seq, FP8PA_E4M3, mode, 64, 1, FP8PA_OUT_BF16);
-  if (path.status != FP8PA_OK) return 0;
+size_t fp8pa_multiquery_workspace_bytes(int batch, int q_len, int n_q_heads, int n_kv_heads,
+                                        int head_dim, int head_dim_v, int block_size,
+                                        int max_blocks_per_seq) {
+  if (q_len <= 0 || batch < 0 || static_cast<long long>(batch) * q_len >= (1ll << 31)) return 0;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-  path.shape.workers = decode_workers(path.shape, FP8PA_E4M3, mode, dev);
-  return decode_workspace_bytes(path.shape);
+  // The largest need over the scale modes and formats of this layout (the
+  // split count follows each kernel's occupancy).
+  const bool mla = head_dim == 576;
+  const int modes[3] = {mla ? FP8PA_SCALE_TOKEN_GROUP : FP8PA_SCALE_TOKEN_HEAD,
+                        FP8PA_SCALE_CHANNEL_STATIC, FP8PA_SCALE_MX_BLOCK};
+  size_t need = 0;
+  for (int m = 0; m < (mla ? 1 : 3); ++m)
+    for (int fmt = FP8PA_E4M3; fmt <= FP8PA_E5M2; ++fmt) {
+      DecodePath path = decode_path(batch * q_len, n_q_heads, n_kv_heads, head_dim, head_dim_v,
+                                    block_size, max_blocks_per_seq, fmt, modes[m],
+                                    mla ? 64 : 16, 1, FP8PA_OUT_BF16);
+      if (path.status != FP8PA_OK) continue;
+      path.shape.qlen = q_len;
+      path.shape.workers = decode_workers(path.shape, fmt, modes[m], dev);
+      const size_t n = decode_workspace_bytes(path.shape);
+      need = n > need ? n : need;
+    }
+  return need;
+}
+
+size_t fp8pa_decode_workspace_bytes(int batch, int n_q_heads, int n_kv_heads, int head_dim,
+                                    int head_dim_v, int block_size, int max_blocks_per_seq) {
+  return fp8pa_multiquery_workspace_bytes(batch, 1, n_q_heads, n_kv_heads, head_dim, head_dim_v,
+                                          block_size, max_blocks_per_seq);
 }
 
 int fp8pa_paged_decode_attention(const void* q, const uint8_t* k_cache, const uint8_t* v_cache,
@@ -470,7 +490,8 @@ int fp8pa_decode_step(const void* k_new, const void* v_new, const int32_t* slot_
     return num_new_tokens == 0 ? FP8PA_OK : cuda_status(launch_append(ap, fmt, scale_mode, cs));
   PlanArgs pl;
   pl.seq_lens = seq_lens;
-  pl.batch = path.shape.batch;
+  pl.qw = path.shape.mla ? 1 : gqa_qw(path.shape);
+  pl.batch = path.shape.batch / pl.qw;  // planned requests
   pl.qlen = q_len;
   pl.bs = plan_block_size(path.shape);
   pl.max_blocks = max_blocks_per_seq;

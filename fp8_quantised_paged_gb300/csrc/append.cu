@@ -158,8 +158,8 @@ __global__ void __launch_bounds__(kAppendWarps * 32) append_plan_kernel(AppendAr
   griddep_launch_dependents();
   if (blockIdx.x == 0) {
     if (threadIdx.x < 32)
-      plan_warp(pl.seq_lens, pl.batch, pl.qlen, 1, pl.bs, pl.max_blocks, pl.workers, pl.plan,
-                pl.err);
+      plan_warp(pl.seq_lens, pl.batch, pl.qlen, pl.qw, 1, pl.bs, pl.max_blocks, pl.workers,
+                pl.plan, pl.err);
     return;
   }
   append_row<FMT, MODE, R>(a,

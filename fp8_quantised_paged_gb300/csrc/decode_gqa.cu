@@ -49,11 +49,11 @@ __device__ __forceinline__ int ld_i32(const int* p) { return *reinterpret_cast<c
 // ---------------------------------------------------------------- planner
 // One warp; lets the split kernel launch at once (it waits for the plan).
 __global__ void __launch_bounds__(32) plan_kernel(const int32_t* seq_lens, int B, int qlen,
-                                                  int groups, int bs, int max_blocks, int workers,
-                                                  int* ws, uint32_t* err) {
+                                                  int qw, int groups, int bs, int max_blocks,
+                                                  int workers, int* ws, uint32_t* err) {
   griddep_wait();  // inputs may come from the kernel before us in the stream
   griddep_launch_dependents();
-  plan_warp(seq_lens, B, qlen, groups, bs, max_blocks, workers, ws, err);
+  plan_warp(seq_lens, B, qlen, qw, groups, bs, max_blocks, workers, ws, err);
 }
 
 // ---------------------------------------------------------------- split kernel
@@ -68,7 +68,8 @@ struct GqaParams {
   float* part_o;
   uint32_t* err;
   int B, hq, hkv, G, max_blocks, num_blocks;
-  int qlen;  // queries per request: B counts (request, query) pairs
+  int qlen;  // queries per request of a causal chunk
+  int qw;    // query warps per KV head: B planned requests of qw queries each
   int gs;    // dims per block exponent (MX block mode)
   float qk_scale_log2;
 };
@@ -143,7 +144,7 @@ __device__ __forceinline__ uint32_t swz(int r, int ch) {
 
 struct Cursor {
   int b, j, nb;
-  long brow;  // offset of request b's block-table row (b / qlen)
+  long brow;  // offset of the block-table row of planned request b (b * qw / qlen)
 };
 
 template <int D, int BS, int FMT, int MODE, int NST>
@@ -196,9 +197,14 @@ __global__ void __launch_bounds__(kMaxWarps * 32)
   // CTA = (page range, set of W KV heads); warp = one KV head.  All warps of
   // a CTA walk the same pages, so together they read a block's adjacent
   // per-head slices.
-  const int hsets = p.hkv / W;
-  const long wid = blockIdx.x / hsets;                  // page range
-  const int kvh = (blockIdx.x % hsets) * W + warp;      // this warp's KV head
+  // A CTA's warps are (KV head, query) pairs: hpc KV heads x qw queries of
+  // the same planned request, all walking the same pages (the qw warps of a
+  // KV head ask for each page together: one DRAM read, the rest from L2).
+  const int hpc = W / p.qw;
+  const int hsets = p.hkv / hpc;
+  const long wid = blockIdx.x / hsets;                            // page range
+  const int kvh = (blockIdx.x % hsets) * hpc + warp / p.qw;       // this warp's KV head
+  const int qi = warp % p.qw;                                     // and query
   const long u0 = wid * upw;
   if (u0 >= U) return;
   const int n_units = static_cast<int>(min(static_cast<long>(upw), U - u0));
@@ -214,7 +220,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32)
     cu.b = lo;
     cu.nb = uprefix[lo + 1] - uprefix[lo];
     cu.j = static_cast<int>(u - uprefix[lo]);
-    cu.brow = static_cast<long>(lo / p.qlen) * p.max_blocks;
+    cu.brow = static_cast<long>(lo) * p.qw / p.qlen * p.max_blocks;
     return cu;
   };
   auto advance = [&](Cursor& cu) {
@@ -225,7 +231,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32)
     } while (cu.b < p.B && uprefix[cu.b + 1] == uprefix[cu.b]);
     if (cu.b < p.B) {
       cu.nb = uprefix[cu.b + 1] - uprefix[cu.b];
-      cu.brow = static_cast<long>(cu.b / p.qlen) * p.max_blocks;
+      cu.brow = static_cast<long>(cu.b) * p.qw / p.qlen * p.max_blocks;
     }
   };
   auto block_of = [&](const Cursor& cu) { return __ldg(p.block_tables + cu.brow + cu.j); };
@@ -301,12 +307,13 @@ __global__ void __launch_bounds__(kMaxWarps * 32)
     if (i == 0 || cc.j == 0) {
       // ---- new segment: load q for the G heads of (b, kv head)
       bool bad;
-      Lb = visible_len(p.seq_lens, cc.b, p.qlen, p.max_blocks * BS, &bad);
+      const int v = cc.b * p.qw + qi;  // this warp's query: row of q and of out
+      Lb = visible_len(p.seq_lens, v, p.qlen, p.max_blocks * BS, &bad);
       const int h = kvh * p.G + g;
       float qv[D / 4];
       if (g < p.G) {
         const uint4* src = reinterpret_cast<const uint4*>(
-            p.q + (static_cast<long>(cc.b) * p.hq + h) * D + c * (D / 4));
+            p.q + (static_cast<long>(v) * p.hq + h) * D + c * (D / 4));
 #pragma unroll
         for (int x = 0; x < D / 32; ++x) {
           const uint4 u = __ldg(src + x);
@@ -587,7 +594,8 @@ __global__ void __launch_bounds__(kMaxWarps * 32)
         l1 += __shfl_xor_sync(0xffffffffu, l1, o);
       }
       // piece rows: (piece of request b) x KV head x query head of the group
-      const long seg = (segbase[cc.b] + (wid - uprefix[cc.b] / upw)) * p.hkv + kvh;
+      const long seg =
+          ((segbase[cc.b] + (wid - uprefix[cc.b] / upw)) * p.hkv + kvh) * p.qw + qi;
       const float fin = DYN ? exp2i(erun - 15) : (1.0f / 16384.f);
 #pragma unroll
       for (int hsel = 0; hsel < 2; ++hsel) {
@@ -685,16 +693,18 @@ SplitKernel pick(int d, int bs, int fmt, int mode) {
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
-// Warps per CTA, one per KV head of the CTA's head set: the divisor of
-// Hkv (at most 8) that keeps the most warps resident per SM -- large pages
-// make a warp's ring big enough that 8 warps would not fit in one CTA's
-// shared memory, or would leave one CTA per SM.  Ties go to the larger
-// head set (its warps share each page's block-table entry and DRAM rows).
+// Warps per CTA: qw query warps for each KV head of the CTA's head set, the
+// head set being the divisor of Hkv (with at most 8 warps in all) that keeps
+// the most warps resident per SM -- large pages make a warp's ring big
+// enough that 8 warps would not fit in one CTA's shared memory, or would
+// leave one CTA per SM.  Ties go to the larger head set (its warps share each
+// page's block-table entry and DRAM rows).
 constexpr int kMaxCtaSmem = 227 * 1024;
-int gqa_wpc(int hkv, const SplitKernel& k) {
-  int best = 1, best_warps = 0;
-  for (int w = 1; w <= kMaxWarps; ++w) {
-    if (hkv % w != 0 || k.smem(w) > kMaxCtaSmem) continue;
+int gqa_wpc(int hkv, int qw, const SplitKernel& k) {
+  int best = qw, best_warps = 0;
+  for (int h = 1; h * qw <= kMaxWarps; ++h) {
+    const int w = h * qw;
+    if (hkv % h != 0 || k.smem(w) > kMaxCtaSmem) continue;
     const int warps = w * ctas_per_sm(reinterpret_cast<const void*>(k.fn), w * 32, k.smem(w));
     if (warps >= best_warps) {
       best = w;
@@ -721,7 +731,8 @@ int decode_workers(const DecodeShape& s, int fmt, int mode, int device) {
   }
   if (g_decode_workers_override > 0) return g_decode_workers_override;
   const SplitKernel k = pick(s.d, s.bs, fmt, mode);
-  const int wpc = gqa_wpc(s.hkv, k), hsets = s.hkv / wpc;
+  const int qw = gqa_qw(s);
+  const int wpc = gqa_wpc(s.hkv, qw, k), hsets = s.hkv / (wpc / qw);
   const int per_sm = ctas_per_sm(reinterpret_cast<const void*>(k.fn), wpc * 32, k.smem(wpc));
   const int ranges = sms * per_sm / hsets;
   return ranges < 1 ? 1 : ranges;
@@ -733,9 +744,11 @@ int decode_workers(const DecodeShape& s, int fmt, int mode, int device) {
 size_t decode_workspace_bytes(const DecodeShape& s) {
   const int groups = s.mla ? s.hq / 32 : s.hkv;
   const int G = s.hq / groups;
+  const int qw = s.mla ? 1 : gqa_qw(s);
+  const size_t bp = s.batch / qw;  // planned requests
   const size_t ranges = s.mla ? static_cast<size_t>(s.workers / groups) : s.workers;
-  const size_t plan = align256(sizeof(int) * (kPlanHeader + 2 * (s.batch + 1)));
-  const size_t rows = (ranges + s.batch) * groups * G;
+  const size_t plan = align256(sizeof(int) * (kPlanHeader + 2 * (bp + 1)));
+  const size_t rows = (ranges + bp) * groups * qw * G;
   const size_t ml = align256(rows * 2 * sizeof(float));
   const size_t o = align256(rows * static_cast<size_t>(s.dv) * sizeof(float));
   return plan + ml + o;
@@ -744,7 +757,9 @@ size_t decode_workspace_bytes(const DecodeShape& s) {
 cudaError_t launch_decode_gqa(const DecodeShape& s, const DecodeArgs& a, cudaStream_t stream) {
   const int G = s.hq / s.hkv;
   const SplitKernel k = pick(s.d, s.bs, a.fmt, a.mode);
-  const int wpc = gqa_wpc(s.hkv, k), hsets = s.hkv / wpc;
+  const int qw = gqa_qw(s);
+  const int bp = s.batch / qw;  // planned requests
+  const int wpc = gqa_wpc(s.hkv, qw, k), hsets = s.hkv / (wpc / qw);
   const int smem = k.smem(wpc);
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(k.fn), smem);
   if (e != cudaSuccess) return e;
@@ -759,13 +774,13 @@ cudaError_t launch_decode_gqa(const DecodeShape& s, const DecodeArgs& a, cudaStr
 
   char* ws = static_cast<char*>(a.workspace);
   int* plan = reinterpret_cast<int*>(ws);
-  const size_t plan_bytes = align256(sizeof(int) * (kPlanHeader + 2 * (s.batch + 1)));
-  const size_t prow = (static_cast<size_t>(s.workers) + s.batch) * s.hkv * G;
+  const size_t plan_bytes = align256(sizeof(int) * (kPlanHeader + 2 * (bp + 1)));
+  const size_t prow = (static_cast<size_t>(s.workers) + bp) * s.hkv * qw * G;
   float* part_ml = reinterpret_cast<float*>(ws + plan_bytes);
   float* part_o = reinterpret_cast<float*>(ws + plan_bytes + align256(prow * 2 * sizeof(float)));
 
   if (!a.plan_ready) {
-    e = launch_plan(a.seq_lens, s.batch, s.qlen, 1, s.bs, s.max_blocks, s.workers, plan, a.err,
+    e = launch_plan(a.seq_lens, bp, s.qlen, qw, 1, s.bs, s.max_blocks, s.workers, plan, a.err,
                     stream);
     if (e != cudaSuccess) return e;
   }
@@ -789,13 +804,14 @@ cudaError_t launch_decode_gqa(const DecodeShape& s, const DecodeArgs& a, cudaStr
   p.part_ml = part_ml;
   p.part_o = part_o;
   p.err = a.err;
-  p.B = s.batch;
+  p.B = bp;
   p.hq = s.hq;
   p.hkv = s.hkv;
   p.G = G;
   p.max_blocks = s.max_blocks;
   p.num_blocks = a.num_blocks;
   p.qlen = s.qlen;
+  p.qw = qw;
   p.gs = a.gs;
   p.qk_scale_log2 = a.sm_scale * 1.4426950408889634f;
   cfg.gridDim = dim3(static_cast<unsigned>(s.workers) * hsets);
@@ -806,11 +822,11 @@ cudaError_t launch_decode_gqa(const DecodeShape& s, const DecodeArgs& a, cudaStr
   if (e != cudaSuccess) return e;
   if (g_split_ev_stop) cudaEventRecord(g_split_ev_stop, stream);
 
-  return launch_merge(plan, part_ml, part_o, a.out, s.batch, s.hq, s.hkv, G, s.dv, a.out_dtype,
+  return launch_merge(plan, part_ml, part_o, a.out, bp, qw, s.hq, s.hkv, G, s.dv, a.out_dtype,
                       stream);
 }
 
-cudaError_t launch_plan(const int32_t* seq_lens, int batch, int qlen, int groups, int bs,
+cudaError_t launch_plan(const int32_t* seq_lens, int batch, int qlen, int qw, int groups, int bs,
                         int max_blocks, int workers, int* plan, uint32_t* err,
                         cudaStream_t stream) {
   cudaLaunchAttribute pdl[1];
@@ -822,7 +838,7 @@ cudaError_t launch_plan(const int32_t* seq_lens, int batch, int qlen, int groups
   cfg.stream = stream;
   cfg.attrs = pdl;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, plan_kernel, seq_lens, batch, qlen, groups, bs, max_blocks,
+  return cudaLaunchKernelEx(&cfg, plan_kernel, seq_lens, batch, qlen, qw, groups, bs, max_blocks,
                             workers, plan, err);
 }
 

@@ -489,7 +489,7 @@ cudaError_t launch_decode_mla(const DecodeShape& s, const DecodeArgs& a, cudaStr
   float* part_o = reinterpret_cast<float*>(ws + plan_bytes + align256(rows * 2 * sizeof(float)));
 
   if (!a.plan_ready) {
-    e = launch_plan(a.seq_lens, s.batch, s.qlen, 1, kBs, s.max_blocks, ranges, plan, a.err,
+    e = launch_plan(a.seq_lens, s.batch, s.qlen, 1, 1, kBs, s.max_blocks, ranges, plan, a.err,
                     stream);
     if (e != cudaSuccess) return e;
   }
@@ -525,8 +525,8 @@ cudaError_t launch_decode_mla(const DecodeShape& s, const DecodeArgs& a, cudaStr
   e = cudaLaunchKernelEx(&cfg, kfn, p);
   if (e != cudaSuccess) return e;
   if (g_split_ev_stop) cudaEventRecord(g_split_ev_stop, stream);
-  return launch_merge(plan, part_ml, part_o, a.out, s.batch, s.hq, H, kHeads, kDv, a.out_dtype,
-                      stream);
+  return launch_merge(plan, part_ml, part_o, a.out, s.batch, 1, s.hq, H, kHeads, kDv,
+                      a.out_dtype, stream);
 }
 
 }  // namespace fp8pa

@@ -24,6 +24,7 @@ cudaError_t launch_append(const AppendArgs& a, int fmt, int mode, cudaStream_t s
 struct PlanArgs {
   const int32_t* seq_lens;
   int batch, qlen, bs, max_blocks, workers;
+  int qw;  // queries per planned request (batch = planned requests)
   int* plan;
   uint32_t* err;
 };
@@ -45,6 +46,13 @@ struct DecodeShape {
   int mla;            // 1 for the shared-latent kernel
   int qlen;           // queries per request (batch counts request x query)
 };
+
+// Query warps per KV head in the grouped-query split kernel: a causal chunk of
+// up to 8 queries has its queries' warps walk the same pages in one CTA (one
+// DRAM read per page); longer chunks run one virtual request per query.
+inline int gqa_qw(const DecodeShape& s) {
+  return (!s.mla && s.qlen > 1 && s.qlen <= 8) ? s.qlen : 1;
+}
 
 size_t decode_workspace_bytes(const DecodeShape& s);
 
@@ -76,11 +84,11 @@ int decode_workers(const DecodeShape& s, int fmt, int mode, int device);
 // `groups` is the number of head groups per request (KV heads for GQA, groups
 // of 32 query heads for MLA) and G the query heads per group.  `batch`
 // counts virtual requests (request x query of a causal chunk of `qlen`).
-cudaError_t launch_plan(const int32_t* seq_lens, int batch, int qlen, int groups, int bs,
+cudaError_t launch_plan(const int32_t* seq_lens, int batch, int qlen, int qw, int groups, int bs,
                         int max_blocks, int workers, int* plan, uint32_t* err,
                         cudaStream_t stream);
 cudaError_t launch_merge(const int* plan, const float* part_ml, const float* part_o, void* out,
-                         int batch, int hq, int groups, int G, int dv, int out_dtype,
+                         int batch, int qw, int hq, int groups, int G, int dv, int out_dtype,
                          cudaStream_t stream);
 cudaError_t launch_decode_gqa(const DecodeShape& s, const DecodeArgs& a, cudaStream_t stream);
 cudaError_t launch_decode_mla(const DecodeShape& s, const DecodeArgs& a, cudaStream_t stream);

@@ -21,6 +21,7 @@ struct MergeParams {
   const float* part_o;
   void* out;
   int B, hq, hkv, G, dv, out_f32;  // hkv: head groups (KV heads, or 32-head groups)
+  int qw;  // queries per planned request: B planned requests, B * qw output rows of heads
 };
 
 // One CTA of kMergeWarps warps per output row (b, h): the warps share the
@@ -36,14 +37,17 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const MergePara
   griddep_launch_dependents();
   const int row = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int b = row / p.hq, h = row % p.hq;
+  const int v = row / p.hq, h = row % p.hq;  // output row (virtual request v, head h)
+  const int b = v / p.qw, qi = v % p.qw;     // planned request and its query
   const int kvh = h / p.G, hh = h % p.G;
   const int* segbase = p.plan + kPlanHeader + p.B + 1;
-  // pieces of request b: [segbase[b], segbase[b + 1]); piece s holds one row
-  // per (head group, head of the group)
+  // pieces of planned request b: [segbase[b], segbase[b + 1]); piece s holds
+  // one row per (head group, query, head of the group)
   const int sb = segbase[b], se = segbase[b + 1];
   // row of piece s for this head
-  auto prow = [&](int s) -> long { return (static_cast<long>(s) * p.hkv + kvh) * p.G + hh; };
+  auto prow = [&](int s) -> long {
+    return ((static_cast<long>(s) * p.hkv + kvh) * p.qw + qi) * p.G + hh;
+  };
   const float NEG_INF = __int_as_float(0xff800000);
   // Each warp folds its pieces (s = sb + warp, + kMergeWarps, ...) in chunks
   // of C: every load of a chunk (the pieces' (m, l) and this lane's slice of
@@ -117,7 +121,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const MergePara
     acc[e] = v;
   }
   const float inv = Lt > 0.f ? 1.0f / Lt : 0.f;
-  const long ob = (static_cast<long>(b) * p.hq + h) * DV + lane * PER;
+  const long ob = (static_cast<long>(v) * p.hq + h) * DV + lane * PER;
   if (p.out_f32) {
     float* o = reinterpret_cast<float*>(p.out) + ob;
 #pragma unroll
@@ -134,18 +138,18 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const MergePara
 }  // namespace
 
 cudaError_t launch_merge(const int* plan, const float* part_ml, const float* part_o, void* out,
-                         int batch, int hq, int groups, int G, int dv, int out_dtype,
+                         int batch, int qw, int hq, int groups, int G, int dv, int out_dtype,
                          cudaStream_t stream) {
   cudaLaunchAttribute pdl[1];
   pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   pdl[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(batch * hq);
+  cfg.gridDim = dim3(batch * qw * hq);
   cfg.blockDim = dim3(kMergeWarps * 32);
   cfg.stream = stream;
   cfg.attrs = pdl;
   cfg.numAttrs = 1;
-  MergeParams mp{plan, part_ml, part_o, out, batch, hq, groups, G, dv, out_dtype};
+  MergeParams mp{plan, part_ml, part_o, out, batch, hq, groups, G, dv, out_dtype, qw};
   cudaError_t e;
   if (dv == 128)
     e = cudaLaunchKernelEx(&cfg, merge_kernel<128>, mp);

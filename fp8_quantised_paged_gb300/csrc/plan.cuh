@@ -28,10 +28,13 @@ __device__ __forceinline__ int warp_incl_scan(int x) {
 }
 
 // Run by one whole warp.  `groups` multiplies the units of a request (1: the
-// split kernels cover every head group of a page in one unit).
-__device__ __forceinline__ void plan_warp(const int32_t* seq_lens, int B, int qlen, int groups,
-                                          int bs, int max_blocks, int workers, int* ws,
-                                          uint32_t* err) {
+// split kernels cover every head group of a page in one unit).  A planned
+// request b holds the qw queries b*qw .. b*qw + qw - 1 of a causal chunk of
+// qlen (qw = 1: one virtual request per query; qw = qlen: one per real
+// request); its pages are those its last query sees.
+__device__ __forceinline__ void plan_warp(const int32_t* seq_lens, int B, int qlen, int qw,
+                                          int groups, int bs, int max_blocks, int workers,
+                                          int* ws, uint32_t* err) {
   const int lane = threadIdx.x & 31;
   const int cap = max_blocks * bs;
   int* uprefix = ws + kPlanHeader;
@@ -42,7 +45,7 @@ __device__ __forceinline__ void plan_warp(const int32_t* seq_lens, int B, int ql
     int n = 0;
     if (b < B) {
       bool bad;
-      const int L = visible_len(seq_lens, b, qlen, cap, &bad);
+      const int L = visible_len(seq_lens, b * qw + qw - 1, qlen, cap, &bad);
       if (bad) raise_error(err, FP8PA_DEVERR_SEQ_LEN);
       n = (L + bs - 1) / bs;
     }

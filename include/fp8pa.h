@@ -165,10 +165,19 @@ int fp8pa_kv_scales_from_absmax(const float* absmax, int n, int fmt, float* scal
 
 /*
  * Bytes of device workspace fp8pa_paged_decode_attention needs for these
- * shapes on the current device (it depends on the device's SM count).
+ * shapes on the current device (it depends on the device's SM count); enough
+ * for every scale mode and format.  0 if the shapes are rejected.
  */
 size_t fp8pa_decode_workspace_bytes(int batch, int n_q_heads, int n_kv_heads, int head_dim,
                                     int head_dim_v, int block_size, int max_blocks_per_seq);
+
+/*
+ * The same for fp8pa_paged_multiquery_attention (and fp8pa_decode_step) with
+ * q_len queries per request; q_len = 1 is fp8pa_decode_workspace_bytes.
+ */
+size_t fp8pa_multiquery_workspace_bytes(int batch, int q_len, int n_q_heads, int n_kv_heads,
+                                        int head_dim, int head_dim_v, int block_size,
+                                        int max_blocks_per_seq);
 
 /*
  * Decode-step attention of one query token per request over its paged,
@@ -229,7 +238,7 @@ int fp8pa_paged_decode_attention(const void* q, const uint8_t* k_cache, const ui
  * seq_lens     i32 [batch], the cached length including the whole chunk.
  *              A request shorter than q_len (or outside [0, cap]) sets
  *              FP8PA_DEVERR_SEQ_LEN; its rows that would see no token are 0.
- * workspace    at least fp8pa_decode_workspace_bytes(batch * q_len, ...).
+ * workspace    at least fp8pa_multiquery_workspace_bytes(batch, q_len, ...).
  * Layout limits, other arguments and errors as fp8pa_paged_decode_attention;
  * q_len <= 0 returns FP8PA_ERR_BAD_SHAPE.
  */
