@@ -117,8 +117,9 @@ __device__ __forceinline__ ExpRow exp_row(const uint8_t* base, int t, int nb) {
 
 // Shared-memory layout for `w` warps (each with its own NST-stage ring);
 // SCB = scale bytes per token per tensor in the ring (4 for one fp32 scale,
-// D/16 for the largest count of E8M0 block exponents, 0 for static scales).
-template <int D, int BS, int NST, int SCB>
+// D/16 for the largest count of E8M0 block exponents, 0 for static scales);
+// XTW = words of the per-warp MX factor table (0 outside MX block mode).
+template <int D, int BS, int NST, int SCB, int XTW>
 struct GqaSmem {
   static constexpr int kPage = BS * D;
   __host__ __device__ static constexpr int pages(int w) { return w * NST * 2 * kPage; }
@@ -126,9 +127,20 @@ struct GqaSmem {
   __host__ __device__ static constexpr int ps(int w) { return w * 512; }
   __host__ __device__ static constexpr int bars(int w) { return w * NST * 8; }
   __host__ __device__ static constexpr int oks(int w) { return w * NST * 4; }
+  __host__ __device__ static constexpr int xt(int w) { return w * XTW * 4; }
   __host__ __device__ static constexpr int bytes(int w) {
-    return pages(w) + scales(w) + ps(w) + bars(w) + oks(w) + 1024;
+    return pages(w) + scales(w) + ps(w) + bars(w) + oks(w) + xt(w) + 1024;
   }
+};
+
+// MX factor table of one 16-token tile: row r < 16 is K token r, row 16 + r
+// is V token r; word k < D/16 of a row holds 2^(e_k - e_max) of block k as
+// an f16 pair, word D/16 the token's scale 2^(e_max - 127) as an fp32.  Rows
+// have an odd stride so that the column reads of a tile spread over banks.
+template <int D>
+struct MxTable {
+  static constexpr int kStride = D / 16 + 1;
+  static constexpr int kWords = 32 * kStride;
 };
 
 // Byte offset of 16-byte chunk `ch` of row `r` in a TMA box written with the
@@ -154,9 +166,10 @@ __global__ void __launch_bounds__(kMaxWarps * 32)
   constexpr bool TOKSC = (MODE == FP8PA_SCALE_TOKEN_HEAD);
   constexpr bool MX = (MODE == FP8PA_SCALE_MX_BLOCK);
   constexpr bool DYN = TOKSC || MX;  // per-token scales: q stays exact in f16
-  using SM = GqaSmem<D, BS, NST, TOKSC ? 4 : (MX ? D / 16 : 0)>;
-  constexpr int PAGE = SM::kPage;
   constexpr int SCB = TOKSC ? 4 : (MX ? D / 16 : 0);
+  constexpr int XS = MxTable<D>::kStride;
+  using SM = GqaSmem<D, BS, NST, SCB, MX ? MxTable<D>::kWords : 0>;
+  constexpr int PAGE = SM::kPage;
   constexpr int TILES = BS / 16;
   constexpr int KW = D / 16;   // K words per row per thread = k-steps
   constexpr int KCH = D / 64;  // 16-byte K chunks per row per thread
@@ -180,6 +193,9 @@ __global__ void __launch_bounds__(kMaxWarps * 32)
       reinterpret_cast<uint64_t*>(smem + SM::pages(W) + SM::scales(W) + SM::ps(W)) + warp * NST;
   int* okf = reinterpret_cast<int*>(smem + SM::pages(W) + SM::scales(W) + SM::ps(W) +
                                     SM::bars(W)) + warp * NST;
+  uint32_t* xt = reinterpret_cast<uint32_t*>(smem + SM::pages(W) + SM::scales(W) + SM::ps(W) +
+                                             SM::bars(W) + SM::oks(W)) +
+                 warp * (MX ? MxTable<D>::kWords : 0);
 
   if (lane == 0) {
     for (int s = 0; s < NST; ++s) mbar_init(&bars[s], 1);
@@ -408,17 +424,29 @@ __global__ void __launch_bounds__(kMaxWarps * 32)
         sv0 = v0 ? svs[r0 + g] : 0.f;
         sv1 = v1 ? svs[r0 + g + 8] : 0.f;
       } else if constexpr (MX) {
+        // Each lane builds one row of the tile's factor table (lane < 16: K
+        // token lane, else V token lane - 16), then every lane reads the
+        // words its fragments need.
+        __syncwarp();  // the previous tile's reads are done
+        {
+          const ExpRow e = exp_row(lane < 16 ? kex : vex, r0 + (lane & 15), nbx);
+          const int em = e.max_byte();
+          uint32_t* row = xt + lane * XS;
+#pragma unroll
+          for (int k = 0; k < D / 16; ++k)
+            if (k < nbx) row[k] = h2_pow2(e.byte(k) - em);
+          row[D / 16] = __float_as_uint(exp2i(em - 127));
+        }
+        __syncwarp();
         const int kb0 = (c * (D / 4)) / p.gs, kb1 = (c * (D / 4) + D / 4 - 1) / p.gs;
-        const ExpRow e0 = exp_row(kex, r0 + g, nbx), e1 = exp_row(kex, r0 + g + 8, nbx);
-        const int m0e = e0.max_byte(), m1e = e1.max_byte();
-        fk0a = h2_pow2(e0.byte(kb0) - m0e);
-        fk0b = h2_pow2(e0.byte(kb1) - m0e);
-        fk1a = h2_pow2(e1.byte(kb0) - m1e);
-        fk1b = h2_pow2(e1.byte(kb1) - m1e);
-        sk0 = exp2i(m0e - 127);
-        sk1 = exp2i(m1e - 127);
-        sv0 = v0 ? exp2i(exp_row(vex, r0 + g, nbx).max_byte() - 127) : 0.f;
-        sv1 = v1 ? exp2i(exp_row(vex, r0 + g + 8, nbx).max_byte() - 127) : 0.f;
+        fk0a = xt[g * XS + kb0];
+        fk0b = xt[g * XS + kb1];
+        fk1a = xt[(g + 8) * XS + kb0];
+        fk1b = xt[(g + 8) * XS + kb1];
+        sk0 = __uint_as_float(xt[g * XS + D / 16]);
+        sk1 = __uint_as_float(xt[(g + 8) * XS + D / 16]);
+        sv0 = v0 ? __uint_as_float(xt[(16 + g) * XS + D / 16]) : 0.f;
+        sv1 = v1 ? __uint_as_float(xt[(24 + g) * XS + D / 16]) : 0.f;
       }
       // two independent accumulator chains (even / odd k-steps)
       float acc[4] = {0.f, 0.f, 0.f, 0.f}, acc2[4] = {0.f, 0.f, 0.f, 0.f};
@@ -551,10 +579,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32)
         const int vb = ((D == 128 ? 16 : 8) * g) / p.gs;
         uint32_t f[4];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const ExpRow e = exp_row(vex, r0 + 4 * c + ((u + c) & 3), nbx);
-          f[u] = h2_pow2(e.byte(vb) - e.max_byte());
-        }
+        for (int u = 0; u < 4; ++u) f[u] = xt[(16 + 4 * c + ((u + c) & 3)) * XS + vb];
         fv01 = (f[0] & 0xFFFFu) | (f[1] & 0xFFFF0000u);
         fv23 = (f[2] & 0xFFFFu) | (f[3] & 0xFFFF0000u);
       }
@@ -658,9 +683,9 @@ struct SplitKernel {
 template <int D, int BS, int FMT, int MODE>
 SplitKernel pick4() {
   constexpr int NST = stages_for<D, BS>();
-  constexpr int SCB =
-      MODE == FP8PA_SCALE_TOKEN_HEAD ? 4 : (MODE == FP8PA_SCALE_MX_BLOCK ? D / 16 : 0);
-  using SM = GqaSmem<D, BS, NST, SCB>;
+  constexpr bool MX = MODE == FP8PA_SCALE_MX_BLOCK;
+  constexpr int SCB = MODE == FP8PA_SCALE_TOKEN_HEAD ? 4 : (MX ? D / 16 : 0);
+  using SM = GqaSmem<D, BS, NST, SCB, MX ? MxTable<D>::kWords : 0>;
   return {gqa_split_kernel<D, BS, FMT, MODE, NST>, SM::bytes(1) - 1024};
 }
 
