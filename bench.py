@@ -29,6 +29,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -118,7 +119,9 @@ class ClockSampler:
     def __init__(self, index: int):
         self.index = index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{index}.csv")
+        # raw samples: FP8PA_CLOCKS_DIR if set (to keep them), else a temp dir
+        out_dir = os.environ.get("FP8PA_CLOCKS_DIR") or tempfile.gettempdir()
+        self.path = os.path.join(out_dir, f"fp8pa_clocks_rank{index}.csv")
 
     def start(self):
         try:
