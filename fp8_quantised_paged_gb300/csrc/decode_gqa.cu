@@ -225,13 +225,19 @@ __global__ void __launch_bounds__(kMaxWarps * 32)
   if (u0 >= U) return;
   const int n_units = static_cast<int>(min(static_cast<long>(upw), U - u0));
 
-  // ---- unit cursor: (request, page) of a flat page index
+  // ---- unit cursor: (request, page) of a flat page index.  The request
+  // holding unit u is the count of request starts <= u, less one (the
+  // prefix is nondecreasing and uprefix[B] = U > u); the whole warp tests
+  // 32 starts per load, so for up to 31 requests this is one load latency.
   auto locate = [&](long u) {
-    int lo = 0, hi = p.B;
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (uprefix[mid] <= u) lo = mid; else hi = mid;
+    int cnt = 0;
+    for (int base = 0; base <= p.B; base += 32) {
+      const int k = base + lane;
+      const unsigned le = __ballot_sync(0xffffffffu, k <= p.B && uprefix[k] <= u);
+      cnt += __popc(le);
+      if (le != 0xffffffffu) break;
     }
+    const int lo = cnt - 1;
     Cursor cu;
     cu.b = lo;
     cu.nb = uprefix[lo + 1] - uprefix[lo];
