@@ -128,3 +128,45 @@ def test_large_batch_matches_oracle(F):
     check_close(gpu_attention(w, F, q, g, out_dtype=torch.float32), oracle_attention(w, q, o),
                 bf16_out=False, what="large batch")
     assert F.get_device_error() == 0
+
+
+# name, hq, hkv, d, bs, fmt, mode, group size
+FAR_CASES = [
+    ("gqa_token_head", 16, 2, 128, 16, E4, TH, None),
+    ("gqa_mx32", 16, 2, 128, 16, E5, MX, 32),
+    ("mla_latent", 32, 1, 576, 64, E4, TG, None),
+]
+
+
+@pytest.mark.parametrize("case", FAR_CASES, ids=[c[0] for c in FAR_CASES])
+def test_blocks_beyond_4gib_of_cache(F, case):
+    """Maximum-size addressing: the requests' blocks sit past the first 4 GiB
+    of the code cache (block ids offset by `off`), so every code, scale and
+    page address of the append and the decode needs 64-bit arithmetic.  The
+    oracle sees the same cache with the offset removed (attention is
+    invariant to where the blocks are)."""
+    import dataclasses
+    from gpu_util import check_close, gpu_attention, gpu_cache, oracle_attention, oracle_cache
+    name, hq, hkv, d, bs, fmt, mode, gs = case
+    w = W.make_shape_case(name, [1, bs + 1, 3 * bs + 5], hq, hkv, d, bs, fmt, mode,
+                          seed=2100 + FAR_CASES.index(case), group_size=gs)
+    block_bytes = hkv * bs * d
+    off = -(-(1 << 32) // block_bytes)  # first block id at or past 4 GiB
+    far = dataclasses.replace(
+        w, num_blocks=w.num_blocks + off,
+        block_tables=np.where(w.block_tables >= 0, w.block_tables + off, -1).astype(np.int32))
+    kvs = [W.request_kv(w, b) for b in range(w.batch)]
+    try:
+        g = gpu_cache(far, F, kvs)
+        o = oracle_cache(w, kvs)
+        assert np.array_equal(g[0][off:].cpu().numpy(), o[0]), "K codes"
+        assert np.array_equal(g[2][off:].cpu().numpy(), o[2]), "K scales"
+        if not w.mla:
+            assert np.array_equal(g[1][off:].cpu().numpy(), o[1]), "V codes"
+        q = W.queries(w)
+        check_close(gpu_attention(far, F, q, g, out_dtype=torch.float32),
+                    oracle_attention(w, q, o), bf16_out=False, what=f"{name} past 4 GiB")
+        assert F.get_device_error() == 0
+    finally:
+        g = None
+        torch.cuda.empty_cache()
