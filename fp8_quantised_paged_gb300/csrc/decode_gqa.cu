@@ -43,6 +43,10 @@ namespace fp8pa {
 namespace {
 
 constexpr int kMaxWarps = 8;  // warps per CTA: one per KV head of the CTA's head set
+// Internal kernel mode: static channel scales with at most 4 query heads per
+// KV head.  The high and low f16 parts of q then share one MMA: the high
+// parts in head columns 0..G-1, the low parts in columns G..2G-1.
+constexpr int kModeStaticPacked = 16;
 
 __device__ __forceinline__ int ld_i32(const int* p) { return *reinterpret_cast<const volatile int*>(p); }
 
@@ -164,6 +168,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32)
     gqa_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                      const GqaParams p) {
   constexpr bool TOKSC = (MODE == FP8PA_SCALE_TOKEN_HEAD);
+  constexpr bool PK = (MODE == kModeStaticPacked);
   constexpr bool MX = (MODE == FP8PA_SCALE_MX_BLOCK);
   constexpr bool DYN = TOKSC || MX;  // per-token scales: q stays exact in f16
   constexpr int SCB = TOKSC ? 4 : (MX ? D / 16 : 0);
@@ -313,8 +318,9 @@ __global__ void __launch_bounds__(kMaxWarps * 32)
   }
   // ---- per-segment state.  Q enters the MMA as f16; with static channel
   // scales folded in it is no longer exact in f16, so it is split into a
-  // high and a low f16 part and the contraction runs twice.
-  constexpr int QP = DYN ? 1 : 2;
+  // high and a low f16 part and the contraction runs twice (or, packed, on
+  // two sets of head columns of one MMA).
+  constexpr int QP = (DYN || PK) ? 1 : 2;
   uint32_t qb[QP][KW][2];
   float O[MT][4];
   float m0 = -FLT_MAX, m1 = -FLT_MAX, l0 = 0.f, l1 = 0.f, zs = 0.f;
@@ -331,9 +337,11 @@ __global__ void __launch_bounds__(kMaxWarps * 32)
       bool bad;
       const int v = cc.b * p.qw + qi;  // this warp's query: row of q and of out
       Lb = visible_len(p.seq_lens, v, p.qlen, p.max_blocks * BS, &bad);
-      const int h = kvh * p.G + g;
+      // packed: column g >= G carries the low part of head g - G
+      const int hc = (PK && g >= p.G) ? g - p.G : g;
+      const int h = kvh * p.G + hc;
       float qv[D / 4];
-      if (g < p.G) {
+      if (g < (PK ? 2 * p.G : p.G)) {
         const uint4* src = reinterpret_cast<const uint4*>(
             p.q + (static_cast<long>(v) * p.hq + h) * D + c * (D / 4));
 #pragma unroll
@@ -375,6 +383,16 @@ __global__ void __launch_bounds__(kMaxWarps * 32)
             r[e] = qv[4 * j + e] - __half2float(__float2half_rn(qv[4 * j + e]));
           qb[QP - 1][j][0] = pack_half2(r[0], r[1]);
           qb[QP - 1][j][1] = pack_half2(r[2], r[3]);
+        }
+        if constexpr (PK) {
+          if (g >= p.G) {
+            float r[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              r[e] = qv[4 * j + e] - __half2float(__float2half_rn(qv[4 * j + e]));
+            qb[0][j][0] = pack_half2(r[0], r[1]);
+            qb[0][j][1] = pack_half2(r[2], r[3]);
+          }
         }
       }
       zs = p.qk_scale_log2 * exp2i(eq - 14);
@@ -475,6 +493,17 @@ __global__ void __launch_bounds__(kMaxWarps * 32)
       }
 #pragma unroll
       for (int e = 0; e < 4; ++e) acc[e] += acc2[e];
+      if constexpr (PK) {
+        // add each head's low-part column (G columns to the right) into its
+        // high-part column; the columns from G on are then unused
+        if (p.G == 1) {
+          acc[0] += acc[1];
+          acc[2] += acc[3];
+        } else {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], p.G >> 1);
+        }
+      }
       const float z00 = v0 ? acc[0] * (zs * sk0) : NEG_INF;
       const float z01 = v0 ? acc[1] * (zs * sk0) : NEG_INF;
       const float z10 = v1 ? acc[2] * (zs * sk1) : NEG_INF;
@@ -700,6 +729,7 @@ SplitKernel pick3(int mode) {
   switch (mode) {
     case FP8PA_SCALE_TOKEN_HEAD: return pick4<D, BS, FMT, FP8PA_SCALE_TOKEN_HEAD>();
     case FP8PA_SCALE_MX_BLOCK: return pick4<D, BS, FMT, FP8PA_SCALE_MX_BLOCK>();
+    case kModeStaticPacked: return pick4<D, BS, FMT, kModeStaticPacked>();
     default: return pick4<D, BS, FMT, FP8PA_SCALE_CHANNEL_STATIC>();
   }
 }
@@ -722,24 +752,34 @@ SplitKernel pick(int d, int bs, int fmt, int mode) {
   return d == 128 ? pick1<128>(bs, fmt, mode) : pick1<64>(bs, fmt, mode);
 }
 
+// Kernel mode of a scale mode for G query heads per KV head.
+int kernel_mode(int mode, int G) {
+  const bool pack = mode == FP8PA_SCALE_CHANNEL_STATIC && (G == 1 || G == 2 || G == 4);
+  return pack ? kModeStaticPacked : mode;
+}
+
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 // Warps per CTA: qw query warps for each KV head of the CTA's head set, the
 // head set being the divisor of Hkv (with at most 8 warps in all) that keeps
 // the most warps resident per SM -- large pages make a warp's ring big
 // enough that 8 warps would not fit in one CTA's shared memory, or would
-// leave one CTA per SM.  Ties go to the larger head set (its warps share each
-// page's block-table entry and DRAM rows).
+// leave one CTA per SM.  Among equals, a layout with at least two CTAs per
+// SM wins (an SM holding one CTA works one page range alone, and ranges of
+// ragged requests differ in cost), then the larger head set (its warps share
+// each page's block-table entry and DRAM rows).
 constexpr int kMaxCtaSmem = 227 * 1024;
 int gqa_wpc(int hkv, int qw, const SplitKernel& k) {
-  int best = qw, best_warps = 0;
+  int best = qw, best_warps = 0, best_two = 0;
   for (int h = 1; h * qw <= kMaxWarps; ++h) {
     const int w = h * qw;
     if (hkv % h != 0 || k.smem(w) > kMaxCtaSmem) continue;
-    const int warps = w * ctas_per_sm(reinterpret_cast<const void*>(k.fn), w * 32, k.smem(w));
-    if (warps >= best_warps) {
+    const int ctas = ctas_per_sm(reinterpret_cast<const void*>(k.fn), w * 32, k.smem(w));
+    const int warps = w * ctas, two = ctas >= 2 ? 1 : 0;
+    if (warps > best_warps || (warps == best_warps && two >= best_two)) {
       best = w;
       best_warps = warps;
+      best_two = two;
     }
   }
   return best;
@@ -761,7 +801,7 @@ int decode_workers(const DecodeShape& s, int fmt, int mode, int device) {
     return (ranges < 1 ? 1 : ranges) * H;
   }
   if (g_decode_workers_override > 0) return g_decode_workers_override;
-  const SplitKernel k = pick(s.d, s.bs, fmt, mode);
+  const SplitKernel k = pick(s.d, s.bs, fmt, kernel_mode(mode, s.hq / s.hkv));
   const int qw = gqa_qw(s);
   const int wpc = gqa_wpc(s.hkv, qw, k), hsets = s.hkv / (wpc / qw);
   const int per_sm = ctas_per_sm(reinterpret_cast<const void*>(k.fn), wpc * 32, k.smem(wpc));
@@ -787,7 +827,7 @@ size_t decode_workspace_bytes(const DecodeShape& s) {
 
 cudaError_t launch_decode_gqa(const DecodeShape& s, const DecodeArgs& a, cudaStream_t stream) {
   const int G = s.hq / s.hkv;
-  const SplitKernel k = pick(s.d, s.bs, a.fmt, a.mode);
+  const SplitKernel k = pick(s.d, s.bs, a.fmt, kernel_mode(a.mode, G));
   const int qw = gqa_qw(s);
   const int bp = s.batch / qw;  // planned requests
   const int wpc = gqa_wpc(s.hkv, qw, k), hsets = s.hkv / (wpc / qw);
