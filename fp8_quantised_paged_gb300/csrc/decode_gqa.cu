@@ -173,15 +173,18 @@ __global__ void __launch_bounds__(kMaxWarps * 32)
   constexpr bool DYN = TOKSC || MX;  // per-token scales: q stays exact in f16
   constexpr int SCB = TOKSC ? 4 : (MX ? D / 16 : 0);
   constexpr int XS = MxTable<D>::kStride;
-  using SM = GqaSmem<D, BS, NST, SCB, MX ? MxTable<D>::kWords : 0>;
-  constexpr int PAGE = SM::kPage;
-  constexpr int TILES = BS / 16;
+  // A stage holds one 16-token slice of a page (SUB slices per page), so
+  // large pages do not make a warp's ring large.
+  constexpr int SUB = BS / 16;
+  using SM = GqaSmem<D, 16, NST, SCB, MX ? MxTable<D>::kWords : 0>;
+  constexpr int PAGE = SM::kPage;  // bytes of one slice of one tensor
+  constexpr int TILES = 1;
   constexpr int KW = D / 16;   // K words per row per thread = k-steps
   constexpr int KCH = D / 64;  // 16-byte K chunks per row per thread
   constexpr int VW = D / 32;   // V words per token per thread
   constexpr int MT = D / 16;   // dv tiles of 16
   const int nbx = MX ? D / p.gs : 0;  // exponent bytes per token (MX)
-  const uint32_t TX = 2 * PAGE + (TOKSC ? 2 * BS * 4 : (MX ? 2 * BS * nbx : 0));
+  const uint32_t TX = 2 * PAGE + (TOKSC ? 2 * 16 * 4 : (MX ? 2 * 16 * nbx : 0));
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -190,7 +193,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32)
   const int g = lane >> 2, c = lane & 3;
   const int W = blockDim.x >> 5;  // warps in this CTA
   uint8_t* pages = smem + warp * (NST * 2 * PAGE);
-  uint8_t* sclb = smem + SM::pages(W) + warp * (NST * 2 * BS * SCB);
+  uint8_t* sclb = smem + SM::pages(W) + warp * (NST * 2 * 16 * SCB);
   float* scl = reinterpret_cast<float*>(sclb);
   // P^T for the PV MMA as two f16 planes (hi + lo carry ~22 significant bits)
   uint16_t* ps = reinterpret_cast<uint16_t*>(smem + SM::pages(W) + SM::scales(W)) + warp * 256;
@@ -262,26 +265,27 @@ __global__ void __launch_bounds__(kMaxWarps * 32)
     }
   };
   auto block_of = [&](const Cursor& cu) { return __ldg(p.block_tables + cu.brow + cu.j); };
-  // Issue the copies of one page into stage s (lane 0 only acts).
-  auto issue = [&](const Cursor& cu, int blk, int s) {
+  // Issue the copies of slice `sub` of one page into stage s (lane 0 only
+  // acts).
+  auto issue = [&](int blk, int s, int sub) {
     if (lane == 0) {
       const bool ok = blk >= 0 && blk < p.num_blocks;
       okf[s] = ok ? 1 : 0;
       if (ok) {
-        const int row = (blk * p.hkv + kvh) * BS;
+        const int row = (blk * p.hkv + kvh) * BS + 16 * sub;
         mbar_arrive_expect_tx(&bars[s], TX);
         tma_load_2d(pages + s * 2 * PAGE, &tmk, 0, row, &bars[s]);
         tma_load_2d(pages + s * 2 * PAGE + PAGE, &tmv, 0, row, &bars[s]);
         if constexpr (TOKSC) {
-          bulk_load(scl + s * 2 * BS, p.k_scale + row, BS * 4, &bars[s]);
-          bulk_load(scl + s * 2 * BS + BS, p.v_scale + row, BS * 4, &bars[s]);
+          bulk_load(scl + s * 2 * 16, p.k_scale + row, 16 * 4, &bars[s]);
+          bulk_load(scl + s * 2 * 16 + 16, p.v_scale + row, 16 * 4, &bars[s]);
         } else if constexpr (MX) {
           const uint8_t* ke = reinterpret_cast<const uint8_t*>(p.k_scale);
           const uint8_t* ve = reinterpret_cast<const uint8_t*>(p.v_scale);
-          bulk_load(sclb + s * 2 * BS * SCB, ke + static_cast<long>(row) * nbx, BS * nbx,
+          bulk_load(sclb + s * 2 * 16 * SCB, ke + static_cast<long>(row) * nbx, 16 * nbx,
                     &bars[s]);
-          bulk_load(sclb + s * 2 * BS * SCB + BS * SCB, ve + static_cast<long>(row) * nbx,
-                    BS * nbx, &bars[s]);
+          bulk_load(sclb + s * 2 * 16 * SCB + 16 * SCB, ve + static_cast<long>(row) * nbx,
+                    16 * nbx, &bars[s]);
         }
       } else {
         raise_error(p.err, FP8PA_DEVERR_BLOCK_RANGE);
@@ -290,9 +294,9 @@ __global__ void __launch_bounds__(kMaxWarps * 32)
     }
   };
 
-  // Per-thread byte offsets inside a page: the swizzle phase of every row a
+  // Per-thread byte offsets inside a slice: the swizzle phase of every row a
   // thread touches depends only on its lane, so they are fixed for the
-  // whole kernel (tile tt adds tt * 16 rows).
+  // whole kernel.
   uint32_t koff[2][KCH], voff[4];
 #pragma unroll
   for (int rr = 0; rr < 2; ++rr)
@@ -304,16 +308,19 @@ __global__ void __launch_bounds__(kMaxWarps * 32)
     voff[u] = D == 128 ? swz<D>(tau, g) : swz<D>(tau, g >> 1) + 8 * (g & 1);
   }
 
+  const int n_sub = n_units * SUB;  // slices of the range, in page order
   Cursor cc = locate(u0);
   Cursor pc = cc;
-  int ip = 0;  // units issued
+  int ip = 0;  // slices issued
   int pblk = block_of(pc);
   {
-    const int npro = min(NST, n_units);
+    const int npro = min(NST, n_sub);
     for (; ip < npro; ++ip) {
-      issue(pc, pblk, ip);
-      advance(pc);
-      if (ip + 1 < n_units) pblk = block_of(pc);
+      issue(pblk, ip, ip % SUB);
+      if (ip % SUB == SUB - 1) {
+        advance(pc);
+        if (ip + 1 < n_sub) pblk = block_of(pc);
+      }
     }
   }
   // ---- per-segment state.  Q enters the MMA as f16; with static channel
@@ -329,10 +336,11 @@ __global__ void __launch_bounds__(kMaxWarps * 32)
   bool abandoned = false;
   int i = 0;
 
-  for (; i < n_units; ++i) {
+  for (; i < n_sub; ++i) {
     const int s = i % NST;
     const uint32_t par = static_cast<uint32_t>((i / NST) & 1);
-    if (i == 0 || cc.j == 0) {
+    const int sub = i % SUB;  // slice of page cc.j
+    if (sub == 0 && (i == 0 || cc.j == 0)) {
       // ---- new segment: load q for the G heads of (b, kv head)
       bool bad;
       const int v = cc.b * p.qw + qi;  // this warp's query: row of q and of out
@@ -409,13 +417,13 @@ __global__ void __launch_bounds__(kMaxWarps * 32)
       abandoned = true;
       break;
     }
-    const int valid = okf[s] ? min(BS, Lb - cc.j * BS) : 0;
+    const int valid = okf[s] ? min(16, Lb - cc.j * BS - 16 * sub) : 0;
     const uint32_t kbase = smem_u32(pages + s * 2 * PAGE);
     const uint32_t vbase = kbase + PAGE;
-    const float* sks = scl + s * 2 * BS;
-    const float* svs = sks + BS;
-    const uint8_t* kex = sclb + s * 2 * BS * SCB;  // MX: exponent bytes of K, V
-    const uint8_t* vex = kex + BS * SCB;
+    const float* sks = scl + s * 2 * 16;
+    const float* svs = sks + 16;
+    const uint8_t* kex = sclb + s * 2 * 16 * SCB;  // MX: exponent bytes of K, V
+    const uint8_t* vex = kex + 16 * SCB;
 
 #pragma unroll
     for (int tt = 0; tt < TILES; ++tt) {
@@ -638,16 +646,19 @@ __global__ void __launch_bounds__(kMaxWarps * 32)
     }
     __syncwarp();
 
-    // ---- refill this stage with the next page of the range
-    if (ip < n_units) {
-      issue(pc, pblk, ip % NST);
+    // ---- refill this stage with the next slice of the range
+    if (ip < n_sub) {
+      issue(pblk, ip % NST, ip % SUB);
+      const bool page_done = ip % SUB == SUB - 1;
       ++ip;
-      advance(pc);
-      if (ip < n_units) pblk = block_of(pc);
+      if (page_done) {
+        advance(pc);
+        if (ip < n_sub) pblk = block_of(pc);
+      }
     }
 
     // ---- segment end: write the partial (m, l, o) of this warp's piece
-    if (i == n_units - 1 || cc.j == cc.nb - 1) {
+    if (sub == SUB - 1 && (i == n_sub - 1 || cc.j == cc.nb - 1)) {
 #pragma unroll
       for (int o = 4; o < 32; o <<= 1) {
         l0 += __shfl_xor_sync(0xffffffffu, l0, o);
@@ -683,7 +694,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32)
         }
       }
     }
-    advance(cc);
+    if (sub == SUB - 1) advance(cc);
   }
 
   if (abandoned) {
@@ -696,13 +707,15 @@ __global__ void __launch_bounds__(kMaxWarps * 32)
 }
 
 // ---------------------------------------------------------------- host side
-// Stages of one warp's ring: 8 KB of K+V pages (2 stages at head_dim 128,
-// block 16).  Registers hold 16 warps per SM; one page in flight per warp
-// while it computes on the other already covers the memory latency (a third
-// stage measured 1 % slower, and 24 warps with 2 stages spill registers).
-template <int D, int BS>
+// Stages of one warp's ring: 8 KB of K+V slices (2 stages at head_dim 128).
+// A stage is one 16-token slice whatever the block size, so a warp's ring
+// (and the warps resident per SM) does not shrink with larger blocks.
+// Registers hold 16 warps per SM; one slice in flight per warp while it
+// computes on the other already covers the memory latency (a third stage
+// measured 1 % slower, and 24 warps with 2 stages spill registers).
+template <int D>
 constexpr int stages_for() {
-  constexpr int stage = 2 * BS * D;
+  constexpr int stage = 2 * 16 * D;  // one 16-token slice of K and of V
   constexpr int n = 8192 / stage;
   return n < 2 ? 2 : (n > 8 ? 8 : n);
 }
@@ -717,10 +730,10 @@ struct SplitKernel {
 
 template <int D, int BS, int FMT, int MODE>
 SplitKernel pick4() {
-  constexpr int NST = stages_for<D, BS>();
+  constexpr int NST = stages_for<D>();
   constexpr bool MX = MODE == FP8PA_SCALE_MX_BLOCK;
   constexpr int SCB = MODE == FP8PA_SCALE_TOKEN_HEAD ? 4 : (MX ? D / 16 : 0);
-  using SM = GqaSmem<D, BS, NST, SCB, MX ? MxTable<D>::kWords : 0>;
+  using SM = GqaSmem<D, 16, NST, SCB, MX ? MxTable<D>::kWords : 0>;
   return {gqa_split_kernel<D, BS, FMT, MODE, NST>, SM::bytes(1) - 1024};
 }
 
@@ -839,8 +852,8 @@ cudaError_t launch_decode_gqa(const DecodeShape& s, const DecodeArgs& a, cudaStr
   const uint64_t rows = static_cast<uint64_t>(a.num_blocks) * s.hkv * s.bs;
   const CUtensorMapSwizzle swz =
       s.d == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
-  if (!encode_tensor_map_2d_u8(&tmk, a.k_cache, s.d, rows, s.d, s.bs, swz) ||
-      !encode_tensor_map_2d_u8(&tmv, a.v_cache, s.d, rows, s.d, s.bs, swz))
+  if (!encode_tensor_map_2d_u8(&tmk, a.k_cache, s.d, rows, s.d, 16, swz) ||
+      !encode_tensor_map_2d_u8(&tmv, a.v_cache, s.d, rows, s.d, 16, swz))
     return cudaErrorInvalidValue;
 
   char* ws = static_cast<char*>(a.workspace);
