@@ -2,7 +2,9 @@
 workloads: block sizes 16/32/64, head_dim 64/128, GQA group sizes 1, 2, 3, 4
 and 8, KV-head counts that are not a power of two or need several head sets
 per CTA, both formats with both GQA scale modes, KV-head counts up to 24,
-and the latent layout with 32 and 64 query heads.  Every output is compared with the FP64 oracle;
+and the latent layout with 32 and 64 query heads.  Static scales with 1, 2
+or 4 query heads per KV head run the packed kernel (q's high and low parts
+in one MMA), at head_dim 64 and 128.  Every output is compared with the FP64 oracle;
 lengths include 1, block_size - 1, block_size, block_size + 1 and several
 pages with a ragged tail."""
 import numpy as np
@@ -28,6 +30,8 @@ CASES = [
     ("g1_hkv13_d128_bs64_e5m2_static", 13, 13, 128, 64, E5, CS),
     ("mla_32_heads_e4m3", 32, 1, 576, 64, E4, TG),
     ("mla_64_heads_e5m2", 64, 1, 576, 64, E5, TG),
+    ("g4_hkv2_d64_bs16_e4m3_static", 8, 2, 64, 16, E4, CS),
+    ("g1_hkv4_d64_bs64_e5m2_static", 4, 4, 64, 64, E5, CS),
 ]
 
 
@@ -63,7 +67,7 @@ def test_shape_matches_oracle(F, case):
     assert F.get_device_error() == 0
 
 
-@pytest.mark.parametrize("case", [CASES[1], CASES[2], CASES[8]], ids=lambda c: c[0])
+@pytest.mark.parametrize("case", [CASES[1], CASES[2], CASES[8], CASES[10]], ids=lambda c: c[0])
 def test_shape_multiquery_matches_oracle(F, case):
     from gpu_util import check_close, gpu_cache, gpu_multiquery, oracle_cache, oracle_multiquery
     name, hq, hkv, d, bs, fmt, mode = case
