@@ -119,15 +119,16 @@ __device__ __forceinline__ ExpRow exp_row(const uint8_t* base, int t, int nb) {
   return r;
 }
 
-// Shared-memory layout for `w` warps (each with its own NST-stage ring);
-// SCB = scale bytes per token per tensor in the ring (4 for one fp32 scale,
-// D/16 for the largest count of E8M0 block exponents, 0 for static scales);
-// XTW = words of the per-warp MX factor table (0 outside MX block mode).
-template <int D, int BS, int NST, int SCB, int XTW>
+// Shared-memory layout for `w` warps (each with its own NST-stage ring of
+// 16-token slices of K and V); SCB = scale bytes per token per tensor in the
+// ring (4 for one fp32 scale, D/16 for the largest count of E8M0 block
+// exponents, 0 for static scales); XTW = words of the per-warp MX factor
+// table (0 outside MX block mode).
+template <int D, int NST, int SCB, int XTW>
 struct GqaSmem {
-  static constexpr int kPage = BS * D;
+  static constexpr int kPage = 16 * D;  // one slice of one tensor
   __host__ __device__ static constexpr int pages(int w) { return w * NST * 2 * kPage; }
-  __host__ __device__ static constexpr int scales(int w) { return w * NST * 2 * BS * SCB; }
+  __host__ __device__ static constexpr int scales(int w) { return w * NST * 2 * 16 * SCB; }
   __host__ __device__ static constexpr int ps(int w) { return w * 512; }
   __host__ __device__ static constexpr int bars(int w) { return w * NST * 8; }
   __host__ __device__ static constexpr int oks(int w) { return w * NST * 4; }
@@ -176,9 +177,8 @@ __global__ void __launch_bounds__(kMaxWarps * 32)
   // A stage holds one 16-token slice of a page (SUB slices per page), so
   // large pages do not make a warp's ring large.
   constexpr int SUB = BS / 16;
-  using SM = GqaSmem<D, 16, NST, SCB, MX ? MxTable<D>::kWords : 0>;
+  using SM = GqaSmem<D, NST, SCB, MX ? MxTable<D>::kWords : 0>;
   constexpr int PAGE = SM::kPage;  // bytes of one slice of one tensor
-  constexpr int TILES = 1;
   constexpr int KW = D / 16;   // K words per row per thread = k-steps
   constexpr int KCH = D / 64;  // 16-byte K chunks per row per thread
   constexpr int VW = D / 32;   // V words per token per thread
@@ -425,10 +425,8 @@ __global__ void __launch_bounds__(kMaxWarps * 32)
     const uint8_t* kex = sclb + s * 2 * 16 * SCB;  // MX: exponent bytes of K, V
     const uint8_t* vex = kex + 16 * SCB;
 
-#pragma unroll
-    for (int tt = 0; tt < TILES; ++tt) {
-      const int r0 = tt * 16;
-      if (r0 >= valid) break;
+    if (valid > 0) {  // the slice holds tokens of the request (one 16-token tile)
+      constexpr int r0 = 0;
       const int tv = valid - r0;
       const bool full = tv >= 16;  // warp-uniform
       // ---- S^T = K . Q^T : rows = tokens (g, g+8), cols = heads (2c, 2c+1)
@@ -733,7 +731,7 @@ SplitKernel pick4() {
   constexpr int NST = stages_for<D>();
   constexpr bool MX = MODE == FP8PA_SCALE_MX_BLOCK;
   constexpr int SCB = MODE == FP8PA_SCALE_TOKEN_HEAD ? 4 : (MX ? D / 16 : 0);
-  using SM = GqaSmem<D, 16, NST, SCB, MX ? MxTable<D>::kWords : 0>;
+  using SM = GqaSmem<D, NST, SCB, MX ? MxTable<D>::kWords : 0>;
   return {gqa_split_kernel<D, BS, FMT, MODE, NST>, SM::bytes(1) - 1024};
 }
 
