@@ -34,7 +34,7 @@ from dataclasses import dataclass, field
 
 import numpy as np
 
-E4M3, E5M2 = 0, 1
+E4M3, E5M2, INT8 = 0, 1, 2
 SCALE_TOKEN_HEAD, SCALE_CHANNEL_STATIC, SCALE_TOKEN_GROUP, SCALE_MX_BLOCK = 0, 1, 2, 3
 
 
@@ -82,7 +82,7 @@ class Workload:
         return {"workload": self.name, "batch": self.batch, "n_q_heads": self.n_q_heads,
                 "n_kv_heads": self.n_kv_heads, "head_dim": self.head_dim,
                 "head_dim_v": self.head_dim_v, "block_size": self.block_size,
-                "kv_fmt": "e4m3" if self.fmt == E4M3 else "e5m2",
+                "kv_fmt": {E4M3: "e4m3", E5M2: "e5m2", INT8: "int8"}[self.fmt],
                 "scale_mode": ["token_head", "channel_static", "token_group",
                                f"mx_block_{self.group_size}"][self.scale_mode],
                 "kv_tokens": self.total_tokens, "num_blocks": self.num_blocks}

@@ -22,7 +22,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "fp8pa_oracle.c")
 _LIB_PATH = os.path.join(_HERE, "liboracle.so")
 
-E4M3, E5M2 = 0, 1
+E4M3, E5M2, INT8 = 0, 1, 2  # INT8: the symmetric alternate codec (FMAX 127)
 SCALE_TOKEN_HEAD, SCALE_CHANNEL_STATIC, SCALE_TOKEN_GROUP, SCALE_MX_BLOCK = 0, 1, 2, 3
 
 _lib = None
@@ -122,6 +122,8 @@ def kv_append_quant(k, v, slot_mapping, fmt, scale_mode, group_size, k_cache, v_
                     k_scale, v_scale, block_size) -> int:
     """In-place append into numpy caches; k/v are bf16 bit patterns (uint16)
     of shape [num_tokens, Hkv, D].  Returns the count of out-of-range slots."""
+    if fmt == INT8 and scale_mode == SCALE_MX_BLOCK:
+        raise ValueError("the power-of-two block mode is defined for FP8 codes only")
     k = _c(k, np.uint16)
     v = _c(v, np.uint16)
     sm = _c(slot_mapping, np.int32)

@@ -42,6 +42,15 @@
  * exponent of the format's largest normal (8 for E4M3, 15 for E5M2), held in
  * [-127, 127] (an all-zero block takes e = -127); codes are the FP8 rounding
  * of x / X, saturated.
+ *
+ * The INT8 codec is the alternate KV format the pages mention only as a
+ * serving option ("--kv_cache_dtype int8", hotelren.com/news/5166672, the
+ * section on inference-engine settings), with no scale or rounding rule.
+ * Reading: symmetric codes with FMAX = 127 in place of the FP8 maximum, so
+ * the scale is fp32 absmax / 127 (IEEE division, clamped at 1e-12) and the
+ * code is x / scale rounded to the nearest integer, ties to even, clamped
+ * to [-127, 127], stored as a two's complement byte; a code's value is
+ * its integer.  The power-of-two block mode is defined for FP8 only.
  */
 #include <math.h>
 #include <stdint.h>
@@ -53,6 +62,7 @@
 
 #define OR_E4M3 0
 #define OR_E5M2 1
+#define OR_INT8 2
 
 #define OR_SCALE_TOKEN_HEAD 0
 #define OR_SCALE_CHANNEL_STATIC 1
@@ -63,8 +73,11 @@
 /* FP8 formats: [P2] sec. 1.1, [P4] sec. 1.1, [P1] sec. 2.1.           */
 /* ------------------------------------------------------------------ */
 
-/* Largest finite magnitude: 448 for E4M3, 57344 for E5M2 ([P4] sec. 1.1). */
-double or_fp8_max(int fmt) { return fmt == OR_E4M3 ? 448.0 : 57344.0; }
+/* Largest finite magnitude: 448 for E4M3, 57344 for E5M2 ([P4] sec. 1.1),
+ * 127 for the symmetric INT8 codec. */
+double or_fp8_max(int fmt) {
+  return fmt == OR_E4M3 ? 448.0 : (fmt == OR_E5M2 ? 57344.0 : 127.0);
+}
 
 /* Value of an FP8 code, read field by field.
  * E4M3: 1 sign, 4 exponent (bias 7), 3 mantissa bits; exponent field 0 is
@@ -72,6 +85,7 @@ double or_fp8_max(int fmt) { return fmt == OR_E4M3 ? 448.0 : 57344.0; }
  * E5M2: 1 sign, 5 exponent (bias 15), 2 mantissa bits; exponent field 0 is
  *       subnormal (m/4)*2^-14; exponent field 31 is inf (m = 0) or NaN. */
 double or_fp8_decode(uint8_t code, int fmt) {
+  if (fmt == OR_INT8) return (double)(int8_t)code;
   int neg = (code >> 7) & 1;
   double mag;
   if (fmt == OR_E4M3) {
@@ -95,10 +109,25 @@ double or_fp8_decode(uint8_t code, int fmt) {
   return neg ? -mag : mag;
 }
 
+/* fp32 -> INT8 code: the nearest integer (from the floor and the remainder),
+ * ties to the even one, clamped to [-127, 127]; NaN -> 0. */
+static uint8_t or_int8_encode(float x) {
+  if (isnan(x)) return 0;
+  const double xd = (double)x;
+  if (xd >= 127.0) return 127;
+  if (xd <= -127.0) return (uint8_t)(int8_t)-127;
+  const double f = floor(xd);
+  const double r = xd - f; /* exact: |xd| < 2^7 */
+  long n = (long)f;
+  if (r > 0.5 || (r == 0.5 && (n & 1l))) n += 1;
+  return (uint8_t)(int8_t)n;
+}
+
 /* fp32 -> FP8 code by integer manipulation of the fp32 bit pattern:
  * round to nearest, ties to even, saturate finite overflow (and +-inf) to
- * +-max, keep the sign of zero, NaN -> 0x7F. */
+ * +-max, keep the sign of zero, NaN -> 0x7F.  (INT8: or_int8_encode.) */
 uint8_t or_fp8_encode(float x, int fmt) {
+  if (fmt == OR_INT8) return or_int8_encode(x);
   uint32_t bits;
   memcpy(&bits, &x, sizeof bits);
   const uint32_t sign = (bits >> 31) ? 0x80u : 0x00u;
@@ -144,6 +173,23 @@ uint8_t or_fp8_encode(float x, int fmt) {
  * of the same sign for the nearest value in FP64; ties go to the code with
  * an even mantissa (an even code number); beyond max it saturates. */
 uint8_t or_fp8_encode_bruteforce(float x, int fmt) {
+  if (fmt == OR_INT8) {
+    /* beyond the range it clamps; inside, scan every integer in
+     * [-127, 127] for the nearest, ties to the even one */
+    if (isnan(x)) return 0;
+    if ((double)x >= 127.0) return 127;
+    if ((double)x <= -127.0) return (uint8_t)(int8_t)-127;
+    int best = 0;
+    double bestd = INFINITY;
+    for (int c = -127; c <= 127; ++c) {
+      const double d = fabs((double)c - (double)x);
+      if (d < bestd || (d == bestd && (c & 1) == 0)) {
+        bestd = d;
+        best = c;
+      }
+    }
+    return (uint8_t)(int8_t)best;
+  }
   if (isnan(x)) return 0x7F;
   const double xd = (double)x;
   const int neg = signbit(x) ? 1 : 0;

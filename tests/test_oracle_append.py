@@ -57,6 +57,7 @@ def test_scale_is_absmax_over_fmax():
     x = _bf16([1.0, -2.0, 0.5, 0.0])
     assert oracle.absmax_scale(x, oracle.E4M3) == np.float32(2.0) / np.float32(448.0)
     assert oracle.absmax_scale(x, oracle.E5M2) == np.float32(2.0) / np.float32(57344.0)
+    assert oracle.absmax_scale(x, oracle.INT8) == np.float32(2.0) / np.float32(127.0)
     assert oracle.absmax_scale(_bf16([0.0, -0.0]), oracle.E4M3) == np.float32(1e-12)
 
 

@@ -12,7 +12,8 @@ import torch
 import oracle
 from fp8_quantised_paged_gb300 import workloads as W
 
-TORCH_T = {oracle.E4M3: torch.float8_e4m3fn, oracle.E5M2: torch.float8_e5m2}
+TORCH_T = {oracle.E4M3: torch.float8_e4m3fn, oracle.E5M2: torch.float8_e5m2,
+           oracle.INT8: torch.int8}
 
 
 def build_cache(w):
@@ -40,7 +41,8 @@ def build_cache(w):
 
 
 def dequant_request(w, cache, scale, b):
-    """[L, Hkv, D] float64 through torch's float8 decode (not the oracle's)."""
+    """[L, Hkv, D] float64 through torch's float8 (or int8) decode, not the
+    oracle's."""
     L = int(w.seq_lens[b])
     t = np.arange(L)
     blk = w.block_tables[b, t // w.block_size]
@@ -245,6 +247,23 @@ def test_mx_block_attention_matches_torch_sdpa(fmt, gs):
                           seed=31, group_size=gs)
     kc, vc, ks, vs = build_cache(w)
     assert ks.dtype == np.uint8 and ks.shape[-1] == 128 // gs
+    q = W.queries(w)
+    got = run_oracle(w, q, kc, vc, ks, vs)
+    ref = sdpa_reference(w, q, kc, vc, ks, vs)
+    assert np.allclose(got, ref, rtol=1e-10, atol=1e-10), np.abs(got - ref).max()
+
+
+@pytest.mark.parametrize("mode,hq,hkv,d,bs", [(W.SCALE_TOKEN_HEAD, 16, 4, 128, 16),
+                                             (W.SCALE_CHANNEL_STATIC, 8, 2, 64, 32),
+                                             (W.SCALE_TOKEN_GROUP, 32, 1, 576, 64)])
+def test_int8_attention_matches_torch_sdpa(mode, hq, hkv, d, bs):
+    """INT8 caches (token-head, static channel and per-latent-group scales):
+    attention over the dequantised cache, integer code * scale, against
+    float64 SDPA."""
+    w = W.make_shape_case("int8", [1, bs - 1, bs, bs + 1, 3 * bs + 5], hq, hkv, d, bs, W.INT8,
+                          mode, seed=41)
+    kc, vc, ks, vs = build_cache(w)
+    assert kc.view(np.int8).min() >= -127
     q = W.queries(w)
     got = run_oracle(w, q, kc, vc, ks, vs)
     ref = sdpa_reference(w, q, kc, vc, ks, vs)
