@@ -52,6 +52,8 @@ def parse_args():
     ap.add_argument("--mx-block", type=int, default=0, choices=[0, 16, 32],
                     help="store the GQA workload's cache in the MX block-scaled mode "
                          "(one E8M0 exponent per block of this many dims)")
+    ap.add_argument("--kv-fmt", choices=["e4m3", "e5m2", "int8"], default=None,
+                    help="store the workload's cache in this code format instead of its own")
     ap.add_argument("--q-len", type=int, default=1,
                     help="queries per request: a causal chunk (the last q_len tokens of each "
                          "request are appended, then attend); 1 is plain decode")
@@ -95,9 +97,17 @@ def accounting(w: W.Workload, b_sel=None, q_len: int = 1) -> dict:
 
 
 def bench_workload(args) -> W.Workload:
-    """The named full-size workload, optionally with an MX block-scaled cache."""
+    """The named full-size workload, optionally with an MX block-scaled cache
+    or another code format."""
     w = W.make_workload(args.workload, "full")
+    if args.kv_fmt is not None:
+        fmt = {"e4m3": W.E4M3, "e5m2": W.E5M2, "int8": W.INT8}[args.kv_fmt]
+        if fmt != w.fmt:
+            w.fmt = fmt
+            w.name = f"{w.name}_{args.kv_fmt}"
     if args.mx_block:
+        if w.fmt == W.INT8:
+            raise SystemExit("--mx-block needs FP8 codes")
         if w.mla:
             raise SystemExit("--mx-block applies to the grouped-query workloads")
         w.scale_mode, w.group_size = W.SCALE_MX_BLOCK, args.mx_block
@@ -512,9 +522,10 @@ def run_gpu(args, rank, world, local_rank):
             "pct_of_peak_hbm": 100.0 * value / world / pk["hbm_gbs"],
             "kv_tokens_per_s": world * acc["kv_tokens"] / (ms_step * 1e-3),
             "config": dict(w.describe(), parallelism=f"replicas x{world}",
-                           kv_dtype="e4m3" if w.fmt == W.E4M3 else "e5m2",
-                           compute="fp8 codes -> exact f16, warp MMA (m16n8k16), f32 accumulate "
-                                   "and softmax",
+                           kv_dtype={W.E4M3: "e4m3", W.E5M2: "e5m2", W.INT8: "int8"}[w.fmt],
+                           compute=("int8" if w.fmt == W.INT8 else "fp8")
+                           + " codes -> exact f16, warp MMA (m16n8k16), f32 accumulate "
+                             "and softmax",
                            l2="no flush: every step reads the whole cache, larger than L2",
                            step=f"fp8pa_decode_step: append ({ql} token(s)/request) and plan, "
                                 "split, merge",

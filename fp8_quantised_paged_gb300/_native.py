@@ -17,7 +17,7 @@ OK = 0
 ERR_NULL_POINTER, ERR_BAD_ENUM, ERR_BAD_SHAPE, ERR_UNSUPPORTED = -1, -2, -3, -4
 ERR_WORKSPACE, ERR_ALIGNMENT, ERR_CUDA = -5, -6, -7
 DEVERR_SLOT_RANGE, DEVERR_BLOCK_RANGE, DEVERR_SEQ_LEN, DEVERR_TIMEOUT = 1, 2, 4, 8
-E4M3, E5M2 = 0, 1
+E4M3, E5M2, INT8 = 0, 1, 2
 SCALE_TOKEN_HEAD, SCALE_CHANNEL_STATIC, SCALE_TOKEN_GROUP, SCALE_MX_BLOCK = 0, 1, 2, 3
 OUT_BF16, OUT_F32 = 0, 1
 

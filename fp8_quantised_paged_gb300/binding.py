@@ -3,7 +3,8 @@
 Two calls, both hand-written CUDA kernels behind a C ABI (``include/fp8pa.h``):
 
 * :func:`kv_append_quant` -- absmax-scale each new token's K/V rows, round
-  them to E4M3 or E5M2 and scatter codes and scales into the paged cache.
+  them to E4M3 or E5M2 (or symmetric INT8 codes) and scatter codes and
+  scales into the paged cache.
 * :func:`paged_decode_attention` -- grouped-query (or shared-latent MLA)
   attention of one query token per request over its paged FP8 cache, split
   across the GPU and merged.
@@ -19,13 +20,13 @@ import ctypes
 import torch
 
 from . import _native as N
-from ._native import (E4M3, E5M2, OUT_BF16, OUT_F32, SCALE_CHANNEL_STATIC, SCALE_MX_BLOCK,
+from ._native import (E4M3, E5M2, INT8, OUT_BF16, OUT_F32, SCALE_CHANNEL_STATIC, SCALE_MX_BLOCK,
                       SCALE_TOKEN_GROUP, SCALE_TOKEN_HEAD, Fp8paError)
 
 __all__ = ["kv_append_quant", "kv_channel_scales", "kv_channel_absmax_update",
            "kv_scales_from_absmax", "paged_decode_attention", "paged_multiquery_attention",
            "decode_step", "decode_workspace_bytes", "get_device_error", "set_decode_workers",
-           "version", "E4M3", "E5M2", "SCALE_TOKEN_HEAD", "SCALE_CHANNEL_STATIC",
+           "version", "E4M3", "E5M2", "INT8", "SCALE_TOKEN_HEAD", "SCALE_CHANNEL_STATIC",
            "SCALE_TOKEN_GROUP", "SCALE_MX_BLOCK", "OUT_BF16", "OUT_F32", "Fp8paError"]
 
 

@@ -168,7 +168,7 @@ DecodePath decode_path(int batch, int hq, int hkv, int d, int dv, int bs, int ma
   s.max_blocks = max_blocks;
   s.mla = 0;
   s.qlen = 1;
-  if ((fmt != FP8PA_E4M3 && fmt != FP8PA_E5M2) ||
+  if ((fmt != FP8PA_E4M3 && fmt != FP8PA_E5M2 && fmt != FP8PA_INT8) ||
       (mode != FP8PA_SCALE_TOKEN_HEAD && mode != FP8PA_SCALE_CHANNEL_STATIC &&
        mode != FP8PA_SCALE_TOKEN_GROUP && mode != FP8PA_SCALE_MX_BLOCK) ||
       (out_dtype != FP8PA_OUT_BF16 && out_dtype != FP8PA_OUT_F32)) {
@@ -195,7 +195,7 @@ DecodePath decode_path(int batch, int hq, int hkv, int d, int dv, int bs, int ma
   }
   if ((d != 64 && d != 128) || dv != d || (bs != 16 && bs != 32 && bs != 64) || hq / hkv > 8 ||
       mode == FP8PA_SCALE_TOKEN_GROUP ||
-      (mode == FP8PA_SCALE_MX_BLOCK && gs != 16 && gs != 32))
+      (mode == FP8PA_SCALE_MX_BLOCK && ((gs != 16 && gs != 32) || fmt == FP8PA_INT8)))
     r.status = FP8PA_ERR_UNSUPPORTED;
   return r;
 }
@@ -285,7 +285,7 @@ int append_prepare(const void* k, const void* v, const int32_t* slot_mapping, in
                    int num_blocks, int block_size, AppendArgs* a) {
   if (num_tokens < 0 || n_kv_heads <= 0 || head_dim <= 0 || num_blocks <= 0 || block_size <= 0)
     return FP8PA_ERR_BAD_SHAPE;
-  if ((fmt != FP8PA_E4M3 && fmt != FP8PA_E5M2) ||
+  if ((fmt != FP8PA_E4M3 && fmt != FP8PA_E5M2 && fmt != FP8PA_INT8) ||
       (scale_mode != FP8PA_SCALE_TOKEN_HEAD && scale_mode != FP8PA_SCALE_CHANNEL_STATIC &&
        scale_mode != FP8PA_SCALE_TOKEN_GROUP && scale_mode != FP8PA_SCALE_MX_BLOCK))
     return FP8PA_ERR_BAD_ENUM;
@@ -294,7 +294,7 @@ int append_prepare(const void* k, const void* v, const int32_t* slot_mapping, in
       (!pow2(group_size) || group_size < 16 || group_size > 256 || head_dim % group_size != 0))
     return FP8PA_ERR_UNSUPPORTED;
   if (scale_mode == FP8PA_SCALE_MX_BLOCK &&
-      ((group_size != 16 && group_size != 32) || head_dim % group_size != 0))
+      ((group_size != 16 && group_size != 32) || head_dim % group_size != 0 || fmt == FP8PA_INT8))
     return FP8PA_ERR_UNSUPPORTED;
   if (static_cast<long long>(num_blocks) * block_size >= (1ll << 31)) return FP8PA_ERR_UNSUPPORTED;
   *a = AppendArgs{};
@@ -373,7 +373,7 @@ int fp8pa_kv_append_quant(const void* k, const void* v, const int32_t* slot_mapp
 int fp8pa_kv_channel_scales(const void* x, int num_tokens, int n_kv_heads, int head_dim, int fmt,
                             float* scale_out, void* stream) {
   if (num_tokens < 0 || n_kv_heads <= 0 || head_dim <= 0) return FP8PA_ERR_BAD_SHAPE;
-  if (fmt != FP8PA_E4M3 && fmt != FP8PA_E5M2) return FP8PA_ERR_BAD_ENUM;
+  if (fmt != FP8PA_E4M3 && fmt != FP8PA_E5M2 && fmt != FP8PA_INT8) return FP8PA_ERR_BAD_ENUM;
   if (head_dim % 16 != 0) return FP8PA_ERR_UNSUPPORTED;
   if (!scale_out || (num_tokens > 0 && !x)) return FP8PA_ERR_NULL_POINTER;
   if ((num_tokens > 0 && !aligned16(x)) || !aligned16(scale_out)) return FP8PA_ERR_ALIGNMENT;
@@ -396,7 +396,7 @@ int fp8pa_kv_channel_absmax_update(const void* x, int num_tokens, int n_kv_heads
 int fp8pa_kv_scales_from_absmax(const float* absmax, int n, int fmt, float* scale_out,
                                 void* stream) {
   if (n <= 0) return FP8PA_ERR_BAD_SHAPE;
-  if (fmt != FP8PA_E4M3 && fmt != FP8PA_E5M2) return FP8PA_ERR_BAD_ENUM;
+  if (fmt != FP8PA_E4M3 && fmt != FP8PA_E5M2 && fmt != FP8PA_INT8) return FP8PA_ERR_BAD_ENUM;
   if (!absmax || !scale_out) return FP8PA_ERR_NULL_POINTER;
   return cuda_status(
       launch_scales_from_absmax(absmax, n, fmt, scale_out, static_cast<cudaStream_t>(stream)));
@@ -415,7 +415,7 @@ size_t fp8pa_multiquery_workspace_bytes(int batch, int q_len, int n_q_heads, int
                         FP8PA_SCALE_CHANNEL_STATIC, FP8PA_SCALE_MX_BLOCK};
   size_t need = 0;
   for (int m = 0; m < (mla ? 1 : 3); ++m)
-    for (int fmt = FP8PA_E4M3; fmt <= FP8PA_E5M2; ++fmt) {
+    for (int fmt = FP8PA_E4M3; fmt <= FP8PA_INT8; ++fmt) {
       DecodePath path = decode_path(batch * q_len, n_q_heads, n_kv_heads, head_dim, head_dim_v,
                                     block_size, max_blocks_per_seq, fmt, modes[m],
                                     mla ? 64 : 16, 1, FP8PA_OUT_BF16);

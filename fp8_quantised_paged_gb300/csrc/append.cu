@@ -202,8 +202,9 @@ cudaError_t launch_append_m(const AppendArgs& a, int mode, const PlanArgs* pl,
       return launch_append_r<FMT, FP8PA_SCALE_TOKEN_HEAD>(a, pl, stream);
     case FP8PA_SCALE_CHANNEL_STATIC:
       return launch_append_r<FMT, FP8PA_SCALE_CHANNEL_STATIC>(a, pl, stream);
-    case FP8PA_SCALE_MX_BLOCK:
-      return launch_append_r<FMT, FP8PA_SCALE_MX_BLOCK>(a, pl, stream);
+    case FP8PA_SCALE_MX_BLOCK:  // FP8 only (rejected for INT8 by the caller)
+      if constexpr (FMT != FP8PA_INT8) return launch_append_r<FMT, FP8PA_SCALE_MX_BLOCK>(a, pl, stream);
+      return cudaErrorInvalidValue;
     default:
       return launch_append_r<FMT, FP8PA_SCALE_TOKEN_GROUP>(a, pl, stream);
   }
@@ -243,14 +244,20 @@ __global__ void chanscale_finalize_kernel(const float* amax, float* s, int hd) {
 }  // namespace
 
 cudaError_t launch_append(const AppendArgs& a, int fmt, int mode, cudaStream_t stream) {
-  return fmt == FP8PA_E4M3 ? launch_append_m<FP8PA_E4M3>(a, mode, nullptr, stream)
-                           : launch_append_m<FP8PA_E5M2>(a, mode, nullptr, stream);
+  switch (fmt) {
+    case FP8PA_E4M3: return launch_append_m<FP8PA_E4M3>(a, mode, nullptr, stream);
+    case FP8PA_E5M2: return launch_append_m<FP8PA_E5M2>(a, mode, nullptr, stream);
+    default: return launch_append_m<FP8PA_INT8>(a, mode, nullptr, stream);
+  }
 }
 
 cudaError_t launch_append_plan(const AppendArgs& a, int fmt, int mode, const PlanArgs& pl,
                                cudaStream_t stream) {
-  return fmt == FP8PA_E4M3 ? launch_append_m<FP8PA_E4M3>(a, mode, &pl, stream)
-                           : launch_append_m<FP8PA_E5M2>(a, mode, &pl, stream);
+  switch (fmt) {
+    case FP8PA_E4M3: return launch_append_m<FP8PA_E4M3>(a, mode, &pl, stream);
+    case FP8PA_E5M2: return launch_append_m<FP8PA_E5M2>(a, mode, &pl, stream);
+    default: return launch_append_m<FP8PA_INT8>(a, mode, &pl, stream);
+  }
 }
 
 cudaError_t launch_channel_absmax(const uint16_t* x, int num_tokens, int hd, float* amax,
@@ -267,8 +274,10 @@ cudaError_t launch_scales_from_absmax(const float* amax, int n, int fmt, float* 
   const int blocks = (n + 255) / 256;
   if (fmt == FP8PA_E4M3)
     chanscale_finalize_kernel<FP8PA_E4M3><<<blocks, 256, 0, stream>>>(amax, out, n);
-  else
+  else if (fmt == FP8PA_E5M2)
     chanscale_finalize_kernel<FP8PA_E5M2><<<blocks, 256, 0, stream>>>(amax, out, n);
+  else
+    chanscale_finalize_kernel<FP8PA_INT8><<<blocks, 256, 0, stream>>>(amax, out, n);
   return cudaGetLastError();
 }
 

@@ -108,10 +108,21 @@ __device__ __forceinline__ uint2 lds64(uint32_t addr) {
   return v;
 }
 
-// ---------------------------------------------------------------- FP8 conversions
-// Two FP8 codes (low byte = element 0) -> f16x2, exact for both formats.
+// ---------------------------------------------------------------- code conversions
+// INT8 codes b in [-128, 127] -> f16, exactly: the byte b + 128 becomes the
+// low mantissa byte of the f16 1024 (giving 1024 + b + 128), then 1152 is
+// subtracted.  `sel` picks the two bytes of `four_codes` (byte permute).
+__device__ __forceinline__ uint32_t int8x2_to_f16x2(uint32_t four_codes, uint32_t sel) {
+  const uint32_t biased = __byte_perm(four_codes ^ 0x80808080u, 0x64646464u, sel);
+  const __half2 r = __hsub2(*reinterpret_cast<const __half2*>(&biased),
+                            __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480)));
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
+
+// Two codes (low byte = element 0) -> f16x2, exact for every format.
 template <int FMT>
 __device__ __forceinline__ uint32_t fp8x2_to_f16x2(uint32_t two_codes) {
+  if constexpr (FMT == FP8PA_INT8) return int8x2_to_f16x2(two_codes, 0x5140u);
   uint32_t r;
   const uint16_t v = static_cast<uint16_t>(two_codes & 0xFFFFu);
   if constexpr (FMT == FP8PA_E4M3) {
@@ -126,7 +137,10 @@ __device__ __forceinline__ uint32_t fp8x2_to_f16x2(uint32_t two_codes) {
 // hi = elements 2,3; the two halves of the word are converted in place.
 template <int FMT>
 __device__ __forceinline__ void fp8x4_to_f16x2x2(uint32_t four_codes, uint32_t& lo, uint32_t& hi) {
-  if constexpr (FMT == FP8PA_E4M3) {
+  if constexpr (FMT == FP8PA_INT8) {
+    lo = int8x2_to_f16x2(four_codes, 0x5140u);
+    hi = int8x2_to_f16x2(four_codes, 0x5342u);
+  } else if constexpr (FMT == FP8PA_E4M3) {
     asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
         "cvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
         : "=r"(lo), "=r"(hi)
@@ -139,10 +153,16 @@ __device__ __forceinline__ void fp8x4_to_f16x2x2(uint32_t four_codes, uint32_t& 
   }
 }
 
-// Two fp32 values -> two FP8 codes (lo -> low byte), round to nearest even,
-// finite overflow saturated to +-max, NaN to NaN.
+// Two fp32 values -> two codes (lo -> low byte), round to nearest even.
+// FP8: finite overflow saturated to +-max, NaN to NaN.  INT8: clamped to
+// [-127, 127] (infinities too), NaN to 0.
 template <int FMT>
 __device__ __forceinline__ uint32_t f32x2_to_fp8x2(float lo, float hi) {
+  if constexpr (FMT == FP8PA_INT8) {
+    const int a = min(127, max(-127, __float2int_rn(lo)));
+    const int b = min(127, max(-127, __float2int_rn(hi)));
+    return (static_cast<uint32_t>(a) & 0xFFu) | ((static_cast<uint32_t>(b) & 0xFFu) << 8);
+  }
   uint16_t r;
   if constexpr (FMT == FP8PA_E4M3) {
     asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
@@ -152,9 +172,10 @@ __device__ __forceinline__ uint32_t f32x2_to_fp8x2(float lo, float hi) {
   return static_cast<uint32_t>(r);
 }
 
+// Largest code magnitude: FMAX of the absmax / FMAX scale.
 template <int FMT>
 __host__ __device__ constexpr float fp8_max() {
-  return FMT == FP8PA_E4M3 ? 448.0f : 57344.0f;
+  return FMT == FP8PA_E4M3 ? 448.0f : (FMT == FP8PA_E5M2 ? 57344.0f : 127.0f);
 }
 
 // ---------------------------------------------------------------- math

@@ -739,7 +739,9 @@ template <int D, int BS, int FMT>
 SplitKernel pick3(int mode) {
   switch (mode) {
     case FP8PA_SCALE_TOKEN_HEAD: return pick4<D, BS, FMT, FP8PA_SCALE_TOKEN_HEAD>();
-    case FP8PA_SCALE_MX_BLOCK: return pick4<D, BS, FMT, FP8PA_SCALE_MX_BLOCK>();
+    case FP8PA_SCALE_MX_BLOCK:  // FP8 codes only (rejected for INT8 before launch)
+      if constexpr (FMT != FP8PA_INT8) return pick4<D, BS, FMT, FP8PA_SCALE_MX_BLOCK>();
+      return pick4<D, BS, FMT, FP8PA_SCALE_TOKEN_HEAD>();
     case kModeStaticPacked: return pick4<D, BS, FMT, kModeStaticPacked>();
     default: return pick4<D, BS, FMT, FP8PA_SCALE_CHANNEL_STATIC>();
   }
@@ -747,7 +749,11 @@ SplitKernel pick3(int mode) {
 
 template <int D, int BS>
 SplitKernel pick2(int fmt, int mode) {
-  return fmt == FP8PA_E4M3 ? pick3<D, BS, FP8PA_E4M3>(mode) : pick3<D, BS, FP8PA_E5M2>(mode);
+  switch (fmt) {
+    case FP8PA_E4M3: return pick3<D, BS, FP8PA_E4M3>(mode);
+    case FP8PA_E5M2: return pick3<D, BS, FP8PA_E5M2>(mode);
+    default: return pick3<D, BS, FP8PA_INT8>(mode);
+  }
 }
 
 template <int D>

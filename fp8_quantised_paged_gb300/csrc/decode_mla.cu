@@ -478,7 +478,9 @@ cudaError_t launch_decode_mla(const DecodeShape& s, const DecodeArgs& a, cudaStr
   const int H = s.hq / kHeads;
   const int ranges = s.workers / H;
   const int smem = MlaSmem::kBytes;
-  auto kfn = a.fmt == FP8PA_E4M3 ? mla_split_kernel<FP8PA_E4M3> : mla_split_kernel<FP8PA_E5M2>;
+  auto kfn = a.fmt == FP8PA_E4M3   ? mla_split_kernel<FP8PA_E4M3>
+             : a.fmt == FP8PA_E5M2 ? mla_split_kernel<FP8PA_E5M2>
+                                   : mla_split_kernel<FP8PA_INT8>;
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kfn), smem);
   if (e != cudaSuccess) return e;
   char* ws = static_cast<char*>(a.workspace);

@@ -76,9 +76,12 @@ extern "C" {
 #define FP8PA_DEVERR_SEQ_LEN 4u      /* decode: seq_len < 0 or > max_blocks_per_seq*block_size (clamped) */
 #define FP8PA_DEVERR_TIMEOUT 8u      /* decode: a bounded wait on an async copy ran out (work abandoned) */
 
-/* FP8 formats. */
+/* Code formats: FP8 E4M3 and E5M2, and symmetric INT8 (the alternate KV
+ * codec; FMAX = 127, codes in [-127, 127] as two's complement bytes, value
+ * = the integer; not with FP8PA_SCALE_MX_BLOCK). */
 #define FP8PA_E4M3 0
 #define FP8PA_E5M2 1
+#define FP8PA_INT8 2
 
 /* Scale granularities. */
 #define FP8PA_SCALE_TOKEN_HEAD 0     /* dynamic: one f32 per (token, kv head), written by append */
@@ -101,7 +104,8 @@ extern "C" {
  *               v_cache/v_scale are ignored: the single-latent MLA cache).
  * slot_mapping  i32 [num_tokens]; a negative slot skips that token.  Two
  *               tokens with the same slot in one call race (undefined).
- * fmt           FP8PA_E4M3 or FP8PA_E5M2.
+ * fmt           FP8PA_E4M3, FP8PA_E5M2 or FP8PA_INT8 (FMAX 127 in every
+ *               scale below).
  * scale_mode    TOKEN_HEAD: s = max(absmax(row)/FMAX, 1e-12), written to
  *               k_scale/v_scale.  TOKEN_GROUP: the same per group of
  *               group_size dims.  CHANNEL_STATIC: s = k_scale[h][d] given
@@ -113,8 +117,13 @@ extern "C" {
  *               that "FP8混合精度推理全链路部署实战"
  *               (ybb.press/ai-applications/14145.html) sec. 7.1 names for
  *               Blackwell; codes = fp8_rne_satfinite(x * 2^-e), exact scaling.
- * code          = fp8_rne_satfinite(x / s), IEEE fp32 division; codes are
- *               bit-exact with the definition above.
+ * code          = fp8_rne_satfinite(x / s), IEEE fp32 division; INT8:
+ *               x / s rounded to the nearest integer, ties to even, clamped
+ *               to [-127, 127] (an INT8 KV cache is named only as a serving
+ *               option, hotelren.com/news/5166672, inference-engine settings;
+ *               the rest is this library's reading).  Codes are bit-exact
+ *               with the definition above.  MX_BLOCK is FP8 only
+ *               (FP8PA_ERR_UNSUPPORTED with INT8).
  * Requirements  head_dim % 16 == 0, head_dim <= 768; group_size in
  *               {16,32,64,128,256} dividing head_dim ({16,32} for MX_BLOCK);
  *               block_size > 0;
@@ -195,12 +204,15 @@ size_t fp8pa_multiquery_workspace_bytes(int batch, int q_len, int n_q_heads, int
  * Two layouts are served:
  *  GQA  n_q_heads % n_kv_heads == 0, n_q_heads/n_kv_heads <= 8, head_dim in
  *       {64, 128}, head_dim_v == head_dim, block_size in {16, 32, 64},
- *       scale_mode TOKEN_HEAD or CHANNEL_STATIC, separate v_cache/v_scale.
+ *       scale_mode TOKEN_HEAD, CHANNEL_STATIC or MX_BLOCK (group_size 16
+ *       or 32, FP8 codes), separate v_cache/v_scale.
  *  MLA  n_kv_heads == 1, head_dim 576 (512 latent + 64 rope), head_dim_v
  *       512 (the first 512 dims of the same latent), v_cache == k_cache,
  *       v_scale == k_scale, scale_mode TOKEN_GROUP, group_size 64,
  *       block_size 64, n_q_heads a multiple of 32.
  *
+ * fmt          FP8PA_E4M3, FP8PA_E5M2 or FP8PA_INT8: the codes as
+ *              fp8pa_kv_append_quant wrote them (decoded exactly to f16).
  * seq_lens     i32 [batch], including any token appended this step; 0 gives
  *              a zero output row.
  * num_blocks   size of the pool (bounds block ids; sizes the copy maps).

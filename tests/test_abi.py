@@ -65,6 +65,9 @@ def test_argument_errors_need_no_device(lib):
     # no tokens: nothing to do
     assert lib.fp8pa_kv_append_quant(None, None, None, 0, 1, 64, 0, 0, 64, None, None, None, None,
                                      8, 16, None) == 0
+    # INT8 codes with power-of-two (MX) block scales: not a defined pairing
+    assert lib.fp8pa_kv_append_quant(fake, None, fake, 4, 1, 64, 2, 3, 32, fake, None, fake, None,
+                                     8, 16, None) == -4
 
     def dec(**kw):
         a = dict(q=fake, kc=fake, vc=fake, ks=fake, vs=fake, bt=fake, mb=4, sl=fake, B=2, bs=16,
@@ -78,6 +81,7 @@ def test_argument_errors_need_no_device(lib):
 
     assert dec(hq=7) == -3          # Hq % Hkv != 0
     assert dec(fmt=3) == -2
+    assert dec(fmt=2, mode=3, gs=32) == -4  # INT8 codes with MX block scales
     assert dec(mode=5) == -2
     assert dec(odt=2) == -2
     assert dec(d=96, dv=96) == -4   # head_dim not served

@@ -4,7 +4,8 @@ and 8, KV-head counts that are not a power of two or need several head sets
 per CTA, both formats with both GQA scale modes, KV-head counts up to 24,
 and the latent layout with 32 and 64 query heads.  Static scales with 1, 2
 or 4 query heads per KV head run the packed kernel (q's high and low parts
-in one MMA), at head_dim 64 and 128.  Every output is compared with the FP64 oracle;
+in one MMA), at head_dim 64 and 128.  INT8 codes run through the same
+layouts (token-head, static, latent).  Every output is compared with the FP64 oracle;
 lengths include 1, block_size - 1, block_size, block_size + 1 and several
 pages with a ragged tail."""
 import numpy as np
@@ -15,7 +16,7 @@ from fp8_quantised_paged_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
 
-E4, E5 = W.E4M3, W.E5M2
+E4, E5, I8 = W.E4M3, W.E5M2, W.INT8
 TH, CS, TG, MX = W.SCALE_TOKEN_HEAD, W.SCALE_CHANNEL_STATIC, W.SCALE_TOKEN_GROUP, W.SCALE_MX_BLOCK
 
 # name, hq, hkv, d, bs, fmt, mode
@@ -32,6 +33,11 @@ CASES = [
     ("mla_64_heads_e5m2", 64, 1, 576, 64, E5, TG),
     ("g4_hkv2_d64_bs16_e4m3_static", 8, 2, 64, 16, E4, CS),
     ("g1_hkv4_d64_bs64_e5m2_static", 4, 4, 64, 64, E5, CS),
+    ("int8_g8_d128_bs16_token", 64, 8, 128, 16, I8, TH),
+    ("int8_g4_hkv2_d64_bs32_static", 8, 2, 64, 32, I8, CS),
+    ("int8_g3_hkv3_d128_bs64_static", 9, 3, 128, 64, I8, CS),
+    ("int8_g2_hkv4_d64_bs16_token", 8, 4, 64, 16, I8, TH),
+    ("int8_mla_32_heads", 32, 1, 576, 64, I8, TG),
 ]
 
 
@@ -67,7 +73,8 @@ def test_shape_matches_oracle(F, case):
     assert F.get_device_error() == 0
 
 
-@pytest.mark.parametrize("case", [CASES[1], CASES[2], CASES[8], CASES[10]], ids=lambda c: c[0])
+@pytest.mark.parametrize("case", [CASES[1], CASES[2], CASES[8], CASES[10], CASES[12], CASES[16]],
+                         ids=lambda c: c[0])
 def test_shape_multiquery_matches_oracle(F, case):
     from gpu_util import check_close, gpu_cache, gpu_multiquery, oracle_cache, oracle_multiquery
     name, hq, hkv, d, bs, fmt, mode = case
