@@ -72,7 +72,7 @@ __device__ __forceinline__ void append_row(const AppendArgs& a, long row, int la
     }
   }
 
-  constexpr float kFmax = fp8_max<FMT>();
+  constexpr float kFmax = code_max<FMT>();
   constexpr int kEmax = FMT == FP8PA_E4M3 ? 8 : 15;  // exponent of the largest normal
   float s[R];
   if constexpr (MODE == FP8PA_SCALE_TOKEN_HEAD) {
@@ -136,8 +136,8 @@ __device__ __forceinline__ void append_row(const AppendArgs& a, long row, int la
       for (int e = 0; e < 8; ++e) q[e] = __fdiv_rn(v[r][e], s[r]);
     }
     uint2 packed;
-    packed.x = f32x2_to_fp8x2<FMT>(q[0], q[1]) | (f32x2_to_fp8x2<FMT>(q[2], q[3]) << 16);
-    packed.y = f32x2_to_fp8x2<FMT>(q[4], q[5]) | (f32x2_to_fp8x2<FMT>(q[6], q[7]) << 16);
+    packed.x = f32x2_to_codes2<FMT>(q[0], q[1]) | (f32x2_to_codes2<FMT>(q[2], q[3]) << 16);
+    packed.y = f32x2_to_codes2<FMT>(q[4], q[5]) | (f32x2_to_codes2<FMT>(q[6], q[7]) << 16);
     *reinterpret_cast<uint2*>(dst + ci * 8) = packed;
   }
 }
@@ -238,7 +238,7 @@ template <int FMT>
 __global__ void chanscale_finalize_kernel(const float* amax, float* s, int hd) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= hd) return;
-  s[i] = fmaxf(__fdiv_rn(amax[i], fp8_max<FMT>()), 1e-12f);
+  s[i] = fmaxf(__fdiv_rn(amax[i], code_max<FMT>()), 1e-12f);
 }
 
 }  // namespace

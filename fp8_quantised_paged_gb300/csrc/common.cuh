@@ -121,7 +121,7 @@ __device__ __forceinline__ uint32_t int8x2_to_f16x2(uint32_t four_codes, uint32_
 
 // Two codes (low byte = element 0) -> f16x2, exact for every format.
 template <int FMT>
-__device__ __forceinline__ uint32_t fp8x2_to_f16x2(uint32_t two_codes) {
+__device__ __forceinline__ uint32_t codes2_to_f16x2(uint32_t two_codes) {
   if constexpr (FMT == FP8PA_INT8) return int8x2_to_f16x2(two_codes, 0x5140u);
   uint32_t r;
   const uint16_t v = static_cast<uint16_t>(two_codes & 0xFFFFu);
@@ -133,10 +133,10 @@ __device__ __forceinline__ uint32_t fp8x2_to_f16x2(uint32_t two_codes) {
   return r;
 }
 
-// Four FP8 codes (byte i = element i) -> two f16x2: lo = elements 0,1 and
+// Four codes (byte i = element i) -> two f16x2: lo = elements 0,1 and
 // hi = elements 2,3; the two halves of the word are converted in place.
 template <int FMT>
-__device__ __forceinline__ void fp8x4_to_f16x2x2(uint32_t four_codes, uint32_t& lo, uint32_t& hi) {
+__device__ __forceinline__ void codes4_to_f16x2x2(uint32_t four_codes, uint32_t& lo, uint32_t& hi) {
   if constexpr (FMT == FP8PA_INT8) {
     lo = int8x2_to_f16x2(four_codes, 0x5140u);
     hi = int8x2_to_f16x2(four_codes, 0x5342u);
@@ -157,7 +157,7 @@ __device__ __forceinline__ void fp8x4_to_f16x2x2(uint32_t four_codes, uint32_t& 
 // FP8: finite overflow saturated to +-max, NaN to NaN.  INT8: clamped to
 // [-127, 127] (infinities too), NaN to 0.
 template <int FMT>
-__device__ __forceinline__ uint32_t f32x2_to_fp8x2(float lo, float hi) {
+__device__ __forceinline__ uint32_t f32x2_to_codes2(float lo, float hi) {
   if constexpr (FMT == FP8PA_INT8) {
     const int a = min(127, max(-127, __float2int_rn(lo)));
     const int b = min(127, max(-127, __float2int_rn(hi)));
@@ -174,7 +174,7 @@ __device__ __forceinline__ uint32_t f32x2_to_fp8x2(float lo, float hi) {
 
 // Largest code magnitude: FMAX of the absmax / FMAX scale.
 template <int FMT>
-__host__ __device__ constexpr float fp8_max() {
+__host__ __device__ constexpr float code_max() {
   return FMT == FP8PA_E4M3 ? 448.0f : (FMT == FP8PA_E5M2 ? 57344.0f : 127.0f);
 }
 

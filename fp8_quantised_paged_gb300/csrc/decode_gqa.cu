@@ -483,8 +483,8 @@ __global__ void __launch_bounds__(kMaxWarps * 32)
 #pragma unroll
       for (int j = 0; j < KW; ++j) {
         uint32_t a0, a1, a2, a3;
-        fp8x4_to_f16x2x2<FMT>(kw[0][j], a0, a2);
-        fp8x4_to_f16x2x2<FMT>(kw[1][j], a1, a3);
+        codes4_to_f16x2x2<FMT>(kw[0][j], a0, a2);
+        codes4_to_f16x2x2<FMT>(kw[1][j], a1, a3);
         if constexpr (MX) {
           const bool hb = 4 * j >= p.gs;
           const uint32_t f0 = hb ? fk0b : fk0a, f1 = hb ? fk1b : fk1a;
@@ -630,8 +630,8 @@ __global__ void __launch_bounds__(kMaxWarps * 32)
         const uint32_t x01 = prmt(vw[0][t >> 1], vw[1][t >> 1], sel);
         const uint32_t x23 = prmt(vw[2][t >> 1], vw[3][t >> 1], sel);
         uint32_t a0, a1, a2, a3;
-        fp8x4_to_f16x2x2<FMT>(x01, a0, a1);
-        fp8x4_to_f16x2x2<FMT>(x23, a2, a3);
+        codes4_to_f16x2x2<FMT>(x01, a0, a1);
+        codes4_to_f16x2x2<FMT>(x23, a2, a3);
         if constexpr (MX) {
           a0 = hmul2_bits(a0, fv01);
           a1 = hmul2_bits(a1, fv01);

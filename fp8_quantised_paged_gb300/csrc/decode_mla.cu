@@ -250,14 +250,14 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const MlaParams 
       uint4 lo4, hi4;
       if (t < valid) {
         const uint4 u = *reinterpret_cast<const uint4*>(codes + t * kDk + col);
-        lo4.x = fp8x2_to_f16x2<FMT>(u.x);
-        lo4.y = fp8x2_to_f16x2<FMT>(u.x >> 16);
-        lo4.z = fp8x2_to_f16x2<FMT>(u.y);
-        lo4.w = fp8x2_to_f16x2<FMT>(u.y >> 16);
-        hi4.x = fp8x2_to_f16x2<FMT>(u.z);
-        hi4.y = fp8x2_to_f16x2<FMT>(u.z >> 16);
-        hi4.z = fp8x2_to_f16x2<FMT>(u.w);
-        hi4.w = fp8x2_to_f16x2<FMT>(u.w >> 16);
+        lo4.x = codes2_to_f16x2<FMT>(u.x);
+        lo4.y = codes2_to_f16x2<FMT>(u.x >> 16);
+        lo4.z = codes2_to_f16x2<FMT>(u.y);
+        lo4.w = codes2_to_f16x2<FMT>(u.y >> 16);
+        hi4.x = codes2_to_f16x2<FMT>(u.z);
+        hi4.y = codes2_to_f16x2<FMT>(u.z >> 16);
+        hi4.z = codes2_to_f16x2<FMT>(u.w);
+        hi4.w = codes2_to_f16x2<FMT>(u.w >> 16);
       } else {
         lo4 = make_uint4(0, 0, 0, 0);
         hi4 = lo4;
