@@ -1,5 +1,6 @@
-// append.cu -- the append step: absmax scale, FP8 rounding and the slot
-// scatter into the paged cache; and the static per-channel scale calibration.
+// append.cu -- the append step: absmax scale, FP8 (or INT8) rounding and the
+// slot scatter into the paged cache; and the static per-channel scale
+// calibration.
 //
 // Method: scale = absmax / 448 (E4M3) or / 57344 (E5M2), clamped below at
 // 1e-12, code = fp8(x / scale) ("Llama 3 70B FP8 deployment",
@@ -9,11 +10,15 @@
 // 2kiu.com/news/4508674, sec. 2.2 / 2.4) or a static one per channel
 // ("DeepSeek-V4.1 512K", hotelren.com/news/5711065, sec. 3.3).  Codes land in
 // block slot / block_size at offset slot % block_size (same page, sec. 3.3).
+// MX block mode: a power-of-two scale per block of 16 or 32 dims (E8M0).
+// The symmetric INT8 codec takes 127 as the maximum and rounds x / scale to
+// the nearest integer, ties to even, clamped to [-127, 127].
 //
 // One warp per (token, kv head, K-or-V) row.  Each lane owns 8 contiguous
 // values (one 16-byte load, one 8-byte code store).  The divisions are IEEE
 // fp32 round-to-nearest (__fdiv_rn) and the FP8 cast is the hardware
-// cvt.rn.satfinite, so codes and scales are bit-exact with the definition.
+// cvt.rn.satfinite (INT8: cvt.rni), so codes and scales are bit-exact with
+// the definition.
 #include "common.cuh"
 #include "internal.h"
 #include "plan.cuh"

@@ -17,20 +17,23 @@
 //    the merge (merge.cu) folds the partials of each output row with the
 //    log-sum-exp rule.  Balance is exact for ragged batches and a
 //    128K-token request spreads over the whole GPU.
-//  * Each warp streams its pages through a private ring of shared-memory
-//    stages filled by the tensor-copy engine (TMA, 2-D boxes of
-//    block_size x head_dim bytes with the 128/64-byte swizzle) plus 1-D bulk
-//    copies of the per-token scales, completion tracked by mbarriers.  One
-//    lane issues; no thread waits on another CTA.  Every wait is bounded.
+//  * Each warp streams its pages, as 16-token slices, through a private
+//    ring of shared-memory stages filled by the tensor-copy engine (TMA,
+//    2-D boxes of 16 x head_dim bytes with the 128/64-byte swizzle) plus 1-D
+//    bulk copies of the per-token scales, completion tracked by mbarriers.
+//    One lane issues; no thread waits on another CTA.  Every wait is
+//    bounded.
 //  * The G <= 8 heads sharing a KV head form a tiny dense contraction
 //    (16 tokens x 8 heads x head_dim per tile).  GB300's FP32 pipe cannot
 //    keep up with HBM on it (about 8 FMA per cached byte), so QK^T and PV
-//    run on warp MMA (m16n8k16, f16 in, f32 accumulate) over codes converted
-//    exactly to f16 in registers.  Scales stay outside the contraction: the
-//    per-token K scale multiplies the score, the per-token V scale folds
-//    into P, per-channel K scales fold into q, per-channel V scales multiply
-//    the output; MX block exponents scale the f16 fragments by exact powers
-//    of two.  Power-of-two normalisers keep q and P inside f16's range.
+//    run on warp MMA (m16n8k16, f16 in, f32 accumulate) over codes (FP8 or
+//    INT8) converted exactly to f16 in registers.  Scales stay outside the
+//    contraction: the per-token K scale multiplies the score, the per-token
+//    V scale folds into P, per-channel K scales fold into q (as an f16 high
+//    and low part; with G <= 4 both parts share one MMA's head columns),
+//    per-channel V scales multiply the output; MX block exponents scale the
+//    f16 fragments by exact powers of two.  Power-of-two normalisers keep q
+//    and P inside f16's range.
 //  * Softmax runs in FP32 in the log2 domain with warp-shuffle maxima.
 #include <float.h>
 
