@@ -91,3 +91,55 @@ def test_argument_errors_need_no_device(lib):
     assert dec(vc=None) == -1
     assert dec(B=0) == 0
     assert dec(d=576, dv=512, hkv=1, hq=128, mode=2, bs=64, vc=P(0x2000)) == -4  # MLA needs v==k
+
+
+C_PROGRAM = r"""
+#include <stdio.h>
+#include <string.h>
+#include "fp8pa.h"
+
+/* Host-only use of the C ABI from plain C: version, status strings and
+ * argument errors (none of these touch a device). */
+int main(void) {
+  const int major = fp8pa_version() >> 16;
+  if (major != 1) { printf("version %d\n", major); return 1; }
+  if (strcmp(fp8pa_error_string(FP8PA_ERR_WORKSPACE), "workspace missing or too small") != 0)
+    return 2;
+  static uint16_t k[4 * 64];
+  static int32_t slots[4];
+  static uint8_t cache[8 * 16 * 64];
+  static float scale[8 * 16];
+  int rc = fp8pa_kv_append_quant(k, NULL, slots, 4, 1, 64, 7 /* no such format */,
+                                 FP8PA_SCALE_TOKEN_HEAD, 64, cache, NULL, scale, NULL, 8, 16,
+                                 NULL);
+  if (rc != FP8PA_ERR_BAD_ENUM) { printf("append rc %d\n", rc); return 3; }
+  rc = fp8pa_kv_append_quant(k, NULL, slots, 4, 1, 64, FP8PA_INT8, FP8PA_SCALE_MX_BLOCK, 32,
+                             cache, NULL, scale, NULL, 8, 16, NULL);
+  if (rc != FP8PA_ERR_UNSUPPORTED) { printf("int8+mx rc %d\n", rc); return 4; }
+  rc = fp8pa_paged_decode_attention(NULL, NULL, NULL, NULL, NULL, NULL, 4, NULL, 0, 16, 8, 2,
+                                    128, 128, FP8PA_E4M3, FP8PA_SCALE_TOKEN_HEAD, 64, 0.1f, 16,
+                                    NULL, FP8PA_OUT_BF16, NULL, 0, NULL);
+  if (rc != FP8PA_OK) { printf("empty batch rc %d\n", rc); return 5; }
+  puts("ok");
+  return 0;
+}
+"""
+
+
+def test_plain_c_program_builds_against_the_header_and_runs(lib, tmp_path):
+    """The boundary is a C ABI: a C11 program (pedantic, warnings as errors)
+    compiles against include/fp8pa.h, links libfp8pa.so and runs."""
+    import shutil
+    import subprocess
+    from fp8_quantised_paged_gb300 import _native
+    if shutil.which("gcc") is None:
+        pytest.skip("no gcc")
+    src = tmp_path / "use_abi.c"
+    src.write_text(C_PROGRAM)
+    exe = tmp_path / "use_abi"
+    libdir = os.path.dirname(_native.LIB_PATH)
+    subprocess.run(["gcc", "-std=c11", "-Wall", "-Wextra", "-pedantic", "-Werror",
+                    "-I", os.path.join(ROOT, "include"), str(src), "-L", libdir, "-lfp8pa",
+                    "-Wl,-rpath," + libdir, "-o", str(exe)], check=True)
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0 and r.stdout.strip() == "ok", (r.returncode, r.stdout, r.stderr)
