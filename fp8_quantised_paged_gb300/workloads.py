@@ -36,6 +36,7 @@ import numpy as np
 
 E4M3, E5M2, INT8 = 0, 1, 2
 SCALE_TOKEN_HEAD, SCALE_CHANNEL_STATIC, SCALE_TOKEN_GROUP, SCALE_MX_BLOCK = 0, 1, 2, 3
+SCALE_SEGMENT = 4  # one scale per (page, KV head), refreshed every 1024 tokens
 
 
 def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
@@ -84,7 +85,7 @@ class Workload:
                 "head_dim_v": self.head_dim_v, "block_size": self.block_size,
                 "kv_fmt": {E4M3: "e4m3", E5M2: "e5m2", INT8: "int8"}[self.fmt],
                 "scale_mode": ["token_head", "channel_static", "token_group",
-                               f"mx_block_{self.group_size}"][self.scale_mode],
+                               f"mx_block_{self.group_size}", "segment_1024"][self.scale_mode],
                 "kv_tokens": self.total_tokens, "num_blocks": self.num_blocks}
 
 

@@ -24,6 +24,8 @@ _LIB_PATH = os.path.join(_HERE, "liboracle.so")
 
 E4M3, E5M2, INT8 = 0, 1, 2  # INT8: the symmetric alternate codec (FMAX 127)
 SCALE_TOKEN_HEAD, SCALE_CHANNEL_STATIC, SCALE_TOKEN_GROUP, SCALE_MX_BLOCK = 0, 1, 2, 3
+SCALE_SEGMENT = 4
+SEGMENT_TOKENS = 1024
 
 _lib = None
 
@@ -63,6 +65,8 @@ def _load():
     lib.or_kv_append_quant.argtypes = [P, P, P, i, i, i, i, i, i, P, P, P, P, i, i]
     lib.or_kv_append_quant.restype = i
     lib.or_kv_channel_scales.argtypes = [P, i, i, i, i, P]
+    lib.or_kv_append_quant_segment.argtypes = [P, P, P, P, P, i, i, i, i, P, P, P, P, P, i, i]
+    lib.or_kv_append_quant_segment.restype = i
     lib.or_paged_decode_attention.argtypes = [P, P, P, P, P, P, i, P, i, i, i, i, i, i, i, i, i,
                                               d, i, P, i, P, i]
     lib.or_paged_decode_attention.restype = i
@@ -124,6 +128,8 @@ def kv_append_quant(k, v, slot_mapping, fmt, scale_mode, group_size, k_cache, v_
     of shape [num_tokens, Hkv, D].  Returns the count of out-of-range slots."""
     if fmt == INT8 and scale_mode == SCALE_MX_BLOCK:
         raise ValueError("the power-of-two block mode is defined for FP8 codes only")
+    if scale_mode == SCALE_SEGMENT:
+        raise ValueError("the segment mode needs positions: use kv_append_quant_segment")
     k = _c(k, np.uint16)
     v = _c(v, np.uint16)
     sm = _c(slot_mapping, np.int32)
@@ -138,6 +144,39 @@ def kv_append_quant(k, v, slot_mapping, fmt, scale_mode, group_size, k_cache, v_
     return int(_load().or_kv_append_quant(_ptr(k), _ptr(v), _ptr(sm), n, hkv, d, fmt, scale_mode,
                                           group_size, _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
                                           _ptr(v_scale), num_blocks, block_size))
+
+
+def segment_scale_heads(n_kv_heads: int) -> int:
+    """Row length of the segment scale array: KV heads rounded up to 4."""
+    return (n_kv_heads + 3) // 4 * 4
+
+
+def kv_append_quant_segment(k, v, slot_mapping, seq_offsets, seq_start_pos, fmt, seg_state,
+                            k_cache, v_cache, k_scale, v_scale, block_size) -> int:
+    """Segment-scale append (block-wise cumulative rescaling), in place.
+    k/v: bf16 bits [num_tokens, Hkv, D]; sequence r owns rows
+    seq_offsets[r]:seq_offsets[r+1] at positions seq_start_pos[r] + 0, 1, ...;
+    seg_state: float32 [num_seqs, 2, Hkv, 2] (running absmax, segment scale),
+    updated; scales: float32 [num_blocks, round_up(Hkv, 4)].  Returns the
+    count of out-of-range slots."""
+    k = _c(k, np.uint16)
+    v = _c(v, np.uint16)
+    sm = _c(slot_mapping, np.int32)
+    off = _c(seq_offsets, np.int32)
+    sp = _c(seq_start_pos, np.int32)
+    n, hkv, d = k.shape
+    assert off.size == sp.size + 1 and int(off[-1]) <= n
+    assert seg_state.dtype == np.float32 and seg_state.flags.c_contiguous
+    assert seg_state.shape == (sp.size, 2, hkv, 2)
+    hp = segment_scale_heads(hkv)
+    for arr in (k_scale, v_scale):
+        if arr is not None:
+            assert arr.dtype == np.float32 and arr.flags.c_contiguous
+            assert arr.shape == (k_cache.shape[0], hp)
+    return int(_load().or_kv_append_quant_segment(
+        _ptr(k), _ptr(v), _ptr(sm), _ptr(off), _ptr(sp), sp.size, hkv, d, fmt, _ptr(seg_state),
+        _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), k_cache.shape[0],
+        block_size))
 
 
 def kv_channel_scales(x, fmt: int) -> np.ndarray:

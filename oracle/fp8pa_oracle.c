@@ -43,6 +43,21 @@
  * [-127, 127] (an all-zero block takes e = -127); codes are the FP8 rounding
  * of x / X, saturated.
  *
+ * The segment mode is the block-wise cumulative rescaling of [P1] sec. 4.3:
+ * the cache is cut into length blocks of 1024 tokens, each block keeps a
+ * cumulative scale, and decode dequantises with the scale of the token's
+ * block.  The page gives no formula; the reading taken here is the plainest
+ * causal one.  Per (sequence, K or V, KV head) a running absmax R covers
+ * every token appended so far (it restarts at the sequence's position 0).
+ * When the token at position p is appended, R = max(R, absmax of its row);
+ * if p is a multiple of 1024 (the token opens segment p / 1024), that
+ * segment's scale is frozen as S = max(R / FMAX, 1e-12) (IEEE fp32
+ * division), so it is cumulative over all earlier segments and the opening
+ * token.  Every token of the segment is coded as x / S; values beyond S *
+ * FMAX saturate until the next segment raises S.  Since 1024 is a multiple
+ * of every supported block size, each page lies in one segment and stores
+ * S once per (page, KV head).
+ *
  * The INT8 codec is the alternate KV format the pages mention only as a
  * serving option ("--kv_cache_dtype int8", hotelren.com/news/5166672, the
  * section on inference-engine settings), with no scale or rounding rule.
@@ -68,6 +83,11 @@
 #define OR_SCALE_CHANNEL_STATIC 1
 #define OR_SCALE_TOKEN_GROUP 2
 #define OR_SCALE_MX_BLOCK 3
+#define OR_SCALE_SEGMENT 4
+
+/* Tokens per segment of the block-wise cumulative rescaling ([P1] sec. 4.3:
+ * the extra offset is refreshed every 1024 tokens). */
+#define OR_SEGMENT_TOKENS 1024
 
 /* ------------------------------------------------------------------ */
 /* FP8 formats: [P2] sec. 1.1, [P4] sec. 1.1, [P1] sec. 2.1.           */
@@ -360,6 +380,69 @@ void or_kv_channel_scales(const uint16_t* x, int num_tokens, int n_kv_heads, int
   free(amax);
 }
 
+/* Heads per page row of the segment scale array: n_kv_heads rounded up to a
+ * multiple of 4 (one 16-byte row per page). */
+static int or_seg_heads(int n_kv_heads) { return (n_kv_heads + 3) / 4 * 4; }
+
+/* Segment-scale append ([P1] sec. 4.3, read as in the header above).
+ * k, v: bf16 [num_tokens][Hkv][D] (v may be NULL); the tokens of sequence r
+ * are rows seq_offsets[r] .. seq_offsets[r+1]-1, at positions
+ * seq_start_pos[r], +1, ...  seg_state f32 [num_seqs][2][Hkv][2] carries
+ * (R, S) of every (sequence, K or V, head) between calls.  Scales:
+ * f32 [num_blocks][round_up(Hkv, 4)], the segment scale of each page.
+ * A token whose slot is negative or past the pool is skipped (it neither
+ * raises R nor opens its segment).  Returns the count of out-of-range
+ * slots. */
+int or_kv_append_quant_segment(const uint16_t* k, const uint16_t* v,
+                               const int32_t* slot_mapping, const int32_t* seq_offsets,
+                               const int32_t* seq_start_pos, int num_seqs, int n_kv_heads,
+                               int head_dim, int fmt, float* seg_state, uint8_t* k_cache,
+                               uint8_t* v_cache, float* k_scale, float* v_scale, int num_blocks,
+                               int block_size) {
+  int bad = 0;
+  const int hp = or_seg_heads(n_kv_heads);
+  volatile float fmax_f = (float)or_fp8_max(fmt);
+  float* x = (float*)malloc(sizeof(float) * (size_t)head_dim);
+  for (int r = 0; r < num_seqs; ++r) {
+    for (int which = 0; which < 2; ++which) {
+      const uint16_t* src = which == 0 ? k : v;
+      if (src == NULL) continue;
+      uint8_t* cache = which == 0 ? k_cache : v_cache;
+      float* sc = which == 0 ? k_scale : v_scale;
+      for (int h = 0; h < n_kv_heads; ++h) {
+        float* st = seg_state + (((long)r * 2 + which) * n_kv_heads + h) * 2;
+        float R = st[0], S = st[1];
+        for (int i = seq_offsets[r]; i < seq_offsets[r + 1]; ++i) {
+          const long p = (long)seq_start_pos[r] + (i - seq_offsets[r]);
+          if (p == 0) R = 0.0f; /* a new sequence */
+          const int slot = slot_mapping[i];
+          if (slot < 0) continue;
+          const long blk = slot / block_size, off = slot % block_size;
+          if (blk >= num_blocks) {
+            if (which == 0 && h == 0) ++bad;
+            continue;
+          }
+          const uint16_t* row = src + ((long)i * n_kv_heads + h) * head_dim;
+          float amax = 0.0f;
+          for (int d = 0; d < head_dim; ++d) {
+            x[d] = bf16_to_f32(row[d]);
+            amax = fmaxf(amax, fabsf(x[d]));
+          }
+          R = fmaxf(R, amax);
+          if (p % OR_SEGMENT_TOKENS == 0) S = fmaxf(R / fmax_f, 1e-12f);
+          uint8_t* dst = cache + (((long)blk * n_kv_heads + h) * block_size + off) * head_dim;
+          for (int d = 0; d < head_dim; ++d) dst[d] = or_fp8_encode(x[d] / S, fmt);
+          sc[blk * hp + h] = S;
+        }
+        st[0] = R;
+        st[1] = S;
+      }
+    }
+  }
+  free(x);
+  return bad;
+}
+
 /* ------------------------------------------------------------------ */
 /* Attention over the paged, dequantised cache in FP64                */
 /* ([P2] sec. 1.2 GQA, [P1] sec. 2.3 softmax, [P5] sec. 2.2 / 3.3).    */
@@ -398,6 +481,8 @@ static double or_deq(const or_attn_t* a, const uint8_t* cache, const float* sc, 
     s = (double)sc[row * (a->dk / a->gs) + d / a->gs];
   else if (a->mode == OR_SCALE_MX_BLOCK)
     s = ldexp(1.0, (int)((const uint8_t*)sc)[row * (a->dk / a->gs) + d / a->gs] - 127);
+  else if (a->mode == OR_SCALE_SEGMENT)
+    s = (double)sc[(long)blk * or_seg_heads(a->hkv) + g];
   else
     s = (double)sc[(long)g * a->dk + d];
   return code * s;
