@@ -121,12 +121,15 @@ def test_decode_bad_arguments_return_codes(F):
     assert F.get_device_error() == 0
 
 
-def _full_size_sampled(F, idx, sample):
-    """Full-size workload through the GPU path (prefill, step append and the
-    decode in the bench's launch configuration); the oracle rebuilds only the
-    sampled requests in a compact pool and checks their codes and outputs."""
-    from gpu_util import DEV, check_close, gpu_attention, to_dev_bf16
-    w = W.make_workload(idx, "full")
+def _full_size_sampled(F, w, sample, q_len=1):
+    """Full-size workload `w` through the GPU path in the bench's launch
+    configuration: every request's first L - q_len tokens are appended, then
+    one fp8pa_decode_step call appends the last q_len tokens of each request
+    and attends (a causal chunk when q_len > 1).  The oracle rebuilds only the
+    sampled requests in a compact pool and checks their codes, scales and
+    outputs (bf16, as the bench writes them)."""
+    from gpu_util import DEV, check_close, n_scale_groups, oracle_multiquery, scale_dtype, \
+        to_dev_bf16
     nb, hkv, bs, d = w.num_blocks, w.n_kv_heads, w.block_size, w.head_dim
     kc = torch.zeros((nb, hkv, bs, d), dtype=torch.uint8, device=DEV)
     vc = None if w.mla else torch.zeros_like(kc)
@@ -141,38 +144,43 @@ def _full_size_sampled(F, idx, sample):
         assert np.array_equal(vs.cpu().numpy().view(np.uint32), ovs.view(np.uint32))
         get = lambda b: allk[b]
     else:
-        ng = d // w.group_size if w.scale_mode == W.SCALE_TOKEN_GROUP else 1
-        ks = torch.zeros((nb, hkv, bs, ng), dtype=torch.float32, device=DEV)
+        ks = torch.zeros((nb, hkv, bs, n_scale_groups(w)), dtype=scale_dtype(w), device=DEV)
         vs = None if w.mla else torch.zeros_like(ks)
         get = lambda b: W.request_kv(w, b)
-    last_k, last_v = [], []
+    last_k, last_v, last_slots = [], [], []
     for b in range(w.batch):
         k, v = get(b)
         L = int(w.seq_lens[b])
+        n = max(L - q_len, 0)
         if b in sample:
             kv_sample[b] = (k, v)
-        if L > 1:
-            F.kv_append_quant(to_dev_bf16(k[:L - 1]), None if v is None else to_dev_bf16(v[:L - 1]),
-                              torch.from_numpy(W.token_slots(w, b, 0, L - 1)).to(DEV), kc, vc, ks,
+        if n > 0:
+            F.kv_append_quant(to_dev_bf16(k[:n]), None if v is None else to_dev_bf16(v[:n]),
+                              torch.from_numpy(W.token_slots(w, b, 0, n)).to(DEV), kc, vc, ks,
                               vs, fmt=w.fmt, scale_mode=w.scale_mode, group_size=w.group_size)
-        last_k.append(k[L - 1])
+        last_k.append(k[n:L])
         if v is not None:
-            last_v.append(v[L - 1])
-    F.kv_append_quant(to_dev_bf16(np.stack(last_k)), None if w.mla else to_dev_bf16(np.stack(last_v)),
-                      torch.from_numpy(W.step_slots(w)).to(DEV), kc, vc, ks, vs, fmt=w.fmt,
-                      scale_mode=w.scale_mode, group_size=w.group_size)
-    if w.mla:
-        vc, vs = kc, ks
-    q = W.queries(w)
-    got = gpu_attention(w, F, q, (kc, vc, ks, vs))
+            last_v.append(v[n:L])
+        last_slots.append(W.token_slots(w, b, n, L))
+    q = W.queries(w) if q_len == 1 else W.chunk_queries(w, q_len)
+    vc_, vs_ = (kc, ks) if w.mla else (vc, vs)
+    out = F.decode_step(to_dev_bf16(np.concatenate(last_k)),
+                        None if w.mla else to_dev_bf16(np.concatenate(last_v)),
+                        torch.from_numpy(np.concatenate(last_slots).astype(np.int32)).to(DEV),
+                        to_dev_bf16(q), kc, vc_, ks, vs_, torch.from_numpy(w.block_tables).to(DEV),
+                        torch.from_numpy(w.seq_lens).to(DEV), hkv, w.sm_scale, fmt=w.fmt,
+                        scale_mode=w.scale_mode, group_size=w.group_size,
+                        head_dim_v=w.head_dim_v)
+    got = out.float().cpu().numpy().astype(np.float64)
     assert F.get_device_error() == 0
     # Compact oracle pool holding only the sampled requests' blocks.
     for b in sample:
         k, v = kv_sample[b]
         L = int(w.seq_lens[b])
         nbl = (L + bs - 1) // bs
-        blocks = w.block_tables[b, :nbl].astype(np.int64)
-        cw = W.make_workload(idx, "full")
+        blocks = torch.from_numpy(w.block_tables[b, :nbl].astype(np.int64)).to(DEV)
+        cw = W.make_workload(w.index, "full")
+        cw.fmt, cw.scale_mode, cw.group_size = w.fmt, w.scale_mode, w.group_size
         cw.batch = 1
         cw.seq_lens = np.array([L], np.int32)
         cw.block_tables = np.arange(nbl, dtype=np.int32)[None]
@@ -182,46 +190,82 @@ def _full_size_sampled(F, idx, sample):
         if w.scale_mode == W.SCALE_CHANNEL_STATIC:
             oks2, ovs2 = oks, ovs
         else:
-            oks2 = np.zeros((nbl, hkv, bs, ks.shape[-1]), np.float32)
+            oks2 = np.zeros((nbl, hkv, bs, ks.shape[-1]), scale_dtype(w, torch_side=False))
             ovs2 = None if w.mla else np.zeros_like(oks2)
         slots = W.token_slots(cw, 0, 0, L)
         assert oracle.kv_append_quant(k, v, slots, w.fmt, w.scale_mode, w.group_size, okc, ovc,
                                       oks2, ovs2, bs) == 0
-        gk = kc[torch.from_numpy(blocks).to(DEV)].cpu().numpy()
-        assert np.array_equal(gk, okc), f"request {b}: K codes differ"
+        assert np.array_equal(kc[blocks].cpu().numpy(), okc), f"request {b}: K codes differ"
         if not w.mla:
-            assert np.array_equal(vc[torch.from_numpy(blocks).to(DEV)].cpu().numpy(), ovc)
+            assert np.array_equal(vc[blocks].cpu().numpy(), ovc), f"request {b}: V codes differ"
         if w.scale_mode != W.SCALE_CHANNEL_STATIC:
-            assert np.array_equal(ks[torch.from_numpy(blocks).to(DEV)].cpu().numpy().view(np.uint32),
-                                  oks2.view(np.uint32))
+            assert np.array_equal(ks[blocks].cpu().numpy().view(np.uint8),
+                                  oks2.view(np.uint8)), f"request {b}: K scales differ"
+            if not w.mla:
+                assert np.array_equal(vs[blocks].cpu().numpy().view(np.uint8),
+                                      ovs2.view(np.uint8)), f"request {b}: V scales differ"
         if w.mla:
             ovc, ovs2 = okc, oks2
-        ref = oracle.paged_decode_attention(q[b:b + 1], okc, ovc, oks2, ovs2, cw.block_tables,
-                                            cw.seq_lens, bs, hkv, w.head_dim_v, w.fmt,
-                                            w.scale_mode, w.group_size, w.sm_scale)
-        check_close(got[b:b + 1], ref, bf16_out=True, what=f"cfg{idx} request {b}")
+        if q_len == 1:
+            ref = oracle.paged_decode_attention(q[b:b + 1], okc, ovc, oks2, ovs2,
+                                                cw.block_tables, cw.seq_lens, bs, hkv,
+                                                w.head_dim_v, w.fmt, w.scale_mode, w.group_size,
+                                                w.sm_scale)
+        else:
+            ref = oracle_multiquery(cw, q[b:b + 1], (okc, ovc, oks2, ovs2), q_len)
+        check_close(got[b:b + 1], ref, bf16_out=True, what=f"{w.name} request {b}")
 
 
 @pytest.mark.slow
 def test_full_llama70b_layer_sampled(F):
-    _full_size_sampled(F, 2, sample=(0, 7, 11))
+    _full_size_sampled(F, W.make_workload(2, "full"), sample=(0, 7, 11))
 
 
 @pytest.mark.slow
 def test_full_long_context_sampled(F):
-    _full_size_sampled(F, 3, sample=(2,))
+    _full_size_sampled(F, W.make_workload(3, "full"), sample=(2,))
 
 
 @pytest.mark.slow
 def test_full_ragged_e5m2_sampled(F):
     w = W.make_workload(4, "full")
     order = np.argsort(w.seq_lens)
-    _full_size_sampled(F, 4, sample=(int(order[0]), int(order[len(order) // 2]), int(order[-1])))
+    _full_size_sampled(F, w, sample=(int(order[0]), int(order[len(order) // 2]),
+                                     int(order[-1])))
 
 
 @pytest.mark.slow
 def test_full_mla_latent_sampled(F):
-    _full_size_sampled(F, 5, sample=(0, 31))
+    _full_size_sampled(F, W.make_workload(5, "full"), sample=(0, 31))
+
+
+def _llama_variant(fmt=None, mode=None, gs=None, tag=""):
+    w = W.make_workload(2, "full")
+    if fmt is not None:
+        w.fmt = fmt
+    if mode is not None:
+        w.scale_mode, w.group_size = mode, gs
+    w.name += tag
+    return w
+
+
+@pytest.mark.slow
+def test_full_llama70b_layer_mx32_sampled(F):
+    """The bench's --mx-block 32 launch, checked on sampled requests."""
+    _full_size_sampled(F, _llama_variant(W.E4M3, W.SCALE_MX_BLOCK, 32, "_mx32"), sample=(0, 11))
+
+
+@pytest.mark.slow
+def test_full_llama70b_layer_int8_sampled(F):
+    """The bench's --kv-fmt int8 launch, checked on sampled requests."""
+    _full_size_sampled(F, _llama_variant(W.INT8, tag="_int8"), sample=(3, 11))
+
+
+@pytest.mark.slow
+def test_full_llama70b_layer_chunk4_sampled(F):
+    """The bench's --q-len 4 launch (a causal chunk of 4 queries per request,
+    its query warps sharing pages), checked on sampled requests."""
+    _full_size_sampled(F, _llama_variant(tag="_chunk4"), sample=(0, 5), q_len=4)
 
 
 def test_bounded_wait_gives_up_and_reports(F):
