@@ -11,10 +11,15 @@ the 129 MB L2, so no flush is needed between steps.
 
 Output: one JSON line (rank 0).  `value` is the achieved algorithmic HBM
 bandwidth of the step in GB/s; `roofline` is for the split kernel alone,
-timed with CUDA events around its launch; `e2e` is the same metric through
-the public API with pinned host inputs copied in and the output copied back
-inside the timed region; `cpu_baseline` times the CPU oracle on a bounded
-sample of the same workload.
+timed with CUDA events around its launch; `append_roofline` is the bulk
+(prefill) append of one request; `per_workload` repeats the split-kernel
+measurement on the other full-size workloads (long context, ragged E5M2,
+MLA latent); `e2e` is the same metric through the public API with pinned
+host inputs copied in and the output copied back inside the timed region
+(a replayed CUDA graph; `e2e_plain_call` the same with plain calls);
+`cpu_baseline` times the CPU oracle on a bounded sample of the same
+workload.  Working sets under 2 x L2 are flushed from L2 before every
+timed step.
 
 Multi-GPU (torchrun): replicas only -- every rank runs its own copy of the
 workload with no collective on the data path (weak scaling); the step time
@@ -52,6 +57,9 @@ def parse_args():
     ap.add_argument("--mx-block", type=int, default=0, choices=[0, 16, 32],
                     help="store the GQA workload's cache in the MX block-scaled mode "
                          "(one E8M0 exponent per block of this many dims)")
+    ap.add_argument("--scale-mode", choices=["segment"], default=None,
+                    help="store the GQA/MLA workload's cache with block-wise cumulative "
+                         "rescaling: one scale per (page, KV head), refreshed every 1024 tokens")
     ap.add_argument("--kv-fmt", choices=["e4m3", "e5m2", "int8"], default=None,
                     help="store the workload's cache in this code format instead of its own")
     ap.add_argument("--q-len", type=int, default=1,
@@ -59,6 +67,10 @@ def parse_args():
                          "request are appended, then attend); 1 is plain decode")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-per-workload", action="store_true",
+                    help="skip the split-kernel lines of the other full-size workloads")
+    ap.add_argument("--no-append-roofline", action="store_true",
+                    help="skip the bulk (prefill) append measurement")
     ap.add_argument("--traffic-json", default=os.path.join(ROOT, "profiles", "traffic.json"),
                     help="per-launch DRAM bytes of the split kernel from an ncu capture")
     return ap.parse_args()
@@ -84,14 +96,18 @@ def accounting(w: W.Workload, b_sel=None, q_len: int = 1) -> dict:
         sc_tok = 0
     static_sc = (4 * w.n_kv_heads * w.head_dim * ntens
                  if w.scale_mode == W.SCALE_CHANNEL_STATIC else 0)
-    kv = kv_tokens * (codes + sc_tok) + static_sc
+    pages = int(sum(math.ceil(int(L) / bs) for L in lens))
+    # segment mode: one f32 per (page, KV head) per tensor
+    seg_sc = 4 * w.n_kv_heads * ntens * pages if w.scale_mode == W.SCALE_SEGMENT else 0
+    kv = kv_tokens * (codes + sc_tok) + static_sc + seg_sc
     q = B * q_len * w.n_q_heads * w.head_dim * 2
     out = B * q_len * w.n_q_heads * w.head_dim_v * 2
-    pages = int(sum(math.ceil(int(L) / bs) for L in lens))
     tables = pages * 4 + B * 4
     split = kv + q + tables
     decode = split + out
     append = B * q_len * (codes * 2 + codes + sc_tok + 4)
+    if w.scale_mode == W.SCALE_SEGMENT:  # page-scale writes, state read and written
+        append += B * q_len * 4 * w.n_kv_heads * ntens + B * 2 * (2 * w.n_kv_heads * 2 * 4)
     return {"kv_tokens": kv_tokens, "bytes_per_token": codes + sc_tok, "split": split,
             "decode": decode, "append": append, "step": decode + append}
 
@@ -105,6 +121,11 @@ def bench_workload(args) -> W.Workload:
         if fmt != w.fmt:
             w.fmt = fmt
             w.name = f"{w.name}_{args.kv_fmt}"
+    if args.scale_mode == "segment":
+        if args.mx_block:
+            raise SystemExit("--scale-mode segment and --mx-block are exclusive")
+        w.scale_mode, w.group_size = W.SCALE_SEGMENT, w.head_dim
+        w.name = f"{w.name}_segment"
     if args.mx_block:
         if w.fmt == W.INT8:
             raise SystemExit("--mx-block needs FP8 codes")
@@ -243,6 +264,9 @@ def oracle_sample(w: W.Workload, b: int, heads=None, threads=None):
     if w.scale_mode == W.SCALE_CHANNEL_STATIC:
         ks = oracle.kv_channel_scales(k, w.fmt)
         vs = oracle.kv_channel_scales(v, w.fmt)
+    elif w.scale_mode == W.SCALE_SEGMENT:
+        ks = np.zeros((nbl, oracle.segment_scale_heads(hkv)), np.float32)
+        vs = None if w.mla else np.zeros_like(ks)
     else:
         ks = np.zeros((nbl, hkv, bs, ng),
                       np.uint8 if w.scale_mode == W.SCALE_MX_BLOCK else np.float32)
@@ -254,7 +278,12 @@ def oracle_sample(w: W.Workload, b: int, heads=None, threads=None):
     q = W.queries(w)[b:b + 1]
     heads = list(range(w.n_q_heads)) if heads is None else list(heads)
     t0 = time.perf_counter()
-    oracle.kv_append_quant(k, v, slots, w.fmt, w.scale_mode, w.group_size, kc, vc, ks, vs, bs)
+    if w.scale_mode == W.SCALE_SEGMENT:
+        st = np.zeros((1, 2, hkv, 2), np.float32)
+        oracle.kv_append_quant_segment(k, v, slots, [0, L], [0], w.fmt, st, kc, vc, ks, vs, bs)
+    else:
+        oracle.kv_append_quant(k, v, slots, w.fmt, w.scale_mode, w.group_size, kc, vc, ks, vs,
+                               bs)
     if w.mla:
         vc, vs = kc, ks
     oracle.paged_decode_attention(q, kc, vc, ks, vs, bt, sl, bs, hkv, w.head_dim_v, w.fmt,
@@ -301,6 +330,262 @@ def run_reference(args, rank):
 
 
 # ---------------------------------------------------------------- GPU arm
+L2_BYTES = 129 * 10**6          # GB300 L2 (129 MB)
+FLUSH_BYTES = 320 * 2**20       # > 2 x L2: written between timed launches when needed
+
+
+def needs_flush(split_bytes: int) -> bool:
+    """Working sets under ~2 x L2 are flushed between timed launches, so that
+    every launch reads its cache from DRAM."""
+    return split_bytes < 2 * L2_BYTES
+
+
+class Case:
+    """One workload made resident on the device: the cache prefilled through
+    the library with every request's first L - q_len tokens, and the step's
+    inputs (the last q_len tokens of each request, the queries)."""
+
+    def __init__(self, F, w, ql, dev):
+        import torch
+        self.F, self.w, self.ql, self.dev = F, w, ql, dev
+        nb, hkv, bs, d = w.num_blocks, w.n_kv_heads, w.block_size, w.head_dim
+        ng = scale_groups(w)
+        self.acc = accounting(w, q_len=ql)
+        kc = torch.zeros((nb, hkv, bs, d), dtype=torch.uint8, device=dev)
+        vc = None if w.mla else torch.zeros_like(kc)
+        last_k, last_v = [], []
+        self.seg_state = None
+        if w.scale_mode == W.SCALE_CHANNEL_STATIC:
+            kvs = [W.request_kv(w, b) for b in range(w.batch)]
+            ks = F.kv_channel_scales(to_bf16_tensor(np.concatenate([k for k, _ in kvs]), dev),
+                                     w.fmt)
+            vs = F.kv_channel_scales(to_bf16_tensor(np.concatenate([v for _, v in kvs]), dev),
+                                     w.fmt)
+            get = lambda b: kvs[b]
+        elif w.scale_mode == W.SCALE_SEGMENT:
+            ks = torch.zeros((nb, F.segment_scale_heads(hkv)), dtype=torch.float32, device=dev)
+            vs = None if w.mla else torch.zeros_like(ks)
+            self.seg_state = torch.zeros((w.batch, 2, hkv, 2), dtype=torch.float32, device=dev)
+            get = lambda b: W.request_kv(w, b)
+        else:
+            sdt = torch.uint8 if w.scale_mode == W.SCALE_MX_BLOCK else torch.float32
+            ks = torch.zeros((nb, hkv, bs, ng), dtype=sdt, device=dev)
+            vs = None if w.mla else torch.zeros_like(ks)
+            get = lambda b: W.request_kv(w, b)
+        self.prefill0 = None  # request 0's prefill rows (the bulk-append measurement)
+        for b in range(w.batch):
+            k, v = get(b)
+            L = int(w.seq_lens[b])
+            if L > ql:
+                kd = to_bf16_tensor(k[:L - ql], dev)
+                vd = None if v is None else to_bf16_tensor(v[:L - ql], dev)
+                sd = torch.from_numpy(W.token_slots(w, b, 0, L - ql)).to(dev)
+                if self.seg_state is not None:
+                    F.kv_append_quant_segment(
+                        kd, vd, sd, torch.tensor([0, L - ql], dtype=torch.int32, device=dev),
+                        torch.zeros(1, dtype=torch.int32, device=dev), kc, vc, ks, vs,
+                        self.seg_state[b:b + 1], fmt=w.fmt)
+                else:
+                    F.kv_append_quant(kd, vd, sd, kc, vc, ks, vs, fmt=w.fmt,
+                                      scale_mode=w.scale_mode, group_size=w.group_size)
+                if b == 0:
+                    self.prefill0 = (kd, vd, sd)
+            last_k.append(k[L - ql:L])
+            if v is not None:
+                last_v.append(v[L - ql:L])
+        self.kc, self.vc, self.ks, self.vs = kc, vc, ks, vs
+        self.vc_, self.vs_ = (kc, ks) if w.mla else (vc, vs)
+        # step inputs, resident
+        self.q_h = W.queries(w) if ql == 1 else W.chunk_queries(w, ql)
+        self.kn_h = np.concatenate(last_k)
+        self.vn_h = None if w.mla else np.concatenate(last_v)
+        self.slot_h = np.concatenate([W.token_slots(w, b, int(w.seq_lens[b]) - ql,
+                                                    int(w.seq_lens[b]))
+                                      for b in range(w.batch)]).astype(np.int32)
+        self.q = to_bf16_tensor(self.q_h, dev)
+        self.kn = to_bf16_tensor(self.kn_h, dev)
+        self.vn = None if w.mla else to_bf16_tensor(self.vn_h, dev)
+        self.slots = torch.from_numpy(self.slot_h).to(dev)
+        self.bt = torch.from_numpy(w.block_tables).to(dev)
+        self.sl = torch.from_numpy(w.seq_lens).to(dev)
+        oshape = (w.batch, w.n_q_heads, w.head_dim_v) if ql == 1 else \
+            (w.batch, ql, w.n_q_heads, w.head_dim_v)
+        self.out = torch.empty(oshape, dtype=torch.bfloat16, device=dev)
+        self.ws = torch.empty(F.decode_workspace_bytes(w.batch, w.n_q_heads, hkv, d, w.head_dim_v,
+                                                       bs, w.max_blocks, dev, q_len=ql),
+                              dtype=torch.uint8, device=dev)
+        if self.seg_state is not None:  # the step's varlen description
+            self.seg_off = torch.arange(0, (w.batch + 1) * ql, ql, dtype=torch.int32, device=dev)
+            self.seg_start = torch.from_numpy(w.seq_lens - ql).to(dev)
+
+    def step(self, q=None, kn=None, vn=None, slots=None, sl=None):
+        """One fp8pa_decode_step call: append (the split planner in the same
+        launch), split kernel, merge.  The segment mode appends through its
+        own call (it needs positions), then attends."""
+        w = self.w
+        if self.seg_state is not None:
+            self.F.kv_append_quant_segment(self.kn if kn is None else kn,
+                                           self.vn if vn is None else vn,
+                                           self.slots if slots is None else slots, self.seg_off,
+                                           self.seg_start, self.kc, self.vc, self.ks, self.vs,
+                                           self.seg_state, fmt=w.fmt)
+            attend = (self.F.paged_decode_attention if self.ql == 1
+                      else self.F.paged_multiquery_attention)
+            attend(self.q if q is None else q, self.kc, self.vc_, self.ks, self.vs_, self.bt,
+                   self.sl if sl is None else sl, w.n_kv_heads, w.sm_scale, fmt=w.fmt,
+                   scale_mode=w.scale_mode, group_size=w.group_size, head_dim_v=w.head_dim_v,
+                   out=self.out, workspace=self.ws)
+            return
+        self.F.decode_step(self.kn if kn is None else kn, self.vn if vn is None else vn,
+                           self.slots if slots is None else slots, self.q if q is None else q,
+                           self.kc, self.vc_, self.ks, self.vs_, self.bt,
+                           self.sl if sl is None else sl, w.n_kv_heads, w.sm_scale, fmt=w.fmt,
+                           scale_mode=w.scale_mode, group_size=w.group_size,
+                           head_dim_v=w.head_dim_v, out=self.out, workspace=self.ws)
+
+
+def time_steps(case, steps, flush_buf, barrier):
+    """Device time of `steps` decode steps (ms, the whole region), and of the
+    split kernel inside each (ms per launch, CUDA events the library records
+    on the call's stream around that launch).  With `flush_buf`, L2 is
+    flushed before every step, outside the timed events."""
+    import ctypes
+    import torch
+    from fp8_quantised_paged_gb300 import _native as N
+    E = lambda: torch.cuda.Event(enable_timing=True)
+    ev = [(E(), E()) for _ in range(steps)]
+    for a, b_ in ev:  # materialise the event handles
+        a.record()
+        b_.record()
+    torch.cuda.synchronize()
+    if flush_buf is None:
+        # Timed region 1: the steps back to back, nothing between launches.
+        t0, t1 = E(), E()
+        barrier()
+        torch.cuda.synchronize()
+        t0.record()
+        for _ in range(steps):
+            case.step()
+        t1.record()
+        torch.cuda.synchronize()
+        barrier()
+        ms_total = t0.elapsed_time(t1)
+    else:
+        st = [(E(), E()) for _ in range(steps)]
+        barrier()
+        torch.cuda.synchronize()
+        for a, b_ in st:
+            flush_buf.zero_()
+            a.record()
+            case.step()
+            b_.record()
+        torch.cuda.synchronize()
+        barrier()
+        ms_total = sum(a.elapsed_time(b_) for a, b_ in st)
+    # Timed region 2: the same steps with the split launch bracketed.
+    torch.cuda.synchronize()
+    for i in range(steps):
+        if flush_buf is not None:
+            flush_buf.zero_()
+        N.check(N.lib.fp8pa_set_split_events(ctypes.c_void_p(ev[i][0].cuda_event),
+                                             ctypes.c_void_p(ev[i][1].cuda_event)), "events")
+        case.step()
+    torch.cuda.synchronize()
+    N.check(N.lib.fp8pa_set_split_events(None, None), "events")
+    return ms_total, [a.elapsed_time(b_) for a, b_ in ev]
+
+
+def split_roofline(w, acc, split_avg_ms, pk, traffic_json):
+    kname = "mla_split_kernel" if w.mla else "gqa_split_kernel"
+    src = "decode_mla.cu" if w.mla else "decode_gqa.cu"
+    traffic = traffic_per_launch(traffic_json, w.name, src)
+    if w.mla:
+        # a dense contraction: tensor-bound; f16 MMA against the measured
+        # dense bf16 rate (same nominal rate as f16)
+        fl = flops_per_step(w)
+        achieved = fl / (split_avg_ms * 1e-3) / 1e12
+        return {"kernel": kname, "bound": "tensor", "achieved": achieved,
+                "peak": pk["bf16_tflops"], "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"],
+                "traffic": traffic, "algorithmic_flops_per_launch": fl,
+                "algorithmic_bytes_per_launch": acc["split"],
+                "hbm_gbs_of_launch": acc["split"] / (split_avg_ms * 1e-3) / 1e9,
+                "hbm_frac_of_launch": acc["split"] / (split_avg_ms * 1e-3) / 1e9 / pk["hbm_gbs"],
+                "avg_launch_ms": split_avg_ms,
+                "peak_source": pk["source"] + " (MEASURED_PEAKS.json bf16_tflops, burst)"}
+    achieved = acc["split"] / (split_avg_ms * 1e-3) / 1e9
+    return {"kernel": kname, "bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"],
+            "unit": "GB/s", "frac": achieved / pk["hbm_gbs"], "traffic": traffic,
+            "algorithmic_bytes_per_launch": acc["split"], "avg_launch_ms": split_avg_ms,
+            "peak_source": pk["source"] + " (MEASURED_PEAKS.json hbm_gbs, copy bandwidth)"}
+
+
+def append_roofline(case, launches, pk, traffic_json):
+    """The bulk (prefill) append: request 0's first L - q_len tokens appended
+    again (same slots, same values) `launches` times back to back from a CUDA
+    graph, timed with CUDA events around the replay.  Algorithmic bytes = bf16 rows read + codes and scales
+    written + slots read."""
+    import torch
+    w, F = case.w, case.F
+    if case.prefill0 is None or case.seg_state is not None:
+        return None
+    kd, vd, sd = case.prefill0
+    n = int(sd.numel())
+    ntens = 1 if w.mla else 2
+    per_row = w.head_dim * 2 + w.head_dim  # bf16 in, codes out
+    if w.scale_mode == W.SCALE_TOKEN_HEAD:
+        per_row += 4
+    elif w.scale_mode == W.SCALE_TOKEN_GROUP:
+        per_row += 4 * (w.head_dim // w.group_size)
+    elif w.scale_mode == W.SCALE_MX_BLOCK:
+        per_row += w.head_dim // w.group_size
+    nbytes = n * ntens * w.n_kv_heads * per_row + 4 * n
+    def call():
+        F.kv_append_quant(kd, vd, sd, case.kc, case.vc, case.ks, case.vs, fmt=w.fmt,
+                          scale_mode=w.scale_mode, group_size=w.group_size)
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize()
+    # The calls are captured once in a CUDA graph and replayed, so the launches
+    # run back to back on the device and the events time the kernels, not the
+    # host's per-call overhead (which is longer than one launch here).
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        call()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for _ in range(launches):
+            call()
+    graph.replay()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    graph.replay()
+    t1.record()
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1) / launches
+    del graph
+    achieved = nbytes / (ms * 1e-3) / 1e9
+    try:
+        with open(traffic_json) as f:
+            t = json.load(f).get("append:" + w.name)
+        traffic = (float(t["dram_bytes_per_launch"])
+                   if t and t.get("kernel_source_sha256") == kernel_source_sha("append.cu")
+                   else None)
+    except (OSError, ValueError, KeyError, TypeError):
+        traffic = None
+    return {"kernel": "append_kernel", "bound": "hbm", "achieved": achieved,
+            "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": achieved / pk["hbm_gbs"],
+            "traffic": traffic, "algorithmic_bytes_per_launch": nbytes, "avg_launch_ms": ms,
+            "tokens": n, "launches": launches,
+            "what": f"bulk prefill append of request 0: {n} tokens x {w.n_kv_heads} KV heads x "
+                    f"{ntens} tensor(s), bf16 in, {w.describe()['kv_fmt']} codes + scales out",
+            "peak_source": pk["source"] + " (MEASURED_PEAKS.json hbm_gbs, copy bandwidth)"}
+
+
 def run_gpu(args, rank, world, local_rank):
     import torch
     import torch.distributed as dist
@@ -312,125 +597,39 @@ def run_gpu(args, rank, world, local_rank):
     ql = args.q_len
     if ql > 1:
         args.no_cpu_baseline = True  # the oracle sample is a one-query decode
-    acc = accounting(w, q_len=ql)
-    nb, hkv, bs, d = w.num_blocks, w.n_kv_heads, w.block_size, w.head_dim
-    ntens = 1 if w.mla else 2
-    ng = scale_groups(w)
-
-    # ---- cache: prefill every request's first L - q_len tokens through the library
-    kc = torch.zeros((nb, hkv, bs, d), dtype=torch.uint8, device=dev)
-    vc = None if w.mla else torch.zeros_like(kc)
-    last_k, last_v = [], []
-    if w.scale_mode == W.SCALE_CHANNEL_STATIC:
-        kvs = [W.request_kv(w, b) for b in range(w.batch)]
-        ks = F.kv_channel_scales(to_bf16_tensor(np.concatenate([k for k, _ in kvs]), dev), w.fmt)
-        vs = F.kv_channel_scales(to_bf16_tensor(np.concatenate([v for _, v in kvs]), dev), w.fmt)
-        get = lambda b: kvs[b]
-    else:
-        sdt = torch.uint8 if w.scale_mode == W.SCALE_MX_BLOCK else torch.float32
-        ks = torch.zeros((nb, hkv, bs, ng), dtype=sdt, device=dev)
-        vs = None if w.mla else torch.zeros_like(ks)
-        get = lambda b: W.request_kv(w, b)
-    for b in range(w.batch):
-        k, v = get(b)
-        L = int(w.seq_lens[b])
-        if L > ql:
-            F.kv_append_quant(to_bf16_tensor(k[:L - ql], dev),
-                              None if v is None else to_bf16_tensor(v[:L - ql], dev),
-                              torch.from_numpy(W.token_slots(w, b, 0, L - ql)).to(dev), kc, vc,
-                              ks, vs, fmt=w.fmt, scale_mode=w.scale_mode,
-                              group_size=w.group_size)
-        last_k.append(k[L - ql:L])
-        if v is not None:
-            last_v.append(v[L - ql:L])
-    if w.mla:
-        vc_, vs_ = kc, ks
-    else:
-        vc_, vs_ = vc, vs
-
-    # ---- step inputs, resident
-    q_h = W.queries(w) if ql == 1 else W.chunk_queries(w, ql)
-    kn_h = np.concatenate(last_k)
-    vn_h = None if w.mla else np.concatenate(last_v)
-    slot_h = np.concatenate([W.token_slots(w, b, int(w.seq_lens[b]) - ql, int(w.seq_lens[b]))
-                             for b in range(w.batch)]).astype(np.int32)
-    q = to_bf16_tensor(q_h, dev)
-    kn = to_bf16_tensor(kn_h, dev)
-    vn = None if w.mla else to_bf16_tensor(vn_h, dev)
-    slots = torch.from_numpy(slot_h).to(dev)
-    bt = torch.from_numpy(w.block_tables).to(dev)
-    sl = torch.from_numpy(w.seq_lens).to(dev)
-    oshape = (w.batch, w.n_q_heads, w.head_dim_v) if ql == 1 else \
-        (w.batch, ql, w.n_q_heads, w.head_dim_v)
-    out = torch.empty(oshape, dtype=torch.bfloat16, device=dev)
-    ws = torch.empty(F.decode_workspace_bytes(w.batch, w.n_q_heads, hkv, d, w.head_dim_v, bs,
-                                              w.max_blocks, dev, q_len=ql),
-                     dtype=torch.uint8, device=dev)
-
-    def step(q_, kn_, vn_, slots_, sl_):
-        # one call: append (with the split planner in the same launch),
-        # split kernel, merge
-        F.decode_step(kn_, vn_, slots_, q_, kc, vc_, ks, vs_, bt, sl_, hkv, w.sm_scale,
-                      fmt=w.fmt, scale_mode=w.scale_mode, group_size=w.group_size,
-                      head_dim_v=w.head_dim_v, out=out, workspace=ws)
+    pk = peaks()
+    case = Case(F, w, ql, dev)
+    acc = case.acc
+    flush = needs_flush(acc["split"])
+    flush_buf = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev) if flush else None
 
     def barrier():
         if world > 1:
             dist.barrier()
 
     for _ in range(args.warmup):
-        step(q, kn, vn, slots, sl)
+        case.step()
     torch.cuda.synchronize()
     assert F.get_device_error() == 0, "device error during warm-up"
 
-    # ---- timed region (device-resident inputs)
-    from fp8_quantised_paged_gb300 import _native as N
-    import ctypes
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
-    for a, b_ in ev:  # materialise the event handles
-        a.record()
-        b_.record()
-    torch.cuda.synchronize()
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_stop = torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local_rank)
     clocks.start()
     time.sleep(0.3)
-    # Timed region 1: the step, nothing between its launches.
-    barrier()
-    torch.cuda.synchronize()
-    t_start.record()
-    for i in range(args.steps):
-        step(q, kn, vn, slots, sl)
-    t_stop.record()
-    torch.cuda.synchronize()
-    barrier()
-    ms_total = t_start.elapsed_time(t_stop)
-    # Timed region 2: the same steps with the library recording an event
-    # pair around each split-kernel launch (for the roofline of that kernel).
-    torch.cuda.synchronize()
-    for i in range(args.steps):
-        N.check(N.lib.fp8pa_set_split_events(ctypes.c_void_p(ev[i][0].cuda_event),
-                                             ctypes.c_void_p(ev[i][1].cuda_event)), "events")
-        step(q, kn, vn, slots, sl)
-    torch.cuda.synchronize()
-    N.check(N.lib.fp8pa_set_split_events(None, None), "events")
+    ms_total, split_ms = time_steps(case, args.steps, flush_buf, barrier)
     clk = clocks.stop()
-    split_ms = [a.elapsed_time(b_) for a, b_ in ev]
     ms_total = max_over_ranks(ms_total, dev)
     ms_step = ms_total / args.steps
     assert F.get_device_error() == 0, "device error during the timed region"
 
     # ---- end to end through the public API with pinned host buffers
-    e2e = None
+    e2e = e2e_plain = None
     if not args.no_e2e:
         # The step's inputs (q, new K/V rows, slots, lengths) are staged in
         # one pinned host buffer and copied in one transfer to a device
         # buffer holding the same layout, as a serving loop would.
-        parts = [q_h.view(np.uint8).reshape(-1), kn_h.view(np.uint8).reshape(-1),
-                 None if w.mla else vn_h.view(np.uint8).reshape(-1),
-                 slot_h.view(np.uint8).reshape(-1), w.seq_lens.view(np.uint8).reshape(-1)]
+        parts = [case.q_h.view(np.uint8).reshape(-1), case.kn_h.view(np.uint8).reshape(-1),
+                 None if w.mla else case.vn_h.view(np.uint8).reshape(-1),
+                 case.slot_h.view(np.uint8).reshape(-1), w.seq_lens.view(np.uint8).reshape(-1)]
         offs, total = [], 0
         for a in parts:
             offs.append(total)
@@ -445,22 +644,38 @@ def run_gpu(args, rank, world, local_rank):
         def dview(k, dtype, shape):
             n = int(np.prod(shape)) * torch.tensor([], dtype=dtype).element_size()
             return dbuf[offs[k]:offs[k] + n].view(dtype).view(shape)
-        qd = dview(0, torch.bfloat16, q.shape)
-        knd = dview(1, torch.bfloat16, kn.shape)
-        vnd = None if w.mla else dview(2, torch.bfloat16, vn.shape)
-        slotd = dview(3, torch.int32, slots.shape)
-        sld = dview(4, torch.int32, sl.shape)
-        out_p = torch.empty(out.shape, dtype=torch.bfloat16).pin_memory()
+        qd = dview(0, torch.bfloat16, case.q.shape)
+        knd = dview(1, torch.bfloat16, case.kn.shape)
+        vnd = None if w.mla else dview(2, torch.bfloat16, case.vn.shape)
+        slotd = dview(3, torch.int32, case.slots.shape)
+        sld = dview(4, torch.int32, case.sl.shape)
+        out_p = torch.empty(case.out.shape, dtype=torch.bfloat16).pin_memory()
         h2d = total
         d2h = out_p.numel() * 2
 
         def e2e_body():
             dbuf.copy_(host, non_blocking=True)
-            step(qd, knd, vnd, slotd, sld)
-            out_p.copy_(out, non_blocking=True)
+            case.step(qd, knd, vnd, slotd, sld)
+            out_p.copy_(case.out, non_blocking=True)
 
-        # A serving loop captures the fixed-shape step once (input copy, the
-        # fp8pa_decode_step call, output copy) and replays it every step.
+        def timed(fn):
+            for _ in range(args.warmup):
+                fn()
+            barrier()
+            t0 = time.perf_counter()
+            for _ in range(args.steps):
+                fn()
+            return max_over_ranks((time.perf_counter() - t0) / args.steps, dev)
+
+        # (1) plain calls: every step is the copy in, the fp8pa_decode_step
+        # call (host-side validation, tensor maps, launches) and the copy out,
+        # then a host synchronisation.
+        def plain_step():
+            e2e_body()
+            torch.cuda.current_stream().synchronize()
+        s_plain = timed(plain_step)
+        # (2) a serving loop with fixed shapes captures the same sequence once
+        # in a CUDA graph and replays it every step.
         side = torch.cuda.Stream()
         side.wait_stream(torch.cuda.current_stream())
         with torch.cuda.stream(side):
@@ -471,50 +686,65 @@ def run_gpu(args, rank, world, local_rank):
         with torch.cuda.graph(graph):
             e2e_body()
 
-        def e2e_step():
+        def graph_step():
             graph.replay()
             torch.cuda.current_stream().synchronize()
-
-        for _ in range(args.warmup):
-            e2e_step()
-        barrier()
-        t0 = time.perf_counter()
-        for _ in range(args.steps):
-            e2e_step()
-        e2e_s = (time.perf_counter() - t0) / args.steps
-        e2e_s = max_over_ranks(e2e_s, dev)
-        e2e = {"value": world * acc["step"] / e2e_s / 1e9, "unit": "GB/s",
-               "ms_per_step": e2e_s * 1e3, "h2d_bytes_per_step": int(h2d),
+        s_graph = timed(graph_step)
+        e2e = {"value": world * acc["step"] / s_graph / 1e9, "unit": "GB/s",
+               "ms_per_step": s_graph * 1e3, "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(d2h),
                "how": "CUDA graph of one pinned H2D copy, fp8pa_decode_step and one D2H copy "
                       "into pinned memory, replayed and host-synchronised every step"}
+        e2e_plain = {"value": world * acc["step"] / s_plain / 1e9, "unit": "GB/s",
+                     "ms_per_step": s_plain * 1e3, "h2d_bytes_per_step": int(h2d),
+                     "d2h_bytes_per_step": int(d2h),
+                     "how": "plain calls: pinned H2D copy, fp8pa_decode_step through the Python "
+                            "binding (validation, tensor maps, launches), D2H copy, host "
+                            "synchronisation, every step"}
+        assert F.get_device_error() == 0, "device error in the e2e runs"
+
+    app = None if args.no_append_roofline else append_roofline(case, min(args.steps, 50), pk,
+                                                                args.traffic_json)
+    split_avg_ms = statistics.mean(split_ms)
+    roof = split_roofline(w, acc, split_avg_ms, pk, args.traffic_json)
+    del case
+    flush_buf = None
+    torch.cuda.empty_cache()
+
+    # ---- the other workloads (each timed the same way, split kernel alone)
+    per_workload = None
+    if (not args.no_per_workload and ql == 1 and not args.mx_block and args.kv_fmt is None
+            and args.scale_mode is None):
+        per_workload = {}
+        for idx in (3, 4, 5):
+            if idx == args.workload:
+                continue
+            wi = W.make_workload(idx, "full")
+            ci = Case(F, wi, 1, dev)
+            fb = (torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+                  if needs_flush(ci.acc["split"]) else None)
+            for _ in range(max(3, min(args.warmup, 5))):
+                ci.step()
+            torch.cuda.synchronize()
+            n = max(5, min(args.steps, 20))
+            tot, sp = time_steps(ci, n, fb, barrier)
+            assert F.get_device_error() == 0, f"device error in workload {idx}"
+            r = split_roofline(wi, ci.acc, statistics.mean(sp), pk, args.traffic_json)
+            per_workload[wi.name] = {
+                "config": dict(wi.describe(),
+                               l2=("flushed (a 320 MiB write) before every step"
+                                   if fb is not None else "no flush: cache larger than 2 x L2")),
+                "steps": n, "ms_per_step": tot / n,
+                "value": ci.acc["step"] / (tot / n * 1e-3) / 1e9, "unit": "GB/s",
+                "kv_tokens_per_s": ci.acc["kv_tokens"] / (tot / n * 1e-3),
+                "roofline": r}
+            del ci, fb
+            torch.cuda.empty_cache()
 
     if rank != 0:
         return
-    pk = peaks()
-    split_avg_ms = statistics.mean(split_ms)
-    kname = "mla_split_kernel" if w.mla else "gqa_split_kernel"
-    src = "decode_mla.cu" if w.mla else "decode_gqa.cu"
-    traffic = traffic_per_launch(args.traffic_json, w.name, src)
-    if w.mla:
-        # a dense contraction: tensor-bound; f16 MMA against the measured
-        # dense bf16 rate (same nominal rate as f16)
-        fl = flops_per_step(w)
-        achieved = fl / (split_avg_ms * 1e-3) / 1e12
-        roof = {"kernel": kname, "bound": "tensor", "achieved": achieved,
-                "peak": pk["bf16_tflops"], "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"],
-                "traffic": traffic, "algorithmic_flops_per_launch": fl,
-                "algorithmic_bytes_per_launch": acc["split"],
-                "hbm_gbs_of_launch": acc["split"] / (split_avg_ms * 1e-3) / 1e9,
-                "avg_launch_ms": split_avg_ms,
-                "peak_source": pk["source"] + " (MEASURED_PEAKS.json bf16_tflops, burst)"}
-    else:
-        achieved = acc["split"] / (split_avg_ms * 1e-3) / 1e9
-        roof = {"kernel": kname, "bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"],
-                "unit": "GB/s", "frac": achieved / pk["hbm_gbs"], "traffic": traffic,
-                "algorithmic_bytes_per_launch": acc["split"], "avg_launch_ms": split_avg_ms,
-                "peak_source": pk["source"] + " (MEASURED_PEAKS.json hbm_gbs, copy bandwidth)"}
     value = world * acc["step"] / (ms_step * 1e-3) / 1e9
+    kname = roof["kernel"]
     line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
@@ -526,16 +756,27 @@ def run_gpu(args, rank, world, local_rank):
                            compute=("int8" if w.fmt == W.INT8 else "fp8")
                            + " codes -> exact f16, warp MMA (m16n8k16), f32 accumulate "
                              "and softmax",
-                           l2="no flush: every step reads the whole cache, larger than L2",
-                           step=f"fp8pa_decode_step: append ({ql} token(s)/request) and plan, "
-                                "split, merge",
+                           l2=("flushed (a 320 MiB write) before every step, outside the timed "
+                               "events" if flush else
+                               "no flush: every step reads the whole cache, larger than 2 x L2"),
+                           step=(f"fp8pa_kv_append_quant_segment ({ql} token(s)/request), "
+                                 "then attention: plan, split, merge"
+                                 if w.scale_mode == W.SCALE_SEGMENT else
+                                 f"fp8pa_decode_step: append ({ql} token(s)/request) and plan, "
+                                 "split, merge"),
                            q_len=ql,
                            bytes_per_step=acc["step"]),
             "roofline": roof,
-            "gpu_launches": 3 * args.steps,
-            "gpu_launches_per_step": {"append_plan_kernel": 1, kname: 1, "merge_kernel": 1},
+            "append_roofline": app,
+            "per_workload": per_workload,
+            "gpu_launches": (4 if w.scale_mode == W.SCALE_SEGMENT else 3) * args.steps,
+            "gpu_launches_per_step": (
+                {"segment_append_kernel": 1, "plan_kernel": 1, kname: 1, "merge_kernel": 1}
+                if w.scale_mode == W.SCALE_SEGMENT else
+                {"append_plan_kernel": 1, kname: 1, "merge_kernel": 1}),
             "clocks": clk,
-            "e2e": e2e}
+            "e2e": e2e,
+            "e2e_plain_call": e2e_plain}
     if not args.no_cpu_baseline:
         import oracle
         threads = oracle.max_threads()

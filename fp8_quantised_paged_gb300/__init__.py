@@ -14,12 +14,13 @@ on first use, so that importing the input generators (:mod:`.workloads`)
 does not need the native library.  Using any wrapper loads ``libfp8pa.so``
 and raises if it is missing: there is no fallback path.
 """
-_API = ("kv_append_quant", "kv_channel_scales", "kv_channel_absmax_update",
+_API = ("kv_append_quant", "kv_append_quant_segment", "segment_scale_heads",
+        "kv_channel_scales", "kv_channel_absmax_update",
         "kv_scales_from_absmax", "paged_decode_attention", "paged_multiquery_attention",
         "decode_step",
         "decode_workspace_bytes", "get_device_error", "set_decode_workers", "version",
         "E4M3", "E5M2", "INT8", "SCALE_TOKEN_HEAD", "SCALE_CHANNEL_STATIC", "SCALE_TOKEN_GROUP",
-        "SCALE_MX_BLOCK",
+        "SCALE_MX_BLOCK", "SCALE_SEGMENT", "SEGMENT_TOKENS",
         "OUT_BF16", "OUT_F32", "Fp8paError")
 
 __all__ = list(_API)

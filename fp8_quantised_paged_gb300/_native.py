@@ -19,6 +19,8 @@ ERR_WORKSPACE, ERR_ALIGNMENT, ERR_CUDA = -5, -6, -7
 DEVERR_SLOT_RANGE, DEVERR_BLOCK_RANGE, DEVERR_SEQ_LEN, DEVERR_TIMEOUT = 1, 2, 4, 8
 E4M3, E5M2, INT8 = 0, 1, 2
 SCALE_TOKEN_HEAD, SCALE_CHANNEL_STATIC, SCALE_TOKEN_GROUP, SCALE_MX_BLOCK = 0, 1, 2, 3
+SCALE_SEGMENT = 4
+SEGMENT_TOKENS = 1024
 OUT_BF16, OUT_F32 = 0, 1
 
 # Every symbol the header declares, with (restype, argtypes).
@@ -27,6 +29,8 @@ _I = ctypes.c_int
 _SIGS = {
     "fp8pa_kv_append_quant": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _I, _I,
                                    _P]),
+    "fp8pa_kv_append_quant_segment": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P,
+                                           _P, _I, _I, _P]),
     "fp8pa_kv_channel_scales": (_I, [_P, _I, _I, _I, _I, _P, _P]),
     "fp8pa_kv_channel_absmax_update": (_I, [_P, _I, _I, _I, _P, _P]),
     "fp8pa_kv_scales_from_absmax": (_I, [_P, _I, _I, _P, _P]),

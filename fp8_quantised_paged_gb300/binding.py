@@ -21,13 +21,16 @@ import torch
 
 from . import _native as N
 from ._native import (E4M3, E5M2, INT8, OUT_BF16, OUT_F32, SCALE_CHANNEL_STATIC, SCALE_MX_BLOCK,
-                      SCALE_TOKEN_GROUP, SCALE_TOKEN_HEAD, Fp8paError)
+                      SCALE_SEGMENT, SCALE_TOKEN_GROUP, SCALE_TOKEN_HEAD, SEGMENT_TOKENS,
+                      Fp8paError)
 
-__all__ = ["kv_append_quant", "kv_channel_scales", "kv_channel_absmax_update",
+__all__ = ["kv_append_quant", "kv_append_quant_segment", "segment_scale_heads",
+           "kv_channel_scales", "kv_channel_absmax_update",
            "kv_scales_from_absmax", "paged_decode_attention", "paged_multiquery_attention",
            "decode_step", "decode_workspace_bytes", "get_device_error", "set_decode_workers",
            "version", "E4M3", "E5M2", "INT8", "SCALE_TOKEN_HEAD", "SCALE_CHANNEL_STATIC",
-           "SCALE_TOKEN_GROUP", "SCALE_MX_BLOCK", "OUT_BF16", "OUT_F32", "Fp8paError"]
+           "SCALE_TOKEN_GROUP", "SCALE_MX_BLOCK", "SCALE_SEGMENT", "SEGMENT_TOKENS", "OUT_BF16",
+           "OUT_F32", "Fp8paError"]
 
 
 def _ptr(t):
@@ -102,6 +105,46 @@ def kv_append_quant(k, v, slot_mapping, k_cache, v_cache, k_scale, v_scale, fmt=
                                          scale_mode, group_size, _ptr(k_cache), _ptr(v_cache),
                                          _ptr(k_scale), _ptr(v_scale), nb, bs, _stream(stream))
     N.check(rc, "kv_append_quant")
+
+
+def segment_scale_heads(n_kv_heads: int) -> int:
+    """Row length of a SCALE_SEGMENT scale tensor: KV heads rounded up to 4."""
+    return (n_kv_heads + 3) // 4 * 4
+
+
+def kv_append_quant_segment(k, v, slot_mapping, seq_offsets, seq_start_pos, k_cache, v_cache,
+                            k_scale, v_scale, seg_state, fmt=E4M3, stream=None):
+    """Append with block-wise cumulative rescaling (SCALE_SEGMENT).
+    k, v: bf16 [num_tokens, Hkv, D] (v may be None); seq_offsets: int32
+    [num_seqs + 1]; seq_start_pos: int32 [num_seqs] (each sequence's cached
+    length before the call); scales: float32 [num_blocks, round_up(Hkv, 4)];
+    seg_state: float32 [num_seqs, 2, Hkv, 2], carried between calls (see
+    include/fp8pa.h)."""
+    _need(k, torch.bfloat16, "k")
+    dev = k.device
+    _need(v, torch.bfloat16, "v", dev)
+    _need(slot_mapping, torch.int32, "slot_mapping", dev)
+    _need(seq_offsets, torch.int32, "seq_offsets", dev)
+    _need(seq_start_pos, torch.int32, "seq_start_pos", dev)
+    _need(k_cache, torch.uint8, "k_cache", dev)
+    _need(v_cache, torch.uint8, "v_cache", dev)
+    _need(k_scale, torch.float32, "k_scale", dev)
+    _need(v_scale, torch.float32, "v_scale", dev)
+    _need(seg_state, torch.float32, "seg_state", dev)
+    n, hkv, d = k.shape
+    nb, _, bs, _ = k_cache.shape
+    ns = seq_start_pos.numel()
+    if seq_offsets.numel() != ns + 1 or tuple(seg_state.shape) != (ns, 2, hkv, 2):
+        raise ValueError("seq_offsets must have num_seqs + 1 entries and seg_state "
+                         "[num_seqs, 2, Hkv, 2]")
+    if tuple(k_scale.shape) != (nb, segment_scale_heads(hkv)):
+        raise ValueError("k_scale must be [num_blocks, round_up(Hkv, 4)]")
+    with _on(dev):
+        rc = N.lib.fp8pa_kv_append_quant_segment(
+            _ptr(k), _ptr(v), _ptr(slot_mapping), _ptr(seq_offsets), _ptr(seq_start_pos), ns,
+            hkv, d, fmt, _ptr(seg_state), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
+            _ptr(v_scale), nb, bs, _stream(stream))
+    N.check(rc, "kv_append_quant_segment")
 
 
 def kv_channel_scales(x, fmt=E5M2, out=None, stream=None):

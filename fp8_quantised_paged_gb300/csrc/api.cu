@@ -17,21 +17,12 @@ __device__ uint32_t g_device_error;
 
 namespace {
 
-constexpr int kMaxDevices = 64;
-uint32_t* g_err_ptr[kMaxDevices] = {nullptr};
-std::mutex g_mu;
+void* g_err_ptr[kMaxDevices] = {nullptr};
 
-uint32_t* device_error_ptr(int* dev_out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  if (dev_out) *dev_out = dev;
-  std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_err_ptr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
-    g_err_ptr[dev] = static_cast<uint32_t*>(p);
-  }
-  return g_err_ptr[dev];
+uint32_t* device_error_ptr(cudaStream_t stream, int* dev_out) {
+  return static_cast<uint32_t*>(
+      symbol_device_address(reinterpret_cast<const void*>(&g_device_error), g_err_ptr, stream,
+                            dev_out));
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -40,7 +31,31 @@ bool pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? FP8PA_OK : FP8PA_ERR_CUDA; }
 
+std::mutex g_sym_mu;
+
 }  // namespace
+
+// Device address of a __device__ variable on the current device.  It is
+// looked up again on every call made outside stream capture, so nothing
+// stale survives a cudaDeviceReset (which reloads the module) or a switch
+// of context; during a capture (where a first-time module load must not
+// happen) the address recorded by the last uncaptured call on this device
+// is used.  `cache` has kMaxDevices entries.
+void* symbol_device_address(const void* symbol, void** cache, cudaStream_t stream,
+                            int* dev_out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  if (dev_out) *dev_out = dev;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) return nullptr;
+  std::lock_guard<std::mutex> lock(g_sym_mu);
+  if (cs == cudaStreamCaptureStatusNone) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, symbol) != cudaSuccess || !p) return nullptr;
+    cache[dev] = p;
+  }
+  return cache[dev];
+}
 
 // Per-device host caches of the launch set-up that does not change between
 // calls: the SM count, the dynamic shared-memory opt-in of each kernel, and
@@ -170,7 +185,8 @@ DecodePath decode_path(int batch, int hq, int hkv, int d, int dv, int bs, int ma
   s.qlen = 1;
   if ((fmt != FP8PA_E4M3 && fmt != FP8PA_E5M2 && fmt != FP8PA_INT8) ||
       (mode != FP8PA_SCALE_TOKEN_HEAD && mode != FP8PA_SCALE_CHANNEL_STATIC &&
-       mode != FP8PA_SCALE_TOKEN_GROUP && mode != FP8PA_SCALE_MX_BLOCK) ||
+       mode != FP8PA_SCALE_TOKEN_GROUP && mode != FP8PA_SCALE_MX_BLOCK &&
+       mode != FP8PA_SCALE_SEGMENT) ||
       (out_dtype != FP8PA_OUT_BF16 && out_dtype != FP8PA_OUT_F32)) {
     r.status = FP8PA_ERR_BAD_ENUM;
     return r;
@@ -188,8 +204,8 @@ DecodePath decode_path(int batch, int hq, int hkv, int d, int dv, int bs, int ma
   }
   if (d == 576) {
     s.mla = 1;
-    if (hkv != 1 || dv != 512 || mode != FP8PA_SCALE_TOKEN_GROUP || gs != 64 || bs != 64 ||
-        hq % 32 != 0)
+    if (hkv != 1 || dv != 512 || bs != 64 || hq % 32 != 0 ||
+        !((mode == FP8PA_SCALE_TOKEN_GROUP && gs == 64) || mode == FP8PA_SCALE_SEGMENT))
       r.status = FP8PA_ERR_UNSUPPORTED;
     return r;
   }
@@ -211,7 +227,8 @@ int attention_prepare(const void* q, const uint8_t* k_cache, const uint8_t* v_ca
                       int block_size, int n_q_heads, int n_kv_heads, int head_dim,
                       int head_dim_v, int fmt, int scale_mode, int group_size, float sm_scale,
                       int num_blocks, void* out, int out_dtype, void* workspace,
-                      size_t workspace_bytes, DecodePath* path, DecodeArgs* a) {
+                      size_t workspace_bytes, cudaStream_t stream, DecodePath* path,
+                      DecodeArgs* a) {
   if (q_len <= 0 || batch < 0) return FP8PA_ERR_BAD_SHAPE;
   if (static_cast<long long>(batch) * q_len >= (1ll << 31)) return FP8PA_ERR_UNSUPPORTED;
   *path = decode_path(batch * q_len, n_q_heads, n_kv_heads, head_dim, head_dim_v, block_size,
@@ -230,7 +247,7 @@ int attention_prepare(const void* q, const uint8_t* k_cache, const uint8_t* v_ca
       !aligned16(v_scale) || !aligned16(workspace) || !aligned16(out))
     return FP8PA_ERR_ALIGNMENT;
   int dev = 0;
-  uint32_t* err = device_error_ptr(&dev);
+  uint32_t* err = device_error_ptr(stream, &dev);
   if (!err) return FP8PA_ERR_CUDA;
   path->shape.workers = decode_workers(path->shape, fmt, scale_mode, dev);
   if (workspace_bytes < decode_workspace_bytes(path->shape)) return FP8PA_ERR_WORKSPACE;
@@ -273,7 +290,7 @@ int attention_impl(const void* q, const uint8_t* k_cache, const uint8_t* v_cache
                                    max_blocks_per_seq, seq_lens, batch, q_len, block_size,
                                    n_q_heads, n_kv_heads, head_dim, head_dim_v, fmt, scale_mode,
                                    group_size, sm_scale, num_blocks, out, out_dtype, workspace,
-                                   workspace_bytes, &path, &a);
+                                   workspace_bytes, static_cast<cudaStream_t>(stream), &path, &a);
   if (st != FP8PA_OK || batch == 0) return st;
   return cuda_status(launch_decode(path, a, static_cast<cudaStream_t>(stream)));
 }
@@ -287,7 +304,8 @@ int append_prepare(const void* k, const void* v, const int32_t* slot_mapping, in
     return FP8PA_ERR_BAD_SHAPE;
   if ((fmt != FP8PA_E4M3 && fmt != FP8PA_E5M2 && fmt != FP8PA_INT8) ||
       (scale_mode != FP8PA_SCALE_TOKEN_HEAD && scale_mode != FP8PA_SCALE_CHANNEL_STATIC &&
-       scale_mode != FP8PA_SCALE_TOKEN_GROUP && scale_mode != FP8PA_SCALE_MX_BLOCK))
+       scale_mode != FP8PA_SCALE_TOKEN_GROUP && scale_mode != FP8PA_SCALE_MX_BLOCK &&
+       scale_mode != FP8PA_SCALE_SEGMENT))
     return FP8PA_ERR_BAD_ENUM;
   if (head_dim % 16 != 0 || head_dim > 768) return FP8PA_ERR_UNSUPPORTED;
   if (scale_mode == FP8PA_SCALE_TOKEN_GROUP &&
@@ -296,7 +314,11 @@ int append_prepare(const void* k, const void* v, const int32_t* slot_mapping, in
   if (scale_mode == FP8PA_SCALE_MX_BLOCK &&
       ((group_size != 16 && group_size != 32) || head_dim % group_size != 0 || fmt == FP8PA_INT8))
     return FP8PA_ERR_UNSUPPORTED;
-  if (static_cast<long long>(num_blocks) * block_size >= (1ll << 31)) return FP8PA_ERR_UNSUPPORTED;
+  // the segment mode needs token positions: fp8pa_kv_append_quant_segment
+  if (scale_mode == FP8PA_SCALE_SEGMENT) return FP8PA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(num_blocks) * block_size >= (1ll << 31) ||
+      static_cast<long long>(num_tokens) * n_kv_heads * 2 >= (1ll << 31))
+    return FP8PA_ERR_UNSUPPORTED;
   *a = AppendArgs{};
   a->num_tokens = num_tokens;
   if (num_tokens == 0) return FP8PA_OK;
@@ -320,6 +342,8 @@ int append_prepare(const void* k, const void* v, const int32_t* slot_mapping, in
               : head_dim;
   a->num_blocks = num_blocks;
   a->bs = block_size;
+  a->div_tok = make_fast_div(static_cast<uint32_t>(n_kv_heads * a->ntens));
+  a->div_bs = make_fast_div(static_cast<uint32_t>(block_size));
   return FP8PA_OK;
 }
 
@@ -365,9 +389,54 @@ int fp8pa_kv_append_quant(const void* k, const void* v, const int32_t* slot_mapp
                                 scale_mode, group_size, k_cache, v_cache, k_scale, v_scale,
                                 num_blocks, block_size, &a);
   if (st != FP8PA_OK || num_tokens == 0) return st;
-  a.err = device_error_ptr(nullptr);
+  a.err = device_error_ptr(static_cast<cudaStream_t>(stream), nullptr);
   if (!a.err) return FP8PA_ERR_CUDA;
   return cuda_status(launch_append(a, fmt, scale_mode, static_cast<cudaStream_t>(stream)));
+}
+
+int fp8pa_kv_append_quant_segment(const void* k, const void* v, const int32_t* slot_mapping,
+                                  const int32_t* seq_offsets, const int32_t* seq_start_pos,
+                                  int num_seqs, int n_kv_heads, int head_dim, int fmt,
+                                  float* seg_state, uint8_t* k_cache, uint8_t* v_cache,
+                                  float* k_scale, float* v_scale, int num_blocks, int block_size,
+                                  void* stream) {
+  if (num_seqs < 0 || n_kv_heads <= 0 || head_dim <= 0 || num_blocks <= 0 || block_size <= 0)
+    return FP8PA_ERR_BAD_SHAPE;
+  if (fmt != FP8PA_E4M3 && fmt != FP8PA_E5M2 && fmt != FP8PA_INT8) return FP8PA_ERR_BAD_ENUM;
+  if (head_dim % 16 != 0 || head_dim > 768 || kSegmentTokens % block_size != 0)
+    return FP8PA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(num_blocks) * block_size >= (1ll << 31) ||
+      static_cast<long long>(num_seqs) * 2 * n_kv_heads >= (1ll << 31))
+    return FP8PA_ERR_UNSUPPORTED;
+  if (num_seqs == 0) return FP8PA_OK;
+  if (!k || !slot_mapping || !seq_offsets || !seq_start_pos || !seg_state || !k_cache ||
+      !k_scale)
+    return FP8PA_ERR_NULL_POINTER;
+  if (v && (!v_cache || !v_scale)) return FP8PA_ERR_NULL_POINTER;
+  if (!aligned16(k) || !aligned16(k_cache) || !aligned16(k_scale) ||
+      (v && (!aligned16(v) || !aligned16(v_cache) || !aligned16(v_scale))))
+    return FP8PA_ERR_ALIGNMENT;
+  SegmentArgs a{};
+  a.src[0] = static_cast<const uint16_t*>(k);
+  a.src[1] = static_cast<const uint16_t*>(v);
+  a.cache[0] = k_cache;
+  a.cache[1] = v_cache;
+  a.scale[0] = k_scale;
+  a.scale[1] = v_scale;
+  a.slot_mapping = slot_mapping;
+  a.seq_offsets = seq_offsets;
+  a.seq_start = seq_start_pos;
+  a.state = seg_state;
+  a.num_seqs = num_seqs;
+  a.hkv = n_kv_heads;
+  a.hp = segment_scale_heads(n_kv_heads);
+  a.d = head_dim;
+  a.ntens = v ? 2 : 1;
+  a.num_blocks = num_blocks;
+  a.bs = block_size;
+  a.err = device_error_ptr(static_cast<cudaStream_t>(stream), nullptr);
+  if (!a.err) return FP8PA_ERR_CUDA;
+  return cuda_status(launch_append_segment(a, fmt, static_cast<cudaStream_t>(stream)));
 }
 
 int fp8pa_kv_channel_scales(const void* x, int num_tokens, int n_kv_heads, int head_dim, int fmt,
@@ -411,10 +480,11 @@ size_t fp8pa_multiquery_workspace_bytes(int batch, int q_len, int n_q_heads, int
   // The largest need over the scale modes and formats of this layout (the
   // split count follows each kernel's occupancy).
   const bool mla = head_dim == 576;
-  const int modes[3] = {mla ? FP8PA_SCALE_TOKEN_GROUP : FP8PA_SCALE_TOKEN_HEAD,
-                        FP8PA_SCALE_CHANNEL_STATIC, FP8PA_SCALE_MX_BLOCK};
+  const int modes[4] = {mla ? FP8PA_SCALE_TOKEN_GROUP : FP8PA_SCALE_TOKEN_HEAD,
+                        mla ? FP8PA_SCALE_SEGMENT : FP8PA_SCALE_CHANNEL_STATIC,
+                        FP8PA_SCALE_MX_BLOCK, FP8PA_SCALE_SEGMENT};
   size_t need = 0;
-  for (int m = 0; m < (mla ? 1 : 3); ++m)
+  for (int m = 0; m < (mla ? 2 : 4); ++m)
     for (int fmt = FP8PA_E4M3; fmt <= FP8PA_INT8; ++fmt) {
       DecodePath path = decode_path(batch * q_len, n_q_heads, n_kv_heads, head_dim, head_dim_v,
                                     block_size, max_blocks_per_seq, fmt, modes[m],
@@ -481,10 +551,11 @@ int fp8pa_decode_step(const void* k_new, const void* v_new, const int32_t* slot_
   st = attention_prepare(q, k_cache, v_cache, k_scale, v_scale, block_tables, max_blocks_per_seq,
                          seq_lens, batch, q_len, block_size, n_q_heads, n_kv_heads, head_dim,
                          head_dim_v, fmt, scale_mode, group_size, sm_scale, num_blocks, out,
-                         out_dtype, workspace, workspace_bytes, &path, &a);
+                         out_dtype, workspace, workspace_bytes, static_cast<cudaStream_t>(stream),
+                         &path, &a);
   if (st != FP8PA_OK) return st;
   const cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  ap.err = device_error_ptr(nullptr);
+  ap.err = a.err ? a.err : device_error_ptr(cs, nullptr);
   if (!ap.err) return FP8PA_ERR_CUDA;
   if (batch == 0)
     return num_new_tokens == 0 ? FP8PA_OK : cuda_status(launch_append(ap, fmt, scale_mode, cs));
@@ -507,7 +578,7 @@ int fp8pa_decode_step(const void* k_new, const void* v_new, const int32_t* slot_
 int fp8pa_selftest_bounded_wait(long long limit_cycles, void* stream) {
   const long long limit =
       limit_cycles < 1000 ? 1000 : (limit_cycles > kWaitLimitCycles ? kWaitLimitCycles : limit_cycles);
-  uint32_t* err = device_error_ptr(nullptr);
+  uint32_t* err = device_error_ptr(static_cast<cudaStream_t>(stream), nullptr);
   if (!err) return FP8PA_ERR_CUDA;
   bounded_wait_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(limit, err);
   return cuda_status(cudaGetLastError());
@@ -517,7 +588,6 @@ int fp8pa_get_device_error(void* stream, uint32_t* flags) {
   if (!flags) return FP8PA_ERR_NULL_POINTER;
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return FP8PA_ERR_CUDA;
-  if (!device_error_ptr(nullptr)) return FP8PA_ERR_CUDA;
   uint32_t v = 0;
   if (cudaMemcpyFromSymbol(&v, g_device_error, sizeof v) != cudaSuccess) return FP8PA_ERR_CUDA;
   const uint32_t zero = 0;

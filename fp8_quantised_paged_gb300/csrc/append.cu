@@ -14,8 +14,9 @@
 // The symmetric INT8 codec takes 127 as the maximum and rounds x / scale to
 // the nearest integer, ties to even, clamped to [-127, 127].
 //
-// One warp per (token, kv head, K-or-V) row.  Each lane owns 8 contiguous
-// values (one 16-byte load, one 8-byte code store).  The divisions are IEEE
+// A group of lanes per (token, kv head, K-or-V) row, several rows per warp.
+// Each lane owns 8 contiguous values per 16-byte chunk (one 16-byte load, one
+// 8-byte code store).  The divisions are IEEE
 // fp32 round-to-nearest (__fdiv_rn) and the FP8 cast is the hardware
 // cvt.rn.satfinite (INT8: cvt.rni), so codes and scales are bit-exact with
 // the definition.
@@ -38,74 +39,93 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float (&f)[8]) {
   }
 }
 
-// One (token, kv head, K-or-V) row per warp.
-template <int FMT, int MODE, int R>
-__device__ __forceinline__ void append_row(const AppendArgs& a, long row, int lane) {
-  const int per_tok = a.hkv * a.ntens;
-  if (row >= static_cast<long>(a.num_tokens) * per_tok) return;
-  const int t = static_cast<int>(row / per_tok);
-  const int rem = static_cast<int>(row % per_tok);
-  const int which = rem / a.hkv;
-  const int h = rem % a.hkv;
-  const int slot = __ldg(a.slot_mapping + t);
-  if (slot < 0) return;  // padding token
-  const long blk = slot / a.bs;
-  const int off = slot % a.bs;
-  if (blk >= a.num_blocks) {
-    if (lane == 0) raise_error(a.err, FP8PA_DEVERR_SLOT_RANGE);
-    return;
-  }
-  const uint16_t* x = a.src[which] + (static_cast<long>(t) * a.hkv + h) * a.d;
-  const long crow = (blk * a.hkv + h) * a.bs + off;
-  uint8_t* dst = a.cache[which] + crow * a.d;
-  const int nch = a.d / 8;
+// Lanes per row: a sub-group of LPR lanes (a power of two >= 8, at most 32)
+// appends one row; a lane owns chunks sl, sl + LPR, ... (R of them) of the
+// row's 16-byte chunks, so a warp covers 32 / LPR rows per step.
 
-  float v[R][8];
-  float cmax[R];
+// Row `row` of the call: its (K-or-V, head) index `rem` (-1 past the end), its
+// slot, and its values (zeros where the lane has no chunk).
+template <int LPR, int R>
+__device__ __forceinline__ void load_row(const AppendArgs& a, long row, int sl, float (&v)[R][8],
+                                         int& rem, int& slot) {
+  const int per_tok = a.hkv * a.ntens;
+  const bool in = row < static_cast<long>(a.num_tokens) * per_tok;
+  const uint32_t r32 = in ? static_cast<uint32_t>(row) : 0u;
+  const uint32_t t = fast_div(r32, a.div_tok);
+  const int rw = static_cast<int>(r32 - t * static_cast<uint32_t>(per_tok));
+  rem = in ? rw : -1;
+  slot = in ? __ldg(a.slot_mapping + t) : -1;
+  const bool second = rw >= a.hkv;  // the V row
+  const uint16_t* x =
+      (second ? a.src[1] : a.src[0]) +
+      (static_cast<long>(t) * a.hkv + (second ? rw - a.hkv : rw)) * a.d;
+  const int nch = a.d / 8;
 #pragma unroll
   for (int r = 0; r < R; ++r) {
-    const int ci = lane + 32 * r;
-    cmax[r] = 0.0f;
-    if (ci < nch) {
-      const uint4 u = __ldg(reinterpret_cast<const uint4*>(x + ci * 8));
-      bf16x8_to_f32(u, v[r]);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) cmax[r] = fmaxf(cmax[r], fabsf(v[r][e]));
+    const int ci = sl + LPR * r;
+    if (in && ci < nch) {
+      bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>(x + ci * 8)), v[r]);
     } else {
 #pragma unroll
       for (int e = 0; e < 8; ++e) v[r][e] = 0.0f;
     }
   }
+}
 
+// Scale, round and scatter one loaded row (the whole sub-group joins the
+// shuffles, also for rows that are skipped: past the end, a negative slot,
+// or a slot past the pool).
+template <int FMT, int MODE, int LPR, int R>
+__device__ __forceinline__ void store_row(const AppendArgs& a, const float (&v)[R][8], int rem,
+                                          int slot, int sl) {
   constexpr float kFmax = code_max<FMT>();
   constexpr int kEmax = FMT == FP8PA_E4M3 ? 8 : 15;  // exponent of the largest normal
+  const int nch = a.d / 8;
+  const int which = rem >= a.hkv ? 1 : 0;
+  const int h = rem - which * a.hkv;
+  const uint32_t bq = slot < 0 ? 0u : fast_div(static_cast<uint32_t>(slot), a.div_bs);
+  const long blk = slot < 0 ? -1 : static_cast<long>(bq);
+  const int off = slot < 0 ? 0 : slot - static_cast<int>(bq) * a.bs;
+  const bool live = rem >= 0 && slot >= 0 && blk < a.num_blocks;
+  if (rem >= 0 && blk >= a.num_blocks && sl == 0) raise_error(a.err, FP8PA_DEVERR_SLOT_RANGE);
+  const long crow = live ? (blk * a.hkv + h) * a.bs + off : 0;
+  uint8_t* dst = live ? (which ? a.cache[1] : a.cache[0]) + crow * a.d : nullptr;
+  float* scl = which ? a.scale[1] : a.scale[0];
+
+  float cmax[R];
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    cmax[r] = 0.0f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) cmax[r] = fmaxf(cmax[r], fabsf(v[r][e]));
+  }
   float s[R];
   if constexpr (MODE == FP8PA_SCALE_TOKEN_HEAD) {
     float m = 0.0f;
 #pragma unroll
     for (int r = 0; r < R; ++r) m = fmaxf(m, cmax[r]);
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    for (int o = LPR / 2; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
     const float sc = fmaxf(__fdiv_rn(m, kFmax), 1e-12f);
 #pragma unroll
     for (int r = 0; r < R; ++r) s[r] = sc;
-    if (lane == 0) a.scale[which][crow] = sc;
+    if (live && sl == 0) scl[crow] = sc;
   } else if constexpr (MODE == FP8PA_SCALE_TOKEN_GROUP) {
-    const int lpg = a.gs / 8;  // lanes per group: a power of two <= 32
+    const int lpg = a.gs / 8;  // lanes per group: a power of two <= LPR
     const int ngroups = a.d / a.gs;
 #pragma unroll
     for (int r = 0; r < R; ++r) {
       float m = cmax[r];
       for (int o = 1; o < lpg; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
       s[r] = fmaxf(__fdiv_rn(m, kFmax), 1e-12f);
-      const int ci = lane + 32 * r;
-      if (ci < nch && (lane & (lpg - 1)) == 0)
-        a.scale[which][crow * ngroups + (ci * 8) / a.gs] = s[r];
+      const int ci = sl + LPR * r;
+      if (live && ci < nch && (sl & (lpg - 1)) == 0)
+        scl[crow * ngroups + (ci * 8) / a.gs] = s[r];
     }
   } else if constexpr (MODE == FP8PA_SCALE_MX_BLOCK) {
     // s = 2^e with e = floor(log2(block absmax)) - emax, read off the fp32
-    // exponent field (a zero or subnormal absmax gives the floor, -127); the
-    // codes below multiply by 2^-e, which is exact.
+    // exponent field (a zero or subnormal absmax gives the floor, -127);
+    // the codes below multiply by 2^-e, which is exact.
     const int lpg = a.gs / 8;
     const int ngroups = a.d / a.gs;
 #pragma unroll
@@ -115,20 +135,21 @@ __device__ __forceinline__ void append_row(const AppendArgs& a, long row, int la
       const int ef = (__float_as_int(m) >> 23) & 0xFF;
       const int e = ef == 0 ? -127 : min(127, max(-127, ef - 127 - kEmax));
       s[r] = exp2i(-e);  // the multiplier 2^-e (e <= 119 for bf16 inputs)
-      const int ci = lane + 32 * r;
-      if (ci < nch && (lane & (lpg - 1)) == 0)
-        reinterpret_cast<uint8_t*>(a.scale[which])[crow * ngroups + (ci * 8) / a.gs] =
+      const int ci = sl + LPR * r;
+      if (live && ci < nch && (sl & (lpg - 1)) == 0)
+        reinterpret_cast<uint8_t*>(scl)[crow * ngroups + (ci * 8) / a.gs] =
             static_cast<uint8_t>(e + 127);
     }
   }
+  if (!live) return;
 
 #pragma unroll
   for (int r = 0; r < R; ++r) {
-    const int ci = lane + 32 * r;
+    const int ci = sl + LPR * r;
     if (ci >= nch) continue;
     float q[8];
     if constexpr (MODE == FP8PA_SCALE_CHANNEL_STATIC) {
-      const float4* sp = reinterpret_cast<const float4*>(a.scale[which] + h * a.d + ci * 8);
+      const float4* sp = reinterpret_cast<const float4*>(scl + h * a.d + ci * 8);
       const float4 s0 = __ldg(sp), s1 = __ldg(sp + 1);
       const float sc[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
 #pragma unroll
@@ -147,17 +168,60 @@ __device__ __forceinline__ void append_row(const AppendArgs& a, long row, int la
   }
 }
 
-template <int FMT, int MODE, int R>
+// Few rows (a decode step): one step of 32 / LPR rows per warp, so the
+// launch (and the attention waiting on it) ends one load latency after it
+// starts.
+template <int FMT, int MODE, int LPR, int R>
+__device__ __forceinline__ void append_step(const AppendArgs& a, long warp, int lane) {
+  constexpr int SG = 32 / LPR;
+  const int sg = lane / LPR, sl = lane % LPR;
+  float v[R][8];
+  int rem, slot;
+  load_row<LPR, R>(a, warp * SG + sg, sl, v, rem, slot);
+  store_row<FMT, MODE, LPR, R>(a, v, rem, slot, sl);
+}
+
+template <int FMT, int MODE, int LPR, int R>
 __global__ void __launch_bounds__(kAppendWarps * 32) append_kernel(AppendArgs a) {
   griddep_wait();  // launched early (programmatic serialisation): inputs may be in flight
   griddep_launch_dependents();
-  append_row<FMT, MODE, R>(a, static_cast<long>(blockIdx.x) * kAppendWarps + (threadIdx.x >> 5),
-                           threadIdx.x & 31);
+  append_step<FMT, MODE, LPR, R>(a, static_cast<long>(blockIdx.x) * kAppendWarps + (threadIdx.x >> 5),
+                                 threadIdx.x & 31);
+}
+
+// Many rows (a prefill): a persistent grid whose warps stride over the
+// steps of rows with a ring of kStreamDepth steps in registers -- a step's
+// loads are issued kStreamDepth - 1 steps before the warp works on it, so
+// loads stay in flight while the warp scales and rounds.
+constexpr int kStreamDepth = 3;
+
+template <int FMT, int MODE, int LPR, int R>
+__global__ void __launch_bounds__(kAppendWarps * 32) append_stream_kernel(AppendArgs a) {
+  griddep_wait();
+  griddep_launch_dependents();
+  constexpr int SG = 32 / LPR, P = kStreamDepth;
+  const int lane = threadIdx.x & 31, sg = lane / LPR, sl = lane % LPR;
+  const long nsteps = (static_cast<long>(a.num_tokens) * a.hkv * a.ntens + SG - 1) / SG;
+  const long stride = static_cast<long>(gridDim.x) * kAppendWarps;
+  const long first = static_cast<long>(blockIdx.x) * kAppendWarps + (threadIdx.x >> 5);
+  float v[P][R][8];
+  int rem[P], slot[P];
+#pragma unroll
+  for (int p = 0; p < P; ++p) load_row<LPR, R>(a, (first + p * stride) * SG + sg, sl, v[p], rem[p], slot[p]);
+  for (long s0 = first; s0 < nsteps; s0 += P * stride) {
+#pragma unroll
+    for (int p = 0; p < P; ++p) {
+      const long st = s0 + p * stride;
+      if (st >= nsteps) break;  // warp-uniform
+      store_row<FMT, MODE, LPR, R>(a, v[p], rem[p], slot[p], sl);
+      load_row<LPR, R>(a, (st + P * stride) * SG + sg, sl, v[p], rem[p], slot[p]);
+    }
+  }
 }
 
 // A decode step's prologue in one launch: CTA 0's first warp plans the
 // split of the attention that follows, the other CTAs append the new rows.
-template <int FMT, int MODE, int R>
+template <int FMT, int MODE, int LPR, int R>
 __global__ void __launch_bounds__(kAppendWarps * 32) append_plan_kernel(AppendArgs a, PlanArgs pl) {
   griddep_wait();
   griddep_launch_dependents();
@@ -167,36 +231,55 @@ __global__ void __launch_bounds__(kAppendWarps * 32) append_plan_kernel(AppendAr
                 pl.plan, pl.err);
     return;
   }
-  append_row<FMT, MODE, R>(a,
-                           static_cast<long>(blockIdx.x - 1) * kAppendWarps + (threadIdx.x >> 5),
-                           threadIdx.x & 31);
+  append_step<FMT, MODE, LPR, R>(
+      a, static_cast<long>(blockIdx.x - 1) * kAppendWarps + (threadIdx.x >> 5), threadIdx.x & 31);
 }
 
-// pl == nullptr: the append alone; else the fused append + plan prologue.
-template <int FMT, int MODE>
-cudaError_t launch_append_r(const AppendArgs& a, const PlanArgs* pl, cudaStream_t stream) {
+// Calls of at least this many rows stream through the persistent kernel.
+constexpr long kBulkRows = 16384;
+
+template <int FMT, int MODE, int LPR, int R>
+cudaError_t launch_append_shape(const AppendArgs& a, const PlanArgs* pl, cudaStream_t stream) {
   const long rows = static_cast<long>(a.num_tokens) * a.hkv * a.ntens;
   if (rows == 0 && !pl) return cudaSuccess;
-  const dim3 grid(
-      static_cast<unsigned>((rows + kAppendWarps - 1) / kAppendWarps + (pl ? 1 : 0)));
-  const int nch = a.d / 8;
+  constexpr long kRowsPerCta = static_cast<long>(kAppendWarps) * (32 / LPR);
+  const long ctas = (rows + kRowsPerCta - 1) / kRowsPerCta;
   cudaLaunchAttribute pdl[1];
   pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   pdl[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
   cfg.blockDim = dim3(kAppendWarps * 32);
   cfg.stream = stream;
   cfg.attrs = pdl;
   cfg.numAttrs = 1;
   if (pl) {
-    if (nch <= 32) return cudaLaunchKernelEx(&cfg, append_plan_kernel<FMT, MODE, 1>, a, *pl);
-    if (nch <= 64) return cudaLaunchKernelEx(&cfg, append_plan_kernel<FMT, MODE, 2>, a, *pl);
-    return cudaLaunchKernelEx(&cfg, append_plan_kernel<FMT, MODE, 3>, a, *pl);
+    cfg.gridDim = dim3(static_cast<unsigned>(ctas + 1));
+    return cudaLaunchKernelEx(&cfg, append_plan_kernel<FMT, MODE, LPR, R>, a, *pl);
   }
-  if (nch <= 32) return cudaLaunchKernelEx(&cfg, append_kernel<FMT, MODE, 1>, a);
-  if (nch <= 64) return cudaLaunchKernelEx(&cfg, append_kernel<FMT, MODE, 2>, a);
-  return cudaLaunchKernelEx(&cfg, append_kernel<FMT, MODE, 3>, a);
+  if (rows >= kBulkRows) {
+    const auto fn = append_stream_kernel<FMT, MODE, LPR, R>;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+    const long resident = static_cast<long>(sm_count(dev)) *
+                          ctas_per_sm(reinterpret_cast<const void*>(fn), kAppendWarps * 32, 0);
+    cfg.gridDim = dim3(static_cast<unsigned>(ctas < resident ? ctas : resident));
+    return cudaLaunchKernelEx(&cfg, fn, a);
+  }
+  cfg.gridDim = dim3(static_cast<unsigned>(ctas));
+  return cudaLaunchKernelEx(&cfg, append_kernel<FMT, MODE, LPR, R>, a);
+}
+
+// pl == nullptr: the append alone; else the fused append + plan prologue.
+// Lanes per row follow the row's 16-byte chunks (head_dim / 8): 8 lanes up
+// to head_dim 64, 16 at 128, 32 (with 2 or 3 chunks each) beyond 256.
+template <int FMT, int MODE>
+cudaError_t launch_append_r(const AppendArgs& a, const PlanArgs* pl, cudaStream_t stream) {
+  const int nch = a.d / 8;
+  if (nch <= 8) return launch_append_shape<FMT, MODE, 8, 1>(a, pl, stream);
+  if (nch <= 16) return launch_append_shape<FMT, MODE, 16, 1>(a, pl, stream);
+  if (nch <= 32) return launch_append_shape<FMT, MODE, 32, 1>(a, pl, stream);
+  if (nch <= 64) return launch_append_shape<FMT, MODE, 32, 2>(a, pl, stream);
+  return launch_append_shape<FMT, MODE, 32, 3>(a, pl, stream);
 }
 
 template <int FMT>

@@ -78,6 +78,7 @@ struct GqaParams {
   int qlen;  // queries per request of a causal chunk
   int qw;    // query warps per KV head: B planned requests of qw queries each
   int gs;    // dims per block exponent (MX block mode)
+  int hp;    // segment mode: page scales per block (KV heads rounded up to 4)
   float qk_scale_log2;
 };
 
@@ -171,11 +172,12 @@ template <int D, int BS, int FMT, int MODE, int NST>
 __global__ void __launch_bounds__(kMaxWarps * 32)
     gqa_split_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                      const GqaParams p) {
-  constexpr bool TOKSC = (MODE == FP8PA_SCALE_TOKEN_HEAD);
+  constexpr bool SEG = (MODE == FP8PA_SCALE_SEGMENT);  // one scale per (page, KV head)
+  constexpr bool TOKSC = (MODE == FP8PA_SCALE_TOKEN_HEAD) || SEG;
   constexpr bool PK = (MODE == kModeStaticPacked);
   constexpr bool MX = (MODE == FP8PA_SCALE_MX_BLOCK);
   constexpr bool DYN = TOKSC || MX;  // per-token scales: q stays exact in f16
-  constexpr int SCB = TOKSC ? 4 : (MX ? D / 16 : 0);
+  constexpr int SCB = SEG ? 1 : (TOKSC ? 4 : (MX ? D / 16 : 0));
   constexpr int XS = MxTable<D>::kStride;
   // A stage holds one 16-token slice of a page (SUB slices per page), so
   // large pages do not make a warp's ring large.
@@ -187,7 +189,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32)
   constexpr int VW = D / 32;   // V words per token per thread
   constexpr int MT = D / 16;   // dv tiles of 16
   const int nbx = MX ? D / p.gs : 0;  // exponent bytes per token (MX)
-  const uint32_t TX = 2 * PAGE + (TOKSC ? 2 * 16 * 4 : (MX ? 2 * 16 * nbx : 0));
+  const uint32_t TX = 2 * PAGE + (SEG ? 2 * 16 : (TOKSC ? 2 * 16 * 4 : (MX ? 2 * 16 * nbx : 0)));
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -279,7 +281,12 @@ __global__ void __launch_bounds__(kMaxWarps * 32)
         mbar_arrive_expect_tx(&bars[s], TX);
         tma_load_2d(pages + s * 2 * PAGE, &tmk, 0, row, &bars[s]);
         tma_load_2d(pages + s * 2 * PAGE + PAGE, &tmv, 0, row, &bars[s]);
-        if constexpr (TOKSC) {
+        if constexpr (SEG) {
+          // the 16-byte quad of page scales holding this KV head's
+          const long quad = static_cast<long>(blk) * p.hp + (kvh & ~3);
+          bulk_load(sclb + s * 2 * 16, p.k_scale + quad, 16, &bars[s]);
+          bulk_load(sclb + s * 2 * 16 + 16, p.v_scale + quad, 16, &bars[s]);
+        } else if constexpr (TOKSC) {
           bulk_load(scl + s * 2 * 16, p.k_scale + row, 16 * 4, &bars[s]);
           bulk_load(scl + s * 2 * 16 + 16, p.v_scale + row, 16 * 4, &bars[s]);
         } else if constexpr (MX) {
@@ -451,7 +458,12 @@ __global__ void __launch_bounds__(kMaxWarps * 32)
       // the token) (exact), and 2^e_max becomes the row's scale; this lane's
       // K words cover block kb0 (words with 4j < gs) and kb1.
       uint32_t fk0a = 0u, fk0b = 0u, fk1a = 0u, fk1b = 0u;
-      if constexpr (TOKSC) {
+      if constexpr (SEG) {
+        const float* quad = reinterpret_cast<const float*>(sclb + s * 2 * 16);
+        sk0 = sk1 = quad[kvh & 3];
+        sv0 = v0 ? quad[4 + (kvh & 3)] : 0.f;
+        sv1 = v1 ? quad[4 + (kvh & 3)] : 0.f;
+      } else if constexpr (TOKSC) {
         sk0 = sks[r0 + g];
         sk1 = sks[r0 + g + 8];
         sv0 = v0 ? svs[r0 + g] : 0.f;
@@ -733,7 +745,9 @@ template <int D, int BS, int FMT, int MODE>
 SplitKernel pick4() {
   constexpr int NST = stages_for<D>();
   constexpr bool MX = MODE == FP8PA_SCALE_MX_BLOCK;
-  constexpr int SCB = MODE == FP8PA_SCALE_TOKEN_HEAD ? 4 : (MX ? D / 16 : 0);
+  constexpr int SCB = MODE == FP8PA_SCALE_SEGMENT
+                          ? 1
+                          : (MODE == FP8PA_SCALE_TOKEN_HEAD ? 4 : (MX ? D / 16 : 0));
   using SM = GqaSmem<D, NST, SCB, MX ? MxTable<D>::kWords : 0>;
   return {gqa_split_kernel<D, BS, FMT, MODE, NST>, SM::bytes(1) - 1024};
 }
@@ -746,6 +760,7 @@ SplitKernel pick3(int mode) {
       if constexpr (FMT != FP8PA_INT8) return pick4<D, BS, FMT, FP8PA_SCALE_MX_BLOCK>();
       return pick4<D, BS, FMT, FP8PA_SCALE_TOKEN_HEAD>();
     case kModeStaticPacked: return pick4<D, BS, FMT, kModeStaticPacked>();
+    case FP8PA_SCALE_SEGMENT: return pick4<D, BS, FMT, FP8PA_SCALE_SEGMENT>();
     default: return pick4<D, BS, FMT, FP8PA_SCALE_CHANNEL_STATIC>();
   }
 }
@@ -904,6 +919,7 @@ cudaError_t launch_decode_gqa(const DecodeShape& s, const DecodeArgs& a, cudaStr
   p.qlen = s.qlen;
   p.qw = qw;
   p.gs = a.gs;
+  p.hp = segment_scale_heads(s.hkv);
   p.qk_scale_log2 = a.sm_scale * 1.4426950408889634f;
   cfg.gridDim = dim3(static_cast<unsigned>(s.workers) * hsets);
   cfg.blockDim = dim3(wpc * 32);

@@ -87,7 +87,9 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t&
                : "r"(addr));
 }
 
-template <int FMT>
+// SEG: one scale per page (the segment mode: block-wise cumulative
+// rescaling) in place of one per (token, 64-dim group).
+template <int FMT, bool SEG>
 __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const MlaParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* stages = smem + MlaSmem::kStages;
@@ -160,11 +162,15 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const MlaParams 
     const bool ok = blk >= 0 && blk < p.num_blocks;
     okf[s] = ok ? 1 : 0;
     if (ok) {
-      mbar_arrive_expect_tx(&bars[s], kStageBytes);
+      mbar_arrive_expect_tx(&bars[s], kCodeBytes + (SEG ? 16 : kScaleBytes));
       bulk_load(stages + s * kStageBytes, p.cache + static_cast<long>(blk) * kCodeBytes,
                 kCodeBytes, &bars[s]);
-      bulk_load(stages + s * kStageBytes + kCodeBytes,
-                p.scale + static_cast<long>(blk) * kBs * kGroups, kScaleBytes, &bars[s]);
+      if constexpr (SEG)  // the page's row of 4 scales (one KV head, padded to 16 bytes)
+        bulk_load(stages + s * kStageBytes + kCodeBytes, p.scale + static_cast<long>(blk) * 4, 16,
+                  &bars[s]);
+      else
+        bulk_load(stages + s * kStageBytes + kCodeBytes,
+                  p.scale + static_cast<long>(blk) * kBs * kGroups, kScaleBytes, &bars[s]);
     } else {
       raise_error(p.err, FP8PA_DEVERR_BLOCK_RANGE);
       mbar_arrive(&bars[s]);
@@ -265,7 +271,8 @@ __global__ void __launch_bounds__(kThreads, 1) mla_split_kernel(const MlaParams 
       *reinterpret_cast<uint4*>(Cs + t * kStride + col) = lo4;
       *reinterpret_cast<uint4*>(Cs + t * kStride + col + 8) = hi4;
     }
-    for (int e = tid; e < kBs * kGroups; e += kThreads) Ss[e] = (e / kGroups) < valid ? sc[e] : 0.f;
+    for (int e = tid; e < kBs * kGroups; e += kThreads)
+      Ss[e] = (e / kGroups) < valid ? sc[SEG ? 0 : e] : 0.f;
     __syncthreads();
     // the stage is consumed: refill it with the page two ahead
     if (ip < n_units) {
@@ -478,9 +485,12 @@ cudaError_t launch_decode_mla(const DecodeShape& s, const DecodeArgs& a, cudaStr
   const int H = s.hq / kHeads;
   const int ranges = s.workers / H;
   const int smem = MlaSmem::kBytes;
-  auto kfn = a.fmt == FP8PA_E4M3   ? mla_split_kernel<FP8PA_E4M3>
-             : a.fmt == FP8PA_E5M2 ? mla_split_kernel<FP8PA_E5M2>
-                                   : mla_split_kernel<FP8PA_INT8>;
+  const bool seg = a.mode == FP8PA_SCALE_SEGMENT;
+  auto kfn = a.fmt == FP8PA_E4M3
+                 ? (seg ? mla_split_kernel<FP8PA_E4M3, true> : mla_split_kernel<FP8PA_E4M3, false>)
+             : a.fmt == FP8PA_E5M2
+                 ? (seg ? mla_split_kernel<FP8PA_E5M2, true> : mla_split_kernel<FP8PA_E5M2, false>)
+                 : (seg ? mla_split_kernel<FP8PA_INT8, true> : mla_split_kernel<FP8PA_INT8, false>);
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kfn), smem);
   if (e != cudaSuccess) return e;
   char* ws = static_cast<char*>(a.workspace);

@@ -11,16 +11,18 @@
 // the library.
 //
 // The array is a file-scope static __device__ buffer of
-// FP8PA_STATIC_WORKSPACE_BYTES.  Its device address is looked up once per
-// device (cudaGetSymbolAddress, with that device current) on the first call
-// made on that device; make that first call before any stream capture.  All
-// calls on a device share the one array and it keeps whatever the last call
-// left there: nothing in it has to start at zero, because every byte the
-// decode reads from its workspace is written earlier in the same call.  Two
-// calls whose kernels overlap on the GPU (different streams, no ordering
+// FP8PA_STATIC_WORKSPACE_BYTES.  In host code its name is only a host-side
+// stand-in, so its device address is looked up (cudaGetSymbolAddress, with
+// the device current) on every call made outside stream capture; a call
+// made during a capture uses the address the last uncaptured call on that
+// device found, so make the first call on each device before any capture.
+// Looking it up again each time keeps the call correct after a
+// cudaDeviceReset, which reloads the library's module at a new address.
+// All calls on a device share the one array and it keeps whatever the last
+// call left there: nothing in it has to start at zero, because every byte
+// the decode reads from its workspace is written earlier in the same call.
+// Two calls whose kernels overlap on the GPU (different streams, no ordering
 // between them) race on the array and give undefined results.
-#include <mutex>
-
 #include "common.cuh"
 #include "internal.h"
 
@@ -29,23 +31,7 @@ namespace {
 
 static __device__ __align__(256) unsigned char g_static_workspace[FP8PA_STATIC_WORKSPACE_BYTES];
 
-constexpr int kMaxDevs = 64;
-void* g_static_ws_addr[kMaxDevs] = {nullptr};
-std::mutex g_static_ws_mu;
-
-// Device address of the array on the current device (set up on first use).
-int static_workspace(void** out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevs) return FP8PA_ERR_CUDA;
-  std::lock_guard<std::mutex> lock(g_static_ws_mu);
-  if (!g_static_ws_addr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_static_workspace) != cudaSuccess || !p) return FP8PA_ERR_CUDA;
-    g_static_ws_addr[dev] = p;
-  }
-  *out = g_static_ws_addr[dev];
-  return FP8PA_OK;
-}
+void* g_static_ws_addr[kMaxDevices] = {nullptr};
 
 }  // namespace
 }  // namespace fp8pa
@@ -56,14 +42,13 @@ extern "C" int fp8pa_paged_decode_attention_static_ws(
     const int32_t* seq_lens, int batch, int block_size, int n_q_heads, int n_kv_heads,
     int head_dim, int head_dim_v, int fmt, int scale_mode, int group_size, float sm_scale,
     int num_blocks, void* out, int out_dtype, void* stream) {
-  void* ws = nullptr;
-  const int st = fp8pa::static_workspace(&ws);
-  if (st != FP8PA_OK) return st;
-  // The size the regular decode needs for these shapes on this device (0
-  // when the shapes are rejected; the call below then returns the reason).
-  const size_t need = fp8pa_decode_workspace_bytes(batch, n_q_heads, n_kv_heads, head_dim,
-                                                   head_dim_v, block_size, max_blocks_per_seq);
-  if (need > FP8PA_STATIC_WORKSPACE_BYTES) return FP8PA_ERR_WORKSPACE;
+  void* ws = fp8pa::symbol_device_address(
+      reinterpret_cast<const void*>(&fp8pa::g_static_workspace), fp8pa::g_static_ws_addr,
+      static_cast<cudaStream_t>(stream), nullptr);
+  if (!ws) return FP8PA_ERR_CUDA;
+  // The regular decode checks this call's own need (its format, scale mode
+  // and split) against the array's size and returns FP8PA_ERR_WORKSPACE,
+  // launching nothing, when it does not fit.
   return fp8pa_paged_decode_attention(q, k_cache, v_cache, k_scale, v_scale, block_tables,
                                       max_blocks_per_seq, seq_lens, batch, block_size, n_q_heads,
                                       n_kv_heads, head_dim, head_dim_v, fmt, scale_mode,

@@ -9,16 +9,67 @@
 
 namespace fp8pa {
 
+constexpr int kMaxDevices = 64;
+
+// Device address of a __device__ variable (`symbol`, its host-side name) on
+// the current device: looked up again on every call made outside stream
+// capture; during a capture, the address the last uncaptured call on this
+// device recorded in cache[device] (kMaxDevices entries) is used.  NULL on
+// failure.
+void* symbol_device_address(const void* symbol, void** cache, cudaStream_t stream,
+                            int* dev_out);
+
+// Division of a non-negative 32-bit integer by a divisor d >= 1 fixed for a
+// launch, as a multiply-high and two shifts (Granlund and Montgomery,
+// "Division by invariant integers using multiplication", PLDI 1994, the
+// N = 32 case of their unsigned algorithm); the magic number is made once
+// on the host by make_fast_div.
+struct FastDiv {
+  uint32_t m;  // multiplier
+  uint32_t s;  // ceil(log2 d)
+};
+inline FastDiv make_fast_div(uint32_t d) {
+  uint32_t s = 0;
+  while ((1ull << s) < d) ++s;
+  const uint64_t m = ((1ull << 32) * ((1ull << s) - d)) / d + 1;
+  return FastDiv{static_cast<uint32_t>(m), s};
+}
+__device__ __forceinline__ uint32_t fast_div(uint32_t n, FastDiv f) {
+  if (f.s == 0) return n;
+  const uint32_t t = __umulhi(f.m, n);
+  return (t + ((n - t) >> 1)) >> (f.s - 1);
+}
+
 struct AppendArgs {
   const uint16_t* src[2];   // k, v rows (bf16 bits), [num_tokens][hkv][d]
   uint8_t* cache[2];        // k, v codes
   float* scale[2];          // k, v scales (written, or read in CHANNEL_STATIC)
   const int32_t* slot_mapping;
   int num_tokens, hkv, d, ntens, gs, num_blocks, bs;
+  FastDiv div_tok;          // by hkv * ntens (rows of a token)
+  FastDiv div_bs;           // by bs
   uint32_t* err;
 };
 
 cudaError_t launch_append(const AppendArgs& a, int fmt, int mode, cudaStream_t stream);
+
+// The segment-scale append (block-wise cumulative rescaling): tokens per
+// segment, and the arguments of one call (sequence r owns rows
+// seq_offsets[r] .. seq_offsets[r+1]-1 at positions seq_start[r] + 0, 1, ...).
+constexpr int kSegmentTokens = 1024;
+inline int segment_scale_heads(int hkv) { return (hkv + 3) / 4 * 4; }
+struct SegmentArgs {
+  const uint16_t* src[2];  // k, v rows (bf16 bits), [num_tokens][hkv][d]
+  uint8_t* cache[2];       // k, v codes
+  float* scale[2];         // k, v page scales [num_blocks][segment_scale_heads(hkv)]
+  const int32_t* slot_mapping;
+  const int32_t* seq_offsets;
+  const int32_t* seq_start;
+  float* state;            // [num_seqs][2][hkv][2]: running absmax, segment scale
+  int num_seqs, hkv, hp, d, ntens, num_blocks, bs;
+  uint32_t* err;
+};
+cudaError_t launch_append_segment(const SegmentArgs& a, int fmt, cudaStream_t stream);
 
 // The planner's inputs (see plan.cuh); `plan` is the head of the workspace.
 struct PlanArgs {

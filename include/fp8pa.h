@@ -43,6 +43,9 @@
  *   MX_BLOCK scale   u8  [num_blocks][n_kv_heads][block_size][head_dim/group_size]
  *                        (E8M0: byte b is the power of two 2^(b - 127); the
  *                        float* scale arguments then carry this byte buffer)
+ *   SEGMENT scale    f32 [num_blocks][round_up(n_kv_heads, 4)]  (one 16-byte-
+ *                        aligned row of page scales per block; the padding
+ *                        entries are never read)
  *   slot s           -> block s / block_size, offset s % block_size
  *   block_tables     i32 [batch][max_blocks_per_seq]; token t of request b
  *                        lives in block block_tables[b][t / block_size]
@@ -88,6 +91,10 @@ extern "C" {
 #define FP8PA_SCALE_CHANNEL_STATIC 1 /* static: caller-given f32 per (kv head, dim), read only   */
 #define FP8PA_SCALE_TOKEN_GROUP 2    /* dynamic: one f32 per (token, kv head, group of dims)     */
 #define FP8PA_SCALE_MX_BLOCK 3       /* dynamic: one E8M0 byte per (token, kv head, 16/32 dims)  */
+#define FP8PA_SCALE_SEGMENT 4        /* cumulative: one f32 per (page, kv head), 1024-token segments */
+
+/* Tokens per segment of FP8PA_SCALE_SEGMENT. */
+#define FP8PA_SEGMENT_TOKENS 1024
 
 /* Output element types of the decode. */
 #define FP8PA_OUT_BF16 0
@@ -135,6 +142,51 @@ int fp8pa_kv_append_quant(const void* k, const void* v, const int32_t* slot_mapp
                           int num_tokens, int n_kv_heads, int head_dim, int fmt, int scale_mode,
                           int group_size, uint8_t* k_cache, uint8_t* v_cache, float* k_scale,
                           float* v_scale, int num_blocks, int block_size, void* stream);
+
+/*
+ * Append with block-wise cumulative rescaling (FP8PA_SCALE_SEGMENT).
+ * Defined by: "DeepSeek V4 950: whole-network FP8 dataflow"
+ * (2kiu.com/news/4508674) sec. 4.3 -- the KV cache is cut into length
+ * blocks, each keeps a cumulative scale that decode re-aligns by, and an
+ * extra offset beyond the per-head scale is refreshed every 1024 tokens.
+ * The page gives no formula; this library's reading:
+ *   per (sequence, K or V, kv head) a running absmax R covers every token
+ *   appended so far (restarting at position 0).  Appending the token at
+ *   position p sets R = max(R, absmax(row)); if p is a multiple of
+ *   FP8PA_SEGMENT_TOKENS the token opens a segment and its scale is frozen
+ *   as S = max(R / FMAX, 1e-12) (IEEE fp32 division).  Every token of the
+ *   segment is coded as fp8_rne_satfinite(x / S) (INT8: as in
+ *   fp8pa_kv_append_quant) and each page stores S once per kv head.
+ *   A value beyond S * FMAX inside a segment saturates; the next segment's
+ *   scale covers it.
+ *
+ * k, v           bf16 [num_tokens][n_kv_heads][head_dim]; v may be NULL.
+ * seq_offsets    i32 [num_seqs + 1] (device): sequence r owns rows
+ *                seq_offsets[r] .. seq_offsets[r+1]-1, in position order.
+ * seq_start_pos  i32 [num_seqs] (device): position of sequence r's first
+ *                row in this call (its cached length before the call).
+ * slot_mapping   i32 [num_tokens]; a negative slot, or one past the pool
+ *                (flagged FP8PA_DEVERR_SLOT_RANGE), skips the token: it
+ *                neither raises R nor opens its segment.
+ * seg_state      f32 [num_seqs][2][n_kv_heads][2] (device, caller-owned):
+ *                (R, S) of each (sequence, K or V, head), carried between
+ *                calls; row r belongs to the call's sequence r, so a caller
+ *                that reorders its batch reorders these rows with it.  Rows
+ *                of a sequence starting at position 0 need no initialisation.
+ * k_scale, v_scale  f32 [num_blocks][round_up(n_kv_heads, 4)]: written.
+ * Requirements   block_size divides FP8PA_SEGMENT_TOKENS; head_dim % 16 == 0,
+ *                head_dim <= 768; 16-byte aligned k, v, caches and scales.
+ * Codes and scales are bit-exact with the definition above, whatever the
+ * split of a sequence's tokens into calls.  Decode reads the page scales
+ * with scale_mode FP8PA_SCALE_SEGMENT.  Calls that touch the same sequence
+ * must be stream-ordered.
+ */
+int fp8pa_kv_append_quant_segment(const void* k, const void* v, const int32_t* slot_mapping,
+                                  const int32_t* seq_offsets, const int32_t* seq_start_pos,
+                                  int num_seqs, int n_kv_heads, int head_dim, int fmt,
+                                  float* seg_state, uint8_t* k_cache, uint8_t* v_cache,
+                                  float* k_scale, float* v_scale, int num_blocks, int block_size,
+                                  void* stream);
 
 /*
  * Static per-channel scales for CHANNEL_STATIC mode: for every (kv head, dim)
@@ -204,12 +256,12 @@ size_t fp8pa_multiquery_workspace_bytes(int batch, int q_len, int n_q_heads, int
  * Two layouts are served:
  *  GQA  n_q_heads % n_kv_heads == 0, n_q_heads/n_kv_heads <= 8, head_dim in
  *       {64, 128}, head_dim_v == head_dim, block_size in {16, 32, 64},
- *       scale_mode TOKEN_HEAD, CHANNEL_STATIC or MX_BLOCK (group_size 16
- *       or 32, FP8 codes), separate v_cache/v_scale.
+ *       scale_mode TOKEN_HEAD, CHANNEL_STATIC, MX_BLOCK (group_size 16
+ *       or 32, FP8 codes) or SEGMENT, separate v_cache/v_scale.
  *  MLA  n_kv_heads == 1, head_dim 576 (512 latent + 64 rope), head_dim_v
  *       512 (the first 512 dims of the same latent), v_cache == k_cache,
- *       v_scale == k_scale, scale_mode TOKEN_GROUP, group_size 64,
- *       block_size 64, n_q_heads a multiple of 32.
+ *       v_scale == k_scale, scale_mode TOKEN_GROUP (group_size 64) or
+ *       SEGMENT, block_size 64, n_q_heads a multiple of 32.
  *
  * fmt          FP8PA_E4M3, FP8PA_E5M2 or FP8PA_INT8: the codes as
  *              fp8pa_kv_append_quant wrote them (decoded exactly to f16).
@@ -277,7 +329,8 @@ int fp8pa_paged_multiquery_attention(const void* q, const uint8_t* k_cache,
  * hotelren.com/news/5711065, sec. 3.3: paged KV blocks).
  * Arguments, layouts, errors: those of the two calls; the cache and scale
  * tensors are shared by both.  Nothing is launched if either argument set
- * is rejected.
+ * is rejected.  FP8PA_SCALE_SEGMENT is not served here (its append needs
+ * token positions: call fp8pa_kv_append_quant_segment, then the attention).
  */
 int fp8pa_decode_step(const void* k_new, const void* v_new, const int32_t* slot_mapping,
                       int num_new_tokens, const void* q, uint8_t* k_cache, uint8_t* v_cache,
@@ -290,7 +343,11 @@ int fp8pa_decode_step(const void* k_new, const void* v_new, const int32_t* slot_
 
 /*
  * Size of the scratch array built into the library for
- * fp8pa_paged_decode_attention_static_ws (16 MiB per device that uses it).
+ * fp8pa_paged_decode_attention_static_ws.  The array is reserved on a device
+ * when the library's module is loaded there: on its first use under lazy
+ * module loading (the CUDA default), at context creation under
+ * CUDA_MODULE_LOADING=EAGER, whether or not this call is ever made.  It is
+ * held until the process exits (or the device is reset).
  */
 #define FP8PA_STATIC_WORKSPACE_BYTES (16u << 20)
 
@@ -306,13 +363,17 @@ int fp8pa_decode_step(const void* k_new, const void* v_new, const int32_t* slot_
  * FP8PA_STATIC_WORKSPACE_BYTES inside the library, so the call allocates
  * nothing (no cudaMalloc, no allocator of any library).  The caller still
  * owns every input and the output.
- *  - The first call on each device looks up the array's device address (with
- *    that device current); make that first call before any stream capture.
+ *  - Every call made outside stream capture looks the array's device address
+ *    up again (with the calling device current), so a device reset between
+ *    calls is safe.  A call made during a capture reuses the address the
+ *    last uncaptured call on that device found: make the first call on each
+ *    device before any stream capture.
  *  - Every call on a device shares the one array; calls whose kernels may
  *    overlap on the GPU (unordered streams) race and give undefined output.
  *    Nothing in the array needs clearing between calls.
- *  - Shapes whose workspace (fp8pa_decode_workspace_bytes) exceeds
- *    FP8PA_STATIC_WORKSPACE_BYTES return FP8PA_ERR_WORKSPACE and launch
+ *  - A call whose own workspace need (for its shapes, format, scale mode and
+ *    split; at most fp8pa_decode_workspace_bytes) exceeds
+ *    FP8PA_STATIC_WORKSPACE_BYTES returns FP8PA_ERR_WORKSPACE and launches
  *    nothing; other errors are those of fp8pa_paged_decode_attention.
  */
 int fp8pa_paged_decode_attention_static_ws(const void* q, const uint8_t* k_cache,
@@ -342,20 +403,28 @@ int fp8pa_get_device_error(void* stream, uint32_t* flags);
 int fp8pa_selftest_bounded_wait(long long limit_cycles, void* stream);
 
 /*
- * Tuning and testing knob: the number of split workers the decode uses
- * (0 = one per resident warp slot on the device, the default).  It changes
- * how the sequences are cut into partials, never the result beyond fp32
- * rounding.  Process-wide; set it between calls, not during them.  It also
- * changes fp8pa_decode_workspace_bytes().
+ * TESTING AND BENCHMARKING ONLY -- not for production callers.
+ * The two calls below set process-global state that every later decode call
+ * of every thread reads, with no synchronisation: they are not thread-safe,
+ * and a change made while another thread is inside a decode call, or while
+ * a decode call is being captured into a CUDA graph, has undefined effect.
+ * Set them only while no other thread uses the library.
+ */
+
+/*
+ * Test hook: the number of split workers the decode uses (0 = one per
+ * resident warp slot on the device, the default).  It changes how the
+ * sequences are cut into partials, never the result beyond fp32 rounding;
+ * the tests use it to run every kind of page range.  It also changes
+ * fp8pa_decode_workspace_bytes().
  */
 int fp8pa_set_decode_workers(int workers);
 
 /*
  * Measurement hook: when both events are non-NULL (cudaEvent_t handles),
- * every later fp8pa_paged_decode_attention call records `start` on its
- * stream immediately before its split kernel and `stop` immediately after
- * it, so a caller can time the dominant kernel alone.  NULL, NULL turns it
- * off.  Process-wide; set it between calls.
+ * every later decode call records `start` on its stream immediately before
+ * its split kernel and `stop` immediately after it, so a benchmark can time
+ * the dominant kernel alone.  NULL, NULL turns it off.
  */
 int fp8pa_set_split_events(void* start, void* stop);
 

@@ -77,6 +77,8 @@ def gpu_cache(w, F, kvs=None, step=True, back=1):
     vc = None if w.mla else torch.zeros_like(kc)
     if kvs is None:
         kvs = [W.request_kv(w, b) for b in range(w.batch)]
+    if w.scale_mode == W.SCALE_SEGMENT:
+        return _gpu_cache_segment(w, F, kvs, kc, vc, step, back)
     if w.scale_mode == W.SCALE_CHANNEL_STATIC:
         ks = F.kv_channel_scales(to_dev_bf16(np.concatenate([k for k, _ in kvs])), w.fmt)
         vs = F.kv_channel_scales(to_dev_bf16(np.concatenate([v for _, v in kvs])), w.fmt)
@@ -107,6 +109,40 @@ def gpu_cache(w, F, kvs=None, step=True, back=1):
     return kc, vc, ks, vs
 
 
+def _gpu_cache_segment(w, F, kvs, kc, vc, step, back):
+    """The segment-scale cache: one prefill call over every request (all but
+    its last `back` tokens), then (step=True) one decode-step call appending
+    each request's last token at its position, with the running state
+    carried between the calls."""
+    nb, hkv = w.num_blocks, w.n_kv_heads
+    hp = F.segment_scale_heads(hkv)
+    ks = torch.zeros((nb, hp), dtype=torch.float32, device=DEV)
+    vs = None if w.mla else torch.zeros_like(ks)
+    state = torch.zeros((w.batch, 2, hkv, 2), dtype=torch.float32, device=DEV)
+    lens = [int(L) for L in w.seq_lens]
+    n = [max(L - back, 0) for L in lens]
+
+    def call(rows_k, rows_v, slots, counts, starts):
+        off = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+        F.kv_append_quant_segment(to_dev_bf16(np.concatenate(rows_k)),
+                                  None if w.mla else to_dev_bf16(np.concatenate(rows_v)),
+                                  torch.from_numpy(np.concatenate(slots).astype(np.int32)).to(DEV),
+                                  torch.from_numpy(off).to(DEV),
+                                  torch.from_numpy(np.asarray(starts, np.int32)).to(DEV),
+                                  kc, vc, ks, vs, state, fmt=w.fmt)
+    call([k[:m] for (k, _), m in zip(kvs, n)],
+         None if w.mla else [v[:m] for (_, v), m in zip(kvs, n)],
+         [W.token_slots(w, b, 0, m) for b, m in enumerate(n)], n, [0] * w.batch)
+    if step:
+        call([k[m:L] for (k, _), m, L in zip(kvs, n, lens)],
+             None if w.mla else [v[m:L] for (_, v), m, L in zip(kvs, n, lens)],
+             [W.token_slots(w, b, m, L) for b, (m, L) in enumerate(zip(n, lens))],
+             [L - m for m, L in zip(n, lens)], n)
+    if w.mla:
+        return kc, kc, ks, ks
+    return kc, vc, ks, vs
+
+
 def oracle_cache(w, kvs=None, requests=None):
     """The same cache built by the oracle on the host (all requests, or only
     `requests`; static channel scales always from every request)."""
@@ -115,6 +151,18 @@ def oracle_cache(w, kvs=None, requests=None):
     vc = None if w.mla else np.zeros_like(kc)
     if kvs is None:
         kvs = [W.request_kv(w, b) for b in range(w.batch)]
+    if w.scale_mode == W.SCALE_SEGMENT:
+        hp = oracle.segment_scale_heads(hkv)
+        ks = np.zeros((nb, hp), np.float32)
+        vs = None if w.mla else np.zeros_like(ks)
+        for b, (k, v) in enumerate(kvs):
+            if requests is not None and b not in requests:
+                continue
+            L = int(w.seq_lens[b])
+            st = np.zeros((1, 2, hkv, 2), np.float32)
+            assert oracle.kv_append_quant_segment(k, v, W.token_slots(w, b, 0, L), [0, L], [0],
+                                                  w.fmt, st, kc, vc, ks, vs, bs) == 0
+        return (kc, kc, ks, ks) if w.mla else (kc, vc, ks, vs)
     if w.scale_mode == W.SCALE_CHANNEL_STATIC:
         ks = oracle.kv_channel_scales(np.concatenate([k for k, _ in kvs]), w.fmt)
         vs = oracle.kv_channel_scales(np.concatenate([v for _, v in kvs]), w.fmt)
