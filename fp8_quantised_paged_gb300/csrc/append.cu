@@ -39,13 +39,20 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float (&f)[8]) {
   }
 }
 
-// Lanes per row: a sub-group of LPR lanes (a power of two >= 8, at most 32)
-// appends one row; a lane owns chunks sl, sl + LPR, ... (R of them) of the
-// row's 16-byte chunks, so a warp covers 32 / LPR rows per step.
+// Lanes per row: a sub-group of LPR lanes (a power of two, at most 32)
+// appends one row; a lane owns R of the row's 16-byte chunks -- chunks sl,
+// sl + LPR, ... (strided, CONSEC false), or R consecutive chunks sl * R ..
+// sl * R + R - 1 (CONSEC true: the bulk kernel's per-token and static-channel
+// modes, where fewer lanes per row spread each row's bookkeeping over more
+// values) -- so a warp covers 32 / LPR rows per step.
+template <int LPR, int R, bool CONSEC>
+__device__ __forceinline__ int chunk_of(int sl, int r) {
+  return CONSEC ? sl * R + r : sl + LPR * r;
+}
 
 // Row `row` of the call: its (K-or-V, head) index `rem` (-1 past the end), its
 // slot, and its values (zeros where the lane has no chunk).
-template <int LPR, int R>
+template <int LPR, int R, bool CONSEC = false>
 __device__ __forceinline__ void load_row(const AppendArgs& a, long row, int sl, float (&v)[R][8],
                                          int& rem, int& slot) {
   const int per_tok = a.hkv * a.ntens;
@@ -62,7 +69,7 @@ __device__ __forceinline__ void load_row(const AppendArgs& a, long row, int sl, 
   const int nch = a.d / 8;
 #pragma unroll
   for (int r = 0; r < R; ++r) {
-    const int ci = sl + LPR * r;
+    const int ci = chunk_of<LPR, R, CONSEC>(sl, r);
     if (in && ci < nch) {
       bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>(x + ci * 8)), v[r]);
     } else {
@@ -75,9 +82,12 @@ __device__ __forceinline__ void load_row(const AppendArgs& a, long row, int sl, 
 // Scale, round and scatter one loaded row (the whole sub-group joins the
 // shuffles, also for rows that are skipped: past the end, a negative slot,
 // or a slot past the pool).
-template <int FMT, int MODE, int LPR, int R>
+template <int FMT, int MODE, int LPR, int R, bool CONSEC = false>
 __device__ __forceinline__ void store_row(const AppendArgs& a, const float (&v)[R][8], int rem,
                                           int slot, int sl) {
+  // per-group modes need the chunks of a group on consecutive lanes
+  static_assert(!CONSEC || MODE == FP8PA_SCALE_TOKEN_HEAD || MODE == FP8PA_SCALE_CHANNEL_STATIC,
+                "consecutive chunks serve the per-token and static-channel modes only");
   constexpr float kFmax = code_max<FMT>();
   constexpr int kEmax = FMT == FP8PA_E4M3 ? 8 : 15;  // exponent of the largest normal
   const int nch = a.d / 8;
@@ -145,7 +155,7 @@ __device__ __forceinline__ void store_row(const AppendArgs& a, const float (&v)[
 
 #pragma unroll
   for (int r = 0; r < R; ++r) {
-    const int ci = sl + LPR * r;
+    const int ci = chunk_of<LPR, R, CONSEC>(sl, r);
     if (ci >= nch) continue;
     float q[8];
     if constexpr (MODE == FP8PA_SCALE_CHANNEL_STATIC) {
@@ -192,10 +202,13 @@ __global__ void __launch_bounds__(kAppendWarps * 32) append_kernel(AppendArgs a)
 // Many rows (a prefill): a persistent grid whose warps stride over the
 // steps of rows with a ring of kStreamDepth steps in registers -- a step's
 // loads are issued kStreamDepth - 1 steps before the warp works on it, so
-// loads stay in flight while the warp scales and rounds.
-constexpr int kStreamDepth = 3;
+// loads stay in flight while the warp scales and rounds.  The kernel is
+// bound by instruction issue (two IEEE divisions' worth of work per value
+// for bit-exact codes), so its rows are spread over few lanes, each with
+// several 16-byte chunks, to share every row's index arithmetic.
+constexpr int kStreamDepth = 2;
 
-template <int FMT, int MODE, int LPR, int R>
+template <int FMT, int MODE, int LPR, int R, bool CONSEC>
 __global__ void __launch_bounds__(kAppendWarps * 32) append_stream_kernel(AppendArgs a) {
   griddep_wait();
   griddep_launch_dependents();
@@ -207,14 +220,15 @@ __global__ void __launch_bounds__(kAppendWarps * 32) append_stream_kernel(Append
   float v[P][R][8];
   int rem[P], slot[P];
 #pragma unroll
-  for (int p = 0; p < P; ++p) load_row<LPR, R>(a, (first + p * stride) * SG + sg, sl, v[p], rem[p], slot[p]);
+  for (int p = 0; p < P; ++p)
+    load_row<LPR, R, CONSEC>(a, (first + p * stride) * SG + sg, sl, v[p], rem[p], slot[p]);
   for (long s0 = first; s0 < nsteps; s0 += P * stride) {
 #pragma unroll
     for (int p = 0; p < P; ++p) {
       const long st = s0 + p * stride;
       if (st >= nsteps) break;  // warp-uniform
-      store_row<FMT, MODE, LPR, R>(a, v[p], rem[p], slot[p], sl);
-      load_row<LPR, R>(a, (st + P * stride) * SG + sg, sl, v[p], rem[p], slot[p]);
+      store_row<FMT, MODE, LPR, R, CONSEC>(a, v[p], rem[p], slot[p], sl);
+      load_row<LPR, R, CONSEC>(a, (st + P * stride) * SG + sg, sl, v[p], rem[p], slot[p]);
     }
   }
 }
@@ -238,7 +252,7 @@ __global__ void __launch_bounds__(kAppendWarps * 32) append_plan_kernel(AppendAr
 // Calls of at least this many rows stream through the persistent kernel.
 constexpr long kBulkRows = 16384;
 
-template <int FMT, int MODE, int LPR, int R>
+template <int FMT, int MODE, int LPR, int R, int SLPR, int SR, bool SCONSEC>
 cudaError_t launch_append_shape(const AppendArgs& a, const PlanArgs* pl, cudaStream_t stream) {
   const long rows = static_cast<long>(a.num_tokens) * a.hkv * a.ntens;
   if (rows == 0 && !pl) return cudaSuccess;
@@ -257,12 +271,14 @@ cudaError_t launch_append_shape(const AppendArgs& a, const PlanArgs* pl, cudaStr
     return cudaLaunchKernelEx(&cfg, append_plan_kernel<FMT, MODE, LPR, R>, a, *pl);
   }
   if (rows >= kBulkRows) {
-    const auto fn = append_stream_kernel<FMT, MODE, LPR, R>;
+    const auto fn = append_stream_kernel<FMT, MODE, SLPR, SR, SCONSEC>;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+    constexpr long kStreamRowsPerCta = static_cast<long>(kAppendWarps) * (32 / SLPR);
+    const long sctas = (rows + kStreamRowsPerCta - 1) / kStreamRowsPerCta;
     const long resident = static_cast<long>(sm_count(dev)) *
                           ctas_per_sm(reinterpret_cast<const void*>(fn), kAppendWarps * 32, 0);
-    cfg.gridDim = dim3(static_cast<unsigned>(ctas < resident ? ctas : resident));
+    cfg.gridDim = dim3(static_cast<unsigned>(sctas < resident ? sctas : resident));
     return cudaLaunchKernelEx(&cfg, fn, a);
   }
   cfg.gridDim = dim3(static_cast<unsigned>(ctas));
@@ -271,15 +287,24 @@ cudaError_t launch_append_shape(const AppendArgs& a, const PlanArgs* pl, cudaStr
 
 // pl == nullptr: the append alone; else the fused append + plan prologue.
 // Lanes per row follow the row's 16-byte chunks (head_dim / 8): 8 lanes up
-// to head_dim 64, 16 at 128, 32 (with 2 or 3 chunks each) beyond 256.
+// to head_dim 64, 16 at 128, 32 (with 2 or 3 chunks each) beyond 256.  The
+// bulk kernel gives a lane 4 consecutive chunks in the per-token and
+// static-channel modes (4 lanes per row at head_dim 128).
 template <int FMT, int MODE>
 cudaError_t launch_append_r(const AppendArgs& a, const PlanArgs* pl, cudaStream_t stream) {
   const int nch = a.d / 8;
-  if (nch <= 8) return launch_append_shape<FMT, MODE, 8, 1>(a, pl, stream);
-  if (nch <= 16) return launch_append_shape<FMT, MODE, 16, 1>(a, pl, stream);
-  if (nch <= 32) return launch_append_shape<FMT, MODE, 32, 1>(a, pl, stream);
-  if (nch <= 64) return launch_append_shape<FMT, MODE, 32, 2>(a, pl, stream);
-  return launch_append_shape<FMT, MODE, 32, 3>(a, pl, stream);
+  if constexpr (MODE == FP8PA_SCALE_TOKEN_HEAD || MODE == FP8PA_SCALE_CHANNEL_STATIC) {
+    if (nch <= 8) return launch_append_shape<FMT, MODE, 8, 1, 2, 4, true>(a, pl, stream);
+    if (nch <= 16) return launch_append_shape<FMT, MODE, 16, 1, 4, 4, true>(a, pl, stream);
+    if (nch <= 32) return launch_append_shape<FMT, MODE, 32, 1, 8, 4, true>(a, pl, stream);
+    if (nch <= 64) return launch_append_shape<FMT, MODE, 32, 2, 16, 4, true>(a, pl, stream);
+  } else {
+    if (nch <= 8) return launch_append_shape<FMT, MODE, 8, 1, 8, 1, false>(a, pl, stream);
+    if (nch <= 16) return launch_append_shape<FMT, MODE, 16, 1, 16, 1, false>(a, pl, stream);
+    if (nch <= 32) return launch_append_shape<FMT, MODE, 32, 1, 32, 1, false>(a, pl, stream);
+    if (nch <= 64) return launch_append_shape<FMT, MODE, 32, 2, 32, 2, false>(a, pl, stream);
+  }
+  return launch_append_shape<FMT, MODE, 32, 3, 32, 3, false>(a, pl, stream);
 }
 
 template <int FMT>
