@@ -207,6 +207,8 @@ DecodePath decode_path(int batch, int hq, int hkv, int d, int dv, int bs, int ma
     if (hkv != 1 || dv != 512 || bs != 64 || hq % 32 != 0 ||
         !((mode == FP8PA_SCALE_TOKEN_GROUP && gs == 64) || mode == FP8PA_SCALE_SEGMENT))
       r.status = FP8PA_ERR_UNSUPPORTED;
+    // FP8 latents with whole groups of 64 heads run on the tensor cores
+    s.mla_tc = (fmt != FP8PA_INT8 && hq % 64 == 0) ? 1 : 0;
     return r;
   }
   if ((d != 64 && d != 128) || dv != d || (bs != 16 && bs != 32 && bs != 64) || hq / hkv > 8 ||
@@ -567,6 +569,7 @@ int fp8pa_decode_step(const void* k_new, const void* v_new, const int32_t* slot_
   pl.bs = plan_block_size(path.shape);
   pl.max_blocks = max_blocks_per_seq;
   pl.workers = plan_workers(path.shape);
+  pl.upages = plan_unit_pages(path.shape);
   pl.plan = static_cast<int*>(workspace);
   pl.err = a.err;
   cudaError_t e = launch_append_plan(ap, fmt, scale_mode, pl, cs);

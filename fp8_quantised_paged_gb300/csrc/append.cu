@@ -242,7 +242,7 @@ __global__ void __launch_bounds__(kAppendWarps * 32) append_plan_kernel(AppendAr
   if (blockIdx.x == 0) {
     if (threadIdx.x < 32)
       plan_warp(pl.seq_lens, pl.batch, pl.qlen, pl.qw, 1, pl.bs, pl.max_blocks, pl.workers,
-                pl.plan, pl.err);
+                pl.plan, pl.err, pl.upages);
     return;
   }
   append_step<FMT, MODE, LPR, R>(

@@ -57,10 +57,11 @@ __device__ __forceinline__ int ld_i32(const int* p) { return *reinterpret_cast<c
 // One warp; lets the split kernel launch at once (it waits for the plan).
 __global__ void __launch_bounds__(32) plan_kernel(const int32_t* seq_lens, int B, int qlen,
                                                   int qw, int groups, int bs, int max_blocks,
-                                                  int workers, int* ws, uint32_t* err) {
+                                                  int workers, int* ws, uint32_t* err,
+                                                  int upages) {
   griddep_wait();  // inputs may come from the kernel before us in the stream
   griddep_launch_dependents();
-  plan_warp(seq_lens, B, qlen, qw, groups, bs, max_blocks, workers, ws, err);
+  plan_warp(seq_lens, B, qlen, qw, groups, bs, max_blocks, workers, ws, err, upages);
 }
 
 // ---------------------------------------------------------------- split kernel
@@ -830,8 +831,9 @@ cudaEvent_t g_split_ev_start = nullptr, g_split_ev_stop = nullptr;
 int decode_workers(const DecodeShape& s, int fmt, int mode, int device) {
   const int sms = sm_count(device);
   if (s.mla) {
-    // one 202 KB CTA per SM; a whole number of head-group sets (H = Hq / 32)
-    const int H = s.hq / 32;
+    // one CTA per SM (202 or 221 KB of shared memory); a whole number of
+    // head-group sets (H = Hq / 32, or Hq / 64 on tensor cores)
+    const int H = s.hq / mla_group_heads(s);
     int ranges = (g_decode_workers_override > 0 ? g_decode_workers_override : sms) / H;
     return (ranges < 1 ? 1 : ranges) * H;
   }
@@ -848,7 +850,7 @@ int decode_workers(const DecodeShape& s, int fmt, int mode, int device) {
 // each piece holds one row per head group (KV head for GQA, 32-head group for
 // MLA) and query head of the group.
 size_t decode_workspace_bytes(const DecodeShape& s) {
-  const int groups = s.mla ? s.hq / 32 : s.hkv;
+  const int groups = s.mla ? s.hq / mla_group_heads(s) : s.hkv;
   const int G = s.hq / groups;
   const int qw = s.mla ? 1 : gqa_qw(s);
   const size_t bp = s.batch / qw;  // planned requests
@@ -935,7 +937,7 @@ cudaError_t launch_decode_gqa(const DecodeShape& s, const DecodeArgs& a, cudaStr
 
 cudaError_t launch_plan(const int32_t* seq_lens, int batch, int qlen, int qw, int groups, int bs,
                         int max_blocks, int workers, int* plan, uint32_t* err,
-                        cudaStream_t stream) {
+                        cudaStream_t stream, int upages) {
   cudaLaunchAttribute pdl[1];
   pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   pdl[0].val.programmaticStreamSerializationAllowed = 1;
@@ -946,7 +948,7 @@ cudaError_t launch_plan(const int32_t* seq_lens, int batch, int qlen, int qw, in
   cfg.attrs = pdl;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, plan_kernel, seq_lens, batch, qlen, qw, groups, bs, max_blocks,
-                            workers, plan, err);
+                            workers, plan, err, upages);
 }
 
 }  // namespace fp8pa

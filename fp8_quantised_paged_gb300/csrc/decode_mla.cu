@@ -482,6 +482,7 @@ size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 // Workspace for the shared-latent layout: same shape as the GQA one with the
 // head groups of 32 in the role of KV heads.
 cudaError_t launch_decode_mla(const DecodeShape& s, const DecodeArgs& a, cudaStream_t stream) {
+  if (s.mla_tc) return launch_decode_mla_tc(s, a, stream);
   const int H = s.hq / kHeads;
   const int ranges = s.workers / H;
   const int smem = MlaSmem::kBytes;

@@ -78,6 +78,7 @@ struct PlanArgs {
   int qw;  // queries per planned request (batch = planned requests)
   int* plan;
   uint32_t* err;
+  int upages;  // blocks per planned unit
 };
 
 // Append and plan in one launch (the prologue of fp8pa_decode_step).
@@ -94,7 +95,8 @@ cudaError_t launch_scales_from_absmax(const float* amax, int n, int fmt, float* 
 struct DecodeShape {
   int batch, hq, hkv, d, dv, bs, max_blocks;
   int workers;        // split workers (warps or CTAs, per kernel family)
-  int mla;            // 1 for the shared-latent kernel
+  int mla;            // 1 for the shared-latent layout
+  int mla_tc;         // 1 when the latent tensor-core kernel serves it (FP8, 64-head groups)
   int qlen;           // queries per request (batch counts request x query)
 };
 
@@ -125,8 +127,13 @@ struct DecodeArgs {
 
 // Page ranges the planner cuts for this shape (its `workers`), and the
 // block size of the pages it counts.
-inline int plan_workers(const DecodeShape& s) { return s.mla ? s.workers / (s.hq / 32) : s.workers; }
+// Query heads per CTA of the latent kernels (64 on tensor cores, 32 on warp MMA).
+inline int mla_group_heads(const DecodeShape& s) { return s.mla_tc ? 64 : 32; }
+inline int plan_workers(const DecodeShape& s) {
+  return s.mla ? s.workers / (s.hq / mla_group_heads(s)) : s.workers;
+}
 inline int plan_block_size(const DecodeShape& s) { return s.mla ? 64 : s.bs; }
+inline int plan_unit_pages(const DecodeShape& s) { return s.mla_tc ? 2 : 1; }
 
 int decode_workers(const DecodeShape& s, int fmt, int mode, int device);
 
@@ -137,12 +144,13 @@ int decode_workers(const DecodeShape& s, int fmt, int mode, int device);
 // counts virtual requests (request x query of a causal chunk of `qlen`).
 cudaError_t launch_plan(const int32_t* seq_lens, int batch, int qlen, int qw, int groups, int bs,
                         int max_blocks, int workers, int* plan, uint32_t* err,
-                        cudaStream_t stream);
+                        cudaStream_t stream, int upages = 1);
 cudaError_t launch_merge(const int* plan, const float* part_ml, const float* part_o, void* out,
                          int batch, int qw, int hq, int groups, int G, int dv, int out_dtype,
                          cudaStream_t stream);
 cudaError_t launch_decode_gqa(const DecodeShape& s, const DecodeArgs& a, cudaStream_t stream);
 cudaError_t launch_decode_mla(const DecodeShape& s, const DecodeArgs& a, cudaStream_t stream);
+cudaError_t launch_decode_mla_tc(const DecodeShape& s, const DecodeArgs& a, cudaStream_t stream);
 
 // Cached launch set-up (per device): SM count, the dynamic shared-memory
 // opt-in of a kernel (made once), and a kernel's resident CTAs per SM.

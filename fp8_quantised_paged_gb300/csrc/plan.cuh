@@ -32,11 +32,14 @@ __device__ __forceinline__ int warp_incl_scan(int x) {
 // request b holds the qw queries b*qw .. b*qw + qw - 1 of a causal chunk of
 // qlen (qw = 1: one virtual request per query; qw = qlen: one per real
 // request); its pages are those its last query sees.
+// A unit is `upages` blocks of `bs` tokens (the latent tensor-core kernel
+// works on page pairs).
 __device__ __forceinline__ void plan_warp(const int32_t* seq_lens, int B, int qlen, int qw,
                                           int groups, int bs, int max_blocks, int workers,
-                                          int* ws, uint32_t* err) {
+                                          int* ws, uint32_t* err, int upages = 1) {
   const int lane = threadIdx.x & 31;
   const int cap = max_blocks * bs;
+  const int ut = bs * upages;  // tokens per unit
   int* uprefix = ws + kPlanHeader;
   int* segbase = uprefix + B + 1;
   int carry = 0;
@@ -47,7 +50,7 @@ __device__ __forceinline__ void plan_warp(const int32_t* seq_lens, int B, int ql
       bool bad;
       const int L = visible_len(seq_lens, b * qw + qw - 1, qlen, cap, &bad);
       if (bad) raise_error(err, FP8PA_DEVERR_SEQ_LEN);
-      n = (L + bs - 1) / bs;
+      n = (L + ut - 1) / ut;
     }
     const int incl = warp_incl_scan(n);
     if (b < B) uprefix[b] = (carry + incl - n) * groups;

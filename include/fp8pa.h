@@ -349,7 +349,7 @@ int fp8pa_decode_step(const void* k_new, const void* v_new, const int32_t* slot_
  * CUDA_MODULE_LOADING=EAGER, whether or not this call is ever made.  It is
  * held until the process exits (or the device is reset).
  */
-#define FP8PA_STATIC_WORKSPACE_BYTES (16u << 20)
+#define FP8PA_STATIC_WORKSPACE_BYTES (32u << 20)
 
 /*
  * The source pages have no counterpart to this call; it serves users of the

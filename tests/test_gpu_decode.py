@@ -57,8 +57,12 @@ def test_decode_independent_of_split_count(F, idx):
             outs.append(o)
     finally:
         F.set_decode_workers(0)
+    # Splits may differ by fp32 rounding and, on the latent tensor-core path,
+    # by the rounding of P's and V^'s 16-bit hi + lo parts: bounded against
+    # the output's scale.
+    tol = 1e-4 * np.abs(outs[0]).max()
     for o in outs[1:]:
-        assert np.allclose(o, outs[0], rtol=2e-5, atol=2e-6)
+        assert np.abs(o - outs[0]).max() <= tol
 
 
 def test_decode_edges(F):

@@ -24,6 +24,7 @@ CASES = [
     ("seg_g3_hkv3_bs64_int8", [64, 65, 1100, 2048], 9, 3, 128, 64, I8),
     ("seg_g1_hkv5_d64_bs16", [500, 1500, 2500], 5, 5, 64, 16, E4),
     ("seg_mla_32_heads", [300, 1025, 2100], 32, 1, 576, 64, E4),
+    ("seg_mla_64_heads_e5m2", [129, 1100, 64], 64, 1, 576, 64, E5),
 ]
 
 
@@ -67,7 +68,7 @@ def test_segment_append_and_decode_match_oracle(F, case):
             outs.append(got)
     finally:
         F.set_decode_workers(0)
-    tol = 2e-5 * np.abs(outs[0]).max()
+    tol = 1e-4 * np.abs(outs[0]).max()
     for got in outs[1:]:
         assert np.abs(got - outs[0]).max() <= tol
     assert F.get_device_error() == 0

@@ -38,6 +38,7 @@ CASES = [
     ("int8_g3_hkv3_d128_bs64_static", 9, 3, 128, 64, I8, CS),
     ("int8_g2_hkv4_d64_bs16_token", 8, 4, 64, 16, I8, TH),
     ("int8_mla_32_heads", 32, 1, 576, 64, I8, TG),
+    ("mla_192_heads_e4m3", 192, 1, 576, 64, E4, TG),
 ]
 
 

@@ -93,10 +93,11 @@ def test_variant_at_every_split(F, name):
             outs.append(got)
     finally:
         F.set_decode_workers(0)
-    # Splits may differ only by fp32 rounding, whose size follows the
-    # magnitude of the values summed (up to x50 outliers here), not of each
-    # output element.
-    tol = 2e-5 * np.abs(outs[0]).max()
+    # Splits may differ by fp32 rounding (and, on the latent tensor-core
+    # path, by the rounding of 16-bit hi + lo operand parts), whose size
+    # follows the magnitude of the values summed (up to x50 outliers here),
+    # not of each output element.
+    tol = 1e-4 * np.abs(outs[0]).max()
     for workers, got in zip(WORKERS[1:], outs[1:]):
         diff = np.abs(got - outs[0]).max()
         assert diff <= tol, f"workers={workers}: max difference {diff:.3g} > {tol:.3g}"
