@@ -495,13 +495,25 @@ def time_steps(case, steps, flush_buf, barrier):
     return ms_total, [a.elapsed_time(b_) for a, b_ in ev]
 
 
+def mla_on_tensor_cores(w) -> bool:
+    """The latent layout runs the tcgen05 kernel for FP8 codes and query
+    heads in groups of 64, the warp-MMA kernel otherwise."""
+    return w.mla and w.fmt != W.INT8 and w.n_q_heads % 64 == 0
+
+
+def split_kernel_name(w):
+    if mla_on_tensor_cores(w):
+        return "mla_tc_kernel", "decode_mla_tc.cu"
+    return ("mla_split_kernel", "decode_mla.cu") if w.mla else ("gqa_split_kernel", "decode_gqa.cu")
+
+
 def split_roofline(w, acc, split_avg_ms, pk, traffic_json):
-    kname = "mla_split_kernel" if w.mla else "gqa_split_kernel"
-    src = "decode_mla.cu" if w.mla else "decode_gqa.cu"
+    kname, src = split_kernel_name(w)
     traffic = traffic_per_launch(traffic_json, w.name, src)
     if w.mla:
-        # a dense contraction: tensor-bound; f16 MMA against the measured
-        # dense bf16 rate (same nominal rate as f16)
+        # a dense contraction: tensor-bound; against the measured dense bf16
+        # rate (the FP8 QK^T half could count against twice that: bf16 is
+        # the conservative denominator)
         fl = flops_per_step(w)
         achieved = fl / (split_avg_ms * 1e-3) / 1e12
         return {"kernel": kname, "bound": "tensor", "achieved": achieved,
@@ -753,9 +765,13 @@ def run_gpu(args, rank, world, local_rank):
             "kv_tokens_per_s": world * acc["kv_tokens"] / (ms_step * 1e-3),
             "config": dict(w.describe(), parallelism=f"replicas x{world}",
                            kv_dtype={W.E4M3: "e4m3", W.E5M2: "e5m2", W.INT8: "int8"}[w.fmt],
-                           compute=("int8" if w.fmt == W.INT8 else "fp8")
-                           + " codes -> exact f16, warp MMA (m16n8k16), f32 accumulate "
-                             "and softmax",
+                           compute=("fp8 codes: QK^T as tcgen05 FP8 MMAs (q as two E4M3 "
+                                    "terms), P.V as tcgen05 bf16 MMAs (V^ and P as bf16 hi + lo), "
+                                    "f32 accumulation in TMEM, f32 softmax"
+                                    if mla_on_tensor_cores(w) else
+                                    ("int8" if w.fmt == W.INT8 else "fp8")
+                                    + " codes -> exact f16, warp MMA (m16n8k16), f32 accumulate "
+                                      "and softmax"),
                            l2=("flushed (a 320 MiB write) before every step, outside the timed "
                                "events" if flush else
                                "no flush: every step reads the whole cache, larger than 2 x L2"),
