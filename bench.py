@@ -501,14 +501,26 @@ def mla_on_tensor_cores(w) -> bool:
     return w.mla and w.fmt != W.INT8 and w.n_q_heads % 64 == 0
 
 
-def split_kernel_name(w):
+def chunk_on_tensor_cores(w, q_len: int) -> bool:
+    """A causal chunk on the grouped-query layout runs the tcgen05 kernel for
+    FP8 codes with one scale per (token, KV head), head_dim 128, block sizes
+    16/32/64 and 16 or 32 (query, head) columns per KV head."""
+    n = (w.n_q_heads // w.n_kv_heads) * q_len
+    return (not w.mla and w.fmt != W.INT8 and w.scale_mode == W.SCALE_TOKEN_HEAD
+            and w.head_dim == 128 and w.head_dim_v == 128 and w.block_size in (16, 32, 64)
+            and 2 <= q_len <= 8 and n in (16, 32))
+
+
+def split_kernel_name(w, q_len: int = 1):
     if mla_on_tensor_cores(w):
         return "mla_tc_kernel", "decode_mla_tc.cu"
+    if chunk_on_tensor_cores(w, q_len):
+        return "gqa_tc_kernel", "decode_gqa_tc.cu"
     return ("mla_split_kernel", "decode_mla.cu") if w.mla else ("gqa_split_kernel", "decode_gqa.cu")
 
 
-def split_roofline(w, acc, split_avg_ms, pk, traffic_json):
-    kname, src = split_kernel_name(w)
+def split_roofline(w, acc, split_avg_ms, pk, traffic_json, q_len: int = 1):
+    kname, src = split_kernel_name(w, q_len)
     traffic = traffic_per_launch(traffic_json, w.name, src)
     if w.mla:
         # a dense contraction: tensor-bound; against the measured dense bf16
@@ -718,7 +730,7 @@ def run_gpu(args, rank, world, local_rank):
     app = None if args.no_append_roofline else append_roofline(case, min(args.steps, 50), pk,
                                                                 args.traffic_json)
     split_avg_ms = statistics.mean(split_ms)
-    roof = split_roofline(w, acc, split_avg_ms, pk, args.traffic_json)
+    roof = split_roofline(w, acc, split_avg_ms, pk, args.traffic_json, ql)
     del case
     flush_buf = None
     torch.cuda.empty_cache()
@@ -769,6 +781,10 @@ def run_gpu(args, rank, world, local_rank):
                                     "terms), P.V as tcgen05 bf16 MMAs (V^ and P as bf16 hi + lo), "
                                     "f32 accumulation in TMEM, f32 softmax"
                                     if mla_on_tensor_cores(w) else
+                                    "fp8 codes: QK^T as tcgen05 FP8 MMAs (q as two E4M3 terms), "
+                                    "P.V as tcgen05 f16 MMAs (V^ exact f16, P' as f16 hi + lo), "
+                                    "f32 accumulation in TMEM, f32 softmax"
+                                    if chunk_on_tensor_cores(w, ql) else
                                     ("int8" if w.fmt == W.INT8 else "fp8")
                                     + " codes -> exact f16, warp MMA (m16n8k16), f32 accumulate "
                                       "and softmax"),

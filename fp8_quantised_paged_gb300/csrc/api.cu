@@ -183,6 +183,7 @@ DecodePath decode_path(int batch, int hq, int hkv, int d, int dv, int bs, int ma
   s.max_blocks = max_blocks;
   s.mla = 0;
   s.qlen = 1;
+  s.gqa_tc = 0;
   if ((fmt != FP8PA_E4M3 && fmt != FP8PA_E5M2 && fmt != FP8PA_INT8) ||
       (mode != FP8PA_SCALE_TOKEN_HEAD && mode != FP8PA_SCALE_CHANNEL_STATIC &&
        mode != FP8PA_SCALE_TOKEN_GROUP && mode != FP8PA_SCALE_MX_BLOCK &&
@@ -237,6 +238,8 @@ int attention_prepare(const void* q, const uint8_t* k_cache, const uint8_t* v_ca
                       max_blocks_per_seq, fmt, scale_mode, group_size, num_blocks, out_dtype);
   if (path->status != FP8PA_OK) return path->status;
   path->shape.qlen = q_len;
+  path->shape.gqa_tc = gqa_tc_eligible(fmt, scale_mode, head_dim, head_dim_v, block_size,
+                                       n_q_heads, n_kv_heads, q_len) ? 1 : 0;
   if (batch == 0) return FP8PA_OK;
   if (!q || !k_cache || !k_scale || !block_tables || !seq_lens || !out || !workspace)
     return FP8PA_ERR_NULL_POINTER;
@@ -493,6 +496,8 @@ size_t fp8pa_multiquery_workspace_bytes(int batch, int q_len, int n_q_heads, int
                                     mla ? 64 : 16, 1, FP8PA_OUT_BF16);
       if (path.status != FP8PA_OK) continue;
       path.shape.qlen = q_len;
+      path.shape.gqa_tc = gqa_tc_eligible(fmt, modes[m], head_dim, head_dim_v, block_size,
+                                          n_q_heads, n_kv_heads, q_len) ? 1 : 0;
       path.shape.workers = decode_workers(path.shape, fmt, modes[m], dev);
       const size_t n = decode_workspace_bytes(path.shape);
       need = n > need ? n : need;

@@ -838,6 +838,7 @@ int decode_workers(const DecodeShape& s, int fmt, int mode, int device) {
     return (ranges < 1 ? 1 : ranges) * H;
   }
   if (g_decode_workers_override > 0) return g_decode_workers_override;
+  if (s.gqa_tc) return gqa_tc_workers(s, device);
   const SplitKernel k = pick(s.d, s.bs, fmt, kernel_mode(mode, s.hq / s.hkv));
   const int qw = gqa_qw(s);
   const int wpc = gqa_wpc(s.hkv, qw, k), hsets = s.hkv / (wpc / qw);
@@ -863,6 +864,7 @@ size_t decode_workspace_bytes(const DecodeShape& s) {
 }
 
 cudaError_t launch_decode_gqa(const DecodeShape& s, const DecodeArgs& a, cudaStream_t stream) {
+  if (s.gqa_tc) return launch_decode_gqa_tc(s, a, stream);
   const int G = s.hq / s.hkv;
   const SplitKernel k = pick(s.d, s.bs, a.fmt, kernel_mode(a.mode, G));
   const int qw = gqa_qw(s);

@@ -98,6 +98,7 @@ struct DecodeShape {
   int mla;            // 1 for the shared-latent layout
   int mla_tc;         // 1 when the latent tensor-core kernel serves it (FP8, 64-head groups)
   int qlen;           // queries per request (batch counts request x query)
+  int gqa_tc;         // 1 when a grouped-query chunk runs the tensor-core kernel
 };
 
 // Query warps per KV head in the grouped-query split kernel: a causal chunk of
@@ -133,7 +134,9 @@ inline int plan_workers(const DecodeShape& s) {
   return s.mla ? s.workers / (s.hq / mla_group_heads(s)) : s.workers;
 }
 inline int plan_block_size(const DecodeShape& s) { return s.mla ? 64 : s.bs; }
-inline int plan_unit_pages(const DecodeShape& s) { return s.mla_tc ? 2 : 1; }
+inline int plan_unit_pages(const DecodeShape& s) {
+  return s.mla_tc ? 2 : (s.gqa_tc ? 128 / s.bs : 1);
+}
 
 int decode_workers(const DecodeShape& s, int fmt, int mode, int device);
 
@@ -151,6 +154,11 @@ cudaError_t launch_merge(const int* plan, const float* part_ml, const float* par
 cudaError_t launch_decode_gqa(const DecodeShape& s, const DecodeArgs& a, cudaStream_t stream);
 cudaError_t launch_decode_mla(const DecodeShape& s, const DecodeArgs& a, cudaStream_t stream);
 cudaError_t launch_decode_mla_tc(const DecodeShape& s, const DecodeArgs& a, cudaStream_t stream);
+// The tensor-core kernel for a causal chunk over the grouped-query layout:
+// FP8 codes, per-token scales, head_dim 128, G x q_len = 16 or 32 columns.
+bool gqa_tc_eligible(int fmt, int mode, int d, int dv, int bs, int hq, int hkv, int qlen);
+int gqa_tc_workers(const DecodeShape& s, int device);
+cudaError_t launch_decode_gqa_tc(const DecodeShape& s, const DecodeArgs& a, cudaStream_t stream);
 
 // Cached launch set-up (per device): SM count, the dynamic shared-memory
 // opt-in of a kernel (made once), and a kernel's resident CTAs per SM.

@@ -40,7 +40,7 @@ def _clone(c):
     return kc2, vc.clone(), ks2, vs.clone()
 
 
-@pytest.mark.parametrize("idx,q_len", [(1, 1), (2, 1), (3, 1), (4, 1), (5, 1), (1, 3), (5, 2)])
+@pytest.mark.parametrize("idx,q_len", [(1, 1), (2, 1), (3, 1), (4, 1), (5, 1), (1, 3), (5, 2), (2, 4), (3, 2)])
 def test_decode_step_equals_append_then_attention(F, idx, q_len):
     from gpu_util import DEV, check_close, gpu_cache, oracle_cache, oracle_attention, \
         oracle_multiquery, to_dev_bf16
