@@ -12,8 +12,9 @@
 // chunk's G heads x q_len queries form the N = 16 or 32 columns of every MMA,
 // so each page is read, and its values converted, once for all of them.
 //  * QK^T on FP8 tensor cores: S^T[t, hq] = sum_d code[t,d] q[hq,d], A = the
-//    step's K codes as TMA landed them (M = 128 tokens, two 64-byte-swizzled
-//    halves of 64 dims), B = q as two E4M3 terms hi + lo; the token's K scale
+//    step's K codes as TMA landed them (M = 128 tokens, 128-byte rows,
+//    128-byte swizzle, one copy per page), B = q as two E4M3 terms hi + lo
+//    (64-byte-swizzled halves of 64 dims); the token's K scale
 //    is applied in fp32 when the score warps read the accumulator.
 //  * FP32 online softmax in the log2 domain with a lazy running maximum per
 //    column (reduced over the tokens only when a score passes it by 2^8);
@@ -49,8 +50,9 @@ constexpr int kD = 128;             // head_dim (K and V)
 constexpr int kT = 128;             // tokens per step: M of QK^T, K of P.V
 constexpr int kThreads = 10 * 32;   // 4 score, 4 converting, 1 MMA-issuing, 1 copying warp
 constexpr int kVS = 4;              // V^ ring slots (16 tokens x 128 dims f16)
-constexpr int kHalf = kT * 64;      // one 64-dim half of a step's K or V: 128 rows x 64 B
-constexpr uint32_t kTmemCols = 128; // scores 2 x N, O^T N
+constexpr int kVP = kVS / 2;        // ... handed over in pairs
+constexpr int kTile = kT * kD;      // a step's K or V codes: 128 rows x 128 B, 128-byte swizzled
+constexpr uint32_t kTmemCols = 128; // scores 2 x N; O^T 2 x N (from P' hi, from P' lo)
 constexpr float kTau = 8.f;
 constexpr float kNegBig = -1e30f;
 
@@ -59,10 +61,10 @@ struct Smem {
   // two K stages (K halves, K scales, V scales); V stages (V halves): two
   // where they fit beside the rest at two CTAs per SM, else one
   static constexpr int kVSt = N <= 16 ? 2 : 1;
-  static constexpr int kKStage = 2 * kHalf + 2 * kT * 4;
+  static constexpr int kKStage = kTile + 2 * kT * 4;
   static constexpr int kKSt = 0;
   static constexpr int kVStg = kKSt + 2 * kKStage;
-  static constexpr int kQ = kVStg + kVSt * 2 * kHalf;           // 2 terms x 2 halves x N x 64 B
+  static constexpr int kQ = kVStg + kVSt * kTile;               // 2 terms x 2 halves x N x 64 B
   static constexpr int kPBuf = 2 * kT * N * 2;                   // 2 terms x 128 x N f16
   static constexpr int kP = kQ + 4 * N * 64;                     // two P' buffers
   static constexpr int kV = kP + 2 * kPBuf;                      // ring of V^ slots
@@ -74,7 +76,7 @@ struct Smem {
   static constexpr int kBlk = kMisc + 128;  // int [K, V][stage][8]: a step's block ids
   static constexpr int kTmem = kBlk + 128;
   static constexpr int kBars = kTmem + 16;
-  static constexpr int kNumBars = 4 * 2 + 2 + 2 + 2 + 2 * kVS + 2 + 1;
+  static constexpr int kNumBars = 4 * 2 + 2 + 2 + 2 + 2 * kVP + 2 + 1;
   static constexpr int kBytes = kBars + kNumBars * 8 + 1024;
 };
 
@@ -93,6 +95,12 @@ struct GtcParams {
   float qk_scale_log2;
 };
 
+// Byte offsets of (row r, byte d) in 64- and 128-byte swizzled tiles: the
+// 16-byte chunk index is XORed with the row's position in its 512 / 1024
+// byte swizzle span.
+__device__ __forceinline__ uint32_t sw128(int r, int d) {
+  return static_cast<uint32_t>(r * 128 + ((((d >> 4) ^ r) & 7) << 4) + (d & 15));
+}
 __device__ __forceinline__ uint32_t sw64(int r, int d) {
   return static_cast<uint32_t>(r * 64 + ((((d >> 4) ^ (r >> 1)) & 3) << 4) + (d & 15));
 }
@@ -153,20 +161,21 @@ __device__ __forceinline__ bool gtc_wait(uint64_t* bar, uint32_t parity, int* ab
   return mbar_try_wait(bar, parity) || gtc_wait_slow(bar, parity, abort_flag, err);
 }
 
-// O^T columns c0 .. c0 + N - 1 of this thread's TMEM lane times
-// beta * (alpha[c] if `rescale`), out of line: it runs only when a running
-// maximum or the V-scale exponent moves.
+// Both N-column halves of O^T (from P' hi and from P' lo) in this thread's
+// TMEM lane times beta * (alpha[c] if `rescale`), out of line: it runs only
+// when a running maximum or the V-scale exponent moves.
 template <int N>
 __device__ __noinline__ void gtc_rescale_o(uint32_t ta, const float* alpha, float beta,
                                            bool rescale) {
-#pragma unroll
-  for (int c0 = 0; c0 < N; c0 += 16) {
+#pragma unroll 1
+  for (int c0 = 0; c0 < 2 * N; c0 += 16) {
     uint32_t r[16];
     tmem_ld16(ta + c0, r);
     tmem_ld_wait();
 #pragma unroll
     for (int i = 0; i < 16; ++i)
-      r[i] = __float_as_uint(__uint_as_float(r[i]) * beta * (rescale ? alpha[c0 + i] : 1.f));
+      r[i] = __float_as_uint(__uint_as_float(r[i]) * beta *
+                             (rescale ? alpha[(c0 + i) % N] : 1.f));
     tmem_st16(ta + c0, r);
   }
   tmem_st_wait();
@@ -207,16 +216,17 @@ __global__ void __launch_bounds__(kThreads, 2)
   uint64_t* bar_qk = bars + 8;          // [2] scores of a step in TMEM
   uint64_t* bar_sfree = bars + 10;      // [2] a score buffer read
   uint64_t* bar_pready = bars + 12;     // [2] P' buffer written (and O rescaled)
-  uint64_t* bar_vfull = bars + 14;      // [kVS]
-  uint64_t* bar_vfree = bar_vfull + kVS;
-  uint64_t* bar_pv = bar_vfree + kVS;   // [2] P.V of a step done, by step parity
+  uint64_t* bar_vfull = bars + 14;      // [kVP] a pair of V^ slots written
+  uint64_t* bar_vfree = bar_vfull + kVP;  // [kVP] ... read by the tensor core
+  uint64_t* bar_pv = bar_vfree + kVP;   // [2] P.V of a step done, by step parity
   uint64_t* bar_drain = bar_pv + 2;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const float NEG_INF = __int_as_float(0xff800000);
-  constexpr uint32_t kPTerm = kT * N * 2;
-  constexpr uint32_t kPLbo = (N / 8) * 128;  // 8 tokens of P' (K direction)
-  const uint32_t idesc_pv = tc_idesc(0, 0, 1, 1, 128, N);  // f16, both MN-major
+  // P' as 2N columns, hi then lo: one MMA per 16 tokens reads V^ once and
+  // accumulates O^T from hi and from lo side by side
+  constexpr uint32_t kPLbo = (2 * N / 8) * 128;  // 8 tokens of P' (K direction)
+  const uint32_t idesc_pv = tc_idesc(0, 0, 1, 1, 128, 2 * N);  // f16, both MN-major
   const int up = kT / p.bs;                   // pages per step
   const int lgbs = __ffs(p.bs) - 1, lgG = __ffs(p.G) - 1;  // both powers of two
 
@@ -233,7 +243,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       mbar_init(bar_pready + s, 4);
       mbar_init(bar_pv + s, 1);
     }
-    for (int v = 0; v < kVS; ++v) {
+    for (int v = 0; v < kVP; ++v) {
       mbar_init(bar_vfull + v, 4);
       mbar_init(bar_vfree + v, 1);
     }
@@ -368,7 +378,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         // descriptors of the first K half, q term, V^ slot and P' k-step; a
         // later tile's start address (bits 0-13: byte address / 16) is the
         // first one's plus its byte offset / 16
-        const uint64_t dk0 = tc_desc(smem_u32(kstages), 16, 512, 4);
+        const uint64_t dk0 = tc_desc(smem_u32(kstages), 16, 1024, 2);  // 128-byte swizzle
         const uint64_t dq0 = tc_desc(smem_u32(qs), 16, 512, 4);
         const uint64_t dv0 = tc_desc(smem_u32(vs), 2048, 128, 0);
         const uint64_t dp0 = tc_desc(smem_u32(ps), kPLbo, 128, 0);
@@ -397,7 +407,7 @@ __global__ void __launch_bounds__(kThreads, 2)
               for (int ks = 0; ks < 2; ++ks)
 #pragma unroll
                 for (int term = 0; term < 2; ++term)
-                  tc_mma_f8(tmem + st * N, dk + ((h * kHalf + ks * 32) >> 4),
+                  tc_mma_f8(tmem + st * N, dk + ((h * 64 + ks * 32) >> 4),
                             dq0 + (((term * 2 + h) * (N * 64) + ks * 32) >> 4), p.idesc_qk,
                             (h | ks | term) != 0);
             tc_commit(bar_qk + st);
@@ -405,21 +415,22 @@ __global__ void __launch_bounds__(kThreads, 2)
             ++qk_next;
           }
           if (!ok) break;
-          // ---- P.V: O^T += V^[slot]^T P'[k-step], hi and lo.  A step uses
-          // the ring's 4 slots twice, so slot s % 4 is in phase s / 4.
+          // ---- P.V: O^T[:, hi | lo] += V^[slot]^T P'[k-step, hi | lo], a
+          // pair of 16-token slots per hand-over.  A step uses the ring's two
+          // pairs twice, so pair pp % 2 is in phase pp / 2.
           if (!wait(bar_pready + (n & 1), (n >> 1) & 1)) { ok = false; break; }
           tc_fence_after();
           uint64_t dp = dp0 + (((n & 1) * SM::kPBuf) >> 4);  // P' buffer of the step
 #pragma unroll 1
-          for (int s = 0; s < kT / 16; ++s) {
-            const int slot = s & (kVS - 1);
-            if (!wait(bar_vfull + slot, (s / kVS) & 1)) { ok = false; break; }
+          for (int pp = 0; pp < kT / 32; ++pp) {
+            const int rp = pp & (kVP - 1);
+            if (!wait(bar_vfull + rp, (pp / kVP) & 1)) { ok = false; break; }
             tc_fence_after();
-            const uint64_t av = dv0 + static_cast<uint32_t>(slot * (4096 >> 4));
-            tc_mma_f16(tmem + 2 * N, av, dp, idesc_pv, n > sc0 || s > 0);
-            tc_mma_f16(tmem + 2 * N, av, dp + (kPTerm >> 4), idesc_pv, true);
-            tc_commit(bar_vfree + slot);
-            dp += (2 * kPLbo) >> 4;
+            const uint64_t av = dv0 + static_cast<uint32_t>(rp * (8192 >> 4));
+            tc_mma_f16(tmem + 2 * N, av, dp, idesc_pv, n > sc0 || pp > 0);
+            tc_mma_f16(tmem + 2 * N, av + (4096 >> 4), dp + ((2 * kPLbo) >> 4), idesc_pv, true);
+            tc_commit(bar_vfree + rp);
+            dp += (4 * kPLbo) >> 4;
           }
           if (!ok) break;
           tc_commit(bar_pv + (n & 1));
@@ -455,13 +466,12 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (n >= 2 && !wait_warp(bar_kfree + st, ((n >> 1) - 1) & 1)) break;
         if (lane < 8) kblk[st * 8 + lane] = blk;  // for the score warps
         __syncwarp();
-        if (lane == 0) mbar_arrive_expect_tx(bar_kfull + st, pages * (2 * p.bs * 64 + 2 * p.bs * 4));
+        if (lane == 0) mbar_arrive_expect_tx(bar_kfull + st, pages * (p.bs * kD + 2 * p.bs * 4));
         __syncwarp();
         if (blk >= 0) {
-          for (int h = 0; h < 2; ++h)
-            tma_load_2d(dst + h * kHalf + lane * p.bs * 64, &tm_k, h * 64, row, bar_kfull + st);
-          bulk_load(dst + 2 * kHalf + lane * p.bs * 4, p.k_scale + row, p.bs * 4, bar_kfull + st);
-          bulk_load(dst + 2 * kHalf + kT * 4 + lane * p.bs * 4, p.v_scale + row, p.bs * 4,
+          tma_load_2d(dst + lane * p.bs * kD, &tm_k, 0, row, bar_kfull + st);
+          bulk_load(dst + kTile + lane * p.bs * 4, p.k_scale + row, p.bs * 4, bar_kfull + st);
+          bulk_load(dst + kTile + kT * 4 + lane * p.bs * 4, p.v_scale + row, p.bs * 4,
                     bar_kfull + st);
         }
         lastk = n;
@@ -469,12 +479,10 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (n >= kVSt && !wait_warp(bar_vsfree + vi, ((n / kVSt) - 1) & 1)) break;
         if (lane < 8) vblk[vi * 8 + lane] = blk;  // for the converting warps
         __syncwarp();
-        if (lane == 0) mbar_arrive_expect_tx(bar_vland + vi, pages * (2 * p.bs * 64));
+        if (lane == 0) mbar_arrive_expect_tx(bar_vland + vi, pages * (p.bs * kD));
         __syncwarp();
         if (blk >= 0)
-          for (int h = 0; h < 2; ++h)
-            tma_load_2d(vstages + vi * (2 * kHalf) + h * kHalf + lane * p.bs * 64, &tm_v, h * 64,
-                        row, bar_vland + vi);
+          tma_load_2d(vstages + vi * kTile + lane * p.bs * kD, &tm_v, 0, row, bar_vland + vi);
         lastv = n;
       }
       // the copies issued land before anything is freed (they normally have:
@@ -502,7 +510,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (!dead && !wait_warp(bar_kfull + st, (n >> 1) & 1)) dead = true;
         const int pos = j * kT + t;
         const bool vpage = kblk[st * 8 + (t >> lgbs)] >= 0;
-        const float* scl = reinterpret_cast<const float*>(kstages + st * SM::kKStage + 2 * kHalf);
+        const float* scl = reinterpret_cast<const float*>(kstages + st * SM::kKStage + kTile);
         const float sk = vpage ? scl[t] : 0.f;
         const float sv = vpage && pos < Lmax ? scl[kT + t] : 0.f;
         __syncwarp();
@@ -612,7 +620,8 @@ __global__ void __launch_bounds__(kThreads, 2)
               split_f16x2(z[ng * 8 + 2 * i], z[ng * 8 + 2 * i + 1], hw[i], lw[i]);
             const uint32_t off = (t >> 3) * kPLbo + ng * 128 + (t & 7) * 16;
             *reinterpret_cast<uint4*>(pb + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-            *reinterpret_cast<uint4*>(pb + kPTerm + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+            *reinterpret_cast<uint4*>(pb + off + (N / 8) * 128) =
+                make_uint4(lw[0], lw[1], lw[2], lw[3]);
           }
           if (resc) gtc_rescale_o<N>(tmem + lane_base + 2 * N, asm_, beta, rescale);
         }
@@ -646,12 +655,14 @@ __global__ void __launch_bounds__(kThreads, 2)
         const float fo = efin < -900 ? 0.f : exp2i(efin + kVExp<FMT>);
 #pragma unroll
         for (int c0 = 0; c0 < N; c0 += 16) {
-          uint32_t r[16];
-          tmem_ld16(tmem + lane_base + 2 * N + c0, r);
+          uint32_t rh[16], rl[16];  // O^T from P' hi and from P' lo
+          tmem_ld16(tmem + lane_base + 2 * N + c0, rh);
+          tmem_ld16(tmem + lane_base + 3 * N + c0, rl);
           tmem_ld_wait();
 #pragma unroll
           for (int i = 0; i < 16; ++i)
-            p.part_o[(row0 + c0 + i) * kD + t] = __uint_as_float(r[i]) * fo;
+            p.part_o[(row0 + c0 + i) * kD + t] =
+                (__uint_as_float(rh[i]) + __uint_as_float(rl[i])) * fo;
         }
       }
       tc_fence_before();
@@ -663,20 +674,22 @@ __global__ void __launch_bounds__(kThreads, 2)
       // code words are read at once, the stage's V half released, and the
       // eight slots filled as the tensor core frees them
       const int bt = tid - 128, tl = bt & 15, mg = bt >> 4;
-      const uint32_t src = sw64(tl, mg * 8);  // + half * kHalf + 1024 per slot (16 rows)
+      // dims 8 mg .. 8 mg + 7 of the first half; the second half's chunk
+      // index differs in bit 2 (64 bytes on); + 2048 per slot (16 rows)
+      const uint32_t src = sw128(tl, mg * 8), src1 = src ^ 64u;
       const uint32_t dst = (tl >> 3) * 2048 + mg * 128 + (tl & 7) * 16;  // + 1024 per half
       bool ok = true;
       for (int k = 0; k < nsteps && ok; ++k) {
         const int n = sc, vi = n % kVSt;
         const int j = static_cast<int>(seg_begin + k - first_u);
         if (!wait_warp(bar_vland + vi, (n / kVSt) & 1)) { ok = false; break; }
-        const uint8_t* vt = vstages + vi * (2 * kHalf) + src;
+        const uint8_t* vt = vstages + vi * kTile;
         uint2 c[kT / 16][2];
 #pragma unroll
         for (int s = 0; s < kT / 16; ++s)
 #pragma unroll
           for (int h = 0; h < 2; ++h)
-            c[s][h] = *reinterpret_cast<const uint2*>(vt + h * kHalf + s * 1024);
+            c[s][h] = *reinterpret_cast<const uint2*>(vt + (h ? src1 : src) + s * 2048);
         // bit s: token s * 16 + tl is cached and visible.  Other tokens have
         // a zero P'; only E5M2 bytes can convert to an infinity or a NaN,
         // which would turn that zero into a NaN, so only E5M2 zeroes them.
@@ -696,18 +709,22 @@ __global__ void __launch_bounds__(kThreads, 2)
           uint4 o[2];
 #pragma unroll
           for (int h = 0; h < 2; ++h) o[h] = codes8_to_f16<FMT>(c[s][h], (vm >> s) & 1);
-          // the ring's 4 slots twice per step: slot s % 4 was last freed in
-          // phase (s / 4) ^ 1 (the previous step's second use for s < 4)
-          const int slot = s % kVS;
-          if ((n > 0 || s >= kVS) && !wait_warp(bar_vfree + slot, ((s / kVS) + 1) & 1)) {
+          // slots in pairs, the ring's two pairs twice per step: pair
+          // position rp was last freed in phase (s / 4) ^ 1 (the previous
+          // step's second use for s < 4)
+          const int slot = s % kVS, rp = (s >> 1) % kVP;
+          if ((s & 1) == 0 && (n > 0 || s >= kVS) &&
+              !wait_warp(bar_vfree + rp, ((s / kVS) + 1) & 1)) {
             ok = false;
             break;
           }
           *reinterpret_cast<uint4*>(vs + slot * 4096 + dst) = o[0];
           *reinterpret_cast<uint4*>(vs + slot * 4096 + 1024 + dst) = o[1];
-          fence_proxy_async();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar_vfull + slot);
+          if (s & 1) {
+            fence_proxy_async();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_vfull + rp);
+          }
         }
         if (!ok) break;
         ++sc;
@@ -765,8 +782,9 @@ cudaError_t launch_decode_gqa_tc(const DecodeShape& s, const DecodeArgs& a, cuda
   if (e != cudaSuccess) return e;
   CUtensorMap tmk, tmv;
   const uint64_t rows = static_cast<uint64_t>(a.num_blocks) * s.hkv * s.bs;
-  if (!encode_tensor_map_2d_u8(&tmk, a.k_cache, kD, rows, 64, s.bs, CU_TENSOR_MAP_SWIZZLE_64B) ||
-      !encode_tensor_map_2d_u8(&tmv, a.v_cache, kD, rows, 64, s.bs, CU_TENSOR_MAP_SWIZZLE_64B))
+  // a page's rows of one KV head, whole (128 bytes), 128-byte swizzled
+  if (!encode_tensor_map_2d_u8(&tmk, a.k_cache, kD, rows, kD, s.bs, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_tensor_map_2d_u8(&tmv, a.v_cache, kD, rows, kD, s.bs, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   char* ws = static_cast<char*>(a.workspace);
   int* plan = reinterpret_cast<int*>(ws);
