@@ -505,7 +505,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       for (int c = 0; c < N; ++c) lt[c] = 0.f;
       bool dead = false;
       for (int k = 0; k < nsteps; ++k) {
-        const int n = sc, st = n & 1, bf = n & 1;
+        const int n = sc, st = n & 1;
         const int j = static_cast<int>(seg_begin + k - first_u);
         if (!dead && !wait_warp(bar_kfull + st, (n >> 1) & 1)) dead = true;
         const int pos = j * kT + t;
@@ -515,38 +515,49 @@ __global__ void __launch_bounds__(kThreads, 2)
         const float sv = vpage && pos < Lmax ? scl[kT + t] : 0.f;
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_kfree + st);
-        float z[N];
-        if (!dead && !wait_warp(bar_qk + bf, (n >> 1) & 1)) dead = true;
-        if (!dead) {
-          tc_fence_after();
-          uint32_t r[N];
-          if constexpr (N == 32) {
-            tmem_ld32(tmem + lane_base + bf * N, r);
-          } else {
-            tmem_ld16(tmem + lane_base + bf * N, r);
+        if (!dead && !wait_warp(bar_qk + st, (n >> 1) & 1)) dead = true;
+        tc_fence_after();
+        const float f = zs * sk;
+        // query qi sees pos < Lc - (qlen - 1 - qi), i.e. qi >= d0: column
+        // c = qi * G + h is visible from c = d0 * G on (none once dead)
+        const int d0 = vpage && !dead ? pos - (Lc - p.qlen + 1) + 1 : N;
+        const int cmin = max(min(d0, N), 0) << lgG;
+        const uint32_t sa = tmem + lane_base + st * N;  // this step's scores
+        // N = 32 scores are read from TMEM 16 columns at a time, up to three
+        // times a step, rather than held (they would not fit beside the
+        // running sums); N = 16 are read once and kept
+        float zk[16];
+        auto scores16 = [&](int c0, float (&z)[16]) {
+          if (N == 16 && c0 < 0) {  // a later pass over the kept scores
+#pragma unroll
+            for (int i = 0; i < 16; ++i) z[i] = zk[i];
+            return;
           }
+          c0 = c0 < 0 ? 0 : c0;
+          uint32_t r[16];
+          tmem_ld16(sa + c0, r);
           tmem_ld_wait();
-          tc_fence_before();
-          const float f = zs * sk;
-          // query qi sees pos < Lc - (qlen - 1 - qi), i.e. qi >= d0: column
-          // c = qi * G + h is visible from c = d0 * G on
-          const int d0 = vpage ? pos - (Lc - p.qlen + 1) + 1 : N;
-          const int cmin = max(min(d0, N), 0) << lgG;
 #pragma unroll
-          for (int c = 0; c < N; ++c) z[c] = c >= cmin ? __uint_as_float(r[c]) * f : NEG_INF;
-        } else {
+          for (int i = 0; i < 16; ++i)
+            z[i] = c0 + i >= cmin ? __uint_as_float(r[i]) * f : NEG_INF;
+          if (N == 16) {
 #pragma unroll
-          for (int c = 0; c < N; ++c) z[c] = NEG_INF;
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar_sfree + bf);
+            for (int i = 0; i < 16; ++i) zk[i] = z[i];
+          }
+        };
+        const int again = N == 16 ? -1 : 0;  // passes after the first: c0 + again
         // ---- running maxima (lazy) and the V-scale exponent
         const int fk = n & 1;
         bool upf = false;
 #pragma unroll
-        for (int c = 0; c < N; c += 4) {
-          const float4 m4 = *reinterpret_cast<const float4*>(mthr + c);
-          upf |= (z[c] > m4.x) | (z[c + 1] > m4.y) | (z[c + 2] > m4.z) | (z[c + 3] > m4.w);
+        for (int c0 = 0; c0 < N; c0 += 16) {
+          float z[16];
+          scores16(c0, z);
+#pragma unroll
+          for (int i = 0; i < 16; i += 4) {
+            const float4 m4 = *reinterpret_cast<const float4*>(mthr + c0 + i);
+            upf |= (z[i] > m4.x) | (z[i + 1] > m4.y) | (z[i + 2] > m4.z) | (z[i + 3] > m4.w);
+          }
         }
         if (__any_sync(0xffffffffu, upf) && lane == 0) misc[fk] = 1.f;
         const float svw = warp_max_f32(sv);
@@ -565,10 +576,15 @@ __global__ void __launch_bounds__(kThreads, 2)
           eexp[fk] = enew;
         }
         if (rescale) {
+#pragma unroll 1
+          for (int c0 = 0; c0 < N; c0 += 16) {
+            float z[16];
+            scores16(c0 + again, z);
 #pragma unroll
-          for (int c = 0; c < N; ++c) {
-            const float m = warp_max_f32(z[c]);
-            if (lane == (c & 31)) red[warp * N + c] = m;
+            for (int i = 0; i < 16; ++i) {
+              const float m = warp_max_f32(z[i]);
+              if (lane == ((c0 + i) & 31)) red[warp * N + c0 + i] = m;
+            }
           }
           named_sync(1, 128);
           if (t < N) {
@@ -589,19 +605,6 @@ __global__ void __launch_bounds__(kThreads, 2)
             lt[c + 3] *= a4.w;
           }
         }
-        // p (at most 2^kTau), its running sums, and P' = p * sv * 2^-enew
-        const float pf = enew < -900 ? 0.f : sv * exp2i(-enew);  // nothing valid yet: sv = 0
-#pragma unroll
-        for (int c = 0; c < N; c += 4) {
-          const float4 m4 = *reinterpret_cast<const float4*>(msm + c);
-          const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const float pv = ex2(z[c + i] - mm[i]);
-            lt[c + i] += pv;
-            z[c + i] = pv * pf;
-          }
-        }
         // P' buffer n & 1 was last read by P.V(n - 2); O is rescaled between
         // P.V(n - 1) and P.V(n), so only then does this step wait for the
         // previous one (a step's P.V overlaps the next step's scores)
@@ -610,21 +613,43 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (resc && !dead && !wait_warp(bar_pv + ((n - 1) & 1), ((n - 1) >> 1) & 1)) dead = true;
         if (!dead) {
           tc_fence_after();
+          // p (at most 2^kTau), its running sums, and P' = p * sv * 2^-enew
+          // as f16 hi + lo, MN-major: core (token / 8, column / 8), row t % 8
+          const float pf = enew < -900 ? 0.f : sv * exp2i(-enew);  // nothing valid yet: sv = 0
           uint8_t* pb = ps + (n & 1) * SM::kPBuf;
-          // P' as f16 hi + lo, MN-major: core (token / 8, column / 8), row t % 8
 #pragma unroll
-          for (int ng = 0; ng < N / 8; ++ng) {
-            uint32_t hw[4], lw[4];
+          for (int c0 = 0; c0 < N; c0 += 16) {
+            float z[16];
+            scores16(c0 + again, z);
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-              split_f16x2(z[ng * 8 + 2 * i], z[ng * 8 + 2 * i + 1], hw[i], lw[i]);
-            const uint32_t off = (t >> 3) * kPLbo + ng * 128 + (t & 7) * 16;
-            *reinterpret_cast<uint4*>(pb + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-            *reinterpret_cast<uint4*>(pb + off + (N / 8) * 128) =
-                make_uint4(lw[0], lw[1], lw[2], lw[3]);
+            for (int i = 0; i < 16; i += 4) {
+              const float4 m4 = *reinterpret_cast<const float4*>(msm + c0 + i);
+              const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float pv = ex2(z[i + e] - mm[e]);
+                lt[c0 + i + e] += pv;
+                z[i + e] = pv * pf;
+              }
+            }
+#pragma unroll
+            for (int g = 0; g < 2; ++g) {
+              uint32_t hw[4], lw[4];
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                split_f16x2(z[g * 8 + 2 * i], z[g * 8 + 2 * i + 1], hw[i], lw[i]);
+              const uint32_t off = (t >> 3) * kPLbo + ((c0 >> 3) + g) * 128 + (t & 7) * 16;
+              *reinterpret_cast<uint4*>(pb + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+              *reinterpret_cast<uint4*>(pb + off + (N / 8) * 128) =
+                  make_uint4(lw[0], lw[1], lw[2], lw[3]);
+            }
           }
           if (resc) gtc_rescale_o<N>(tmem + lane_base + 2 * N, asm_, beta, rescale);
         }
+        // the score buffer is read for the last time
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_sfree + st);
         fence_proxy_async();
         tc_fence_before();
         __syncwarp();
