@@ -52,7 +52,18 @@ constexpr int kThreads = 10 * 32;   // 4 score, 4 converting, 1 MMA-issuing, 1 c
 constexpr int kVS = 4;              // V^ ring slots (16 tokens x 128 dims f16)
 constexpr int kVP = kVS / 2;        // ... handed over in pairs
 constexpr int kTile = kT * kD;      // a step's K or V codes: 128 rows x 128 B, 128-byte swizzled
-constexpr uint32_t kTmemCols = 128; // scores 2 x N; O^T 2 x N (from P' hi, from P' lo)
+// QK^T takes q hi and lo in one MMA of 2N columns (scores from hi and from
+// lo side by side, added when read) where that fits the score warps'
+// registers, N = 16; with N = 32 the two terms accumulate in the same N
+// columns by two MMAs.
+template <int N>
+constexpr bool kQJoin = N == 16;
+// TMEM columns: two score buffers (2N or N wide), then O^T as 2N (from P'
+// hi, from P' lo)
+template <int N>
+constexpr int kSW = kQJoin<N> ? 2 * N : N;
+template <int N>
+constexpr uint32_t kTmemCols = 2 * kSW<N> + 2 * N <= 128 ? 128 : 256;
 constexpr float kTau = 8.f;
 constexpr float kNegBig = -1e30f;
 
@@ -269,7 +280,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int n_units = static_cast<int>(min(static_cast<long>(upw), U - u0));
 
   if (warp == 8) {
-    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_alloc(tmem_slot, kTmemCols<N>);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -361,10 +372,12 @@ __global__ void __launch_bounds__(kThreads, 2)
         hw[k] = h01 | (h23 << 16);
         lw[k] = l01 | (l23 << 16);
       }
+      // per 64-dim half: the N rows of the hi term, then the N of the lo
+      // term, so that one MMA of 2N columns takes both
       const int col = (c % (kD / 8)) * 8, half = col >> 6, d = col & 63;
-      const uint32_t off = half * (N * 64) + sw64(hq, d);
+      const uint32_t off = half * (2 * N * 64) + sw64(hq, d);
       *reinterpret_cast<uint2*>(qs + off) = make_uint2(hw[0], hw[1]);
-      *reinterpret_cast<uint2*>(qs + 2 * N * 64 + off) = make_uint2(lw[0], lw[1]);
+      *reinterpret_cast<uint2*>(qs + N * 64 + off) = make_uint2(lw[0], lw[1]);
     }
     fence_proxy_async();
     if (tid < N) msm[tid] = mthr[tid] = kNegBig;
@@ -406,10 +419,10 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
               for (int ks = 0; ks < 2; ++ks)
 #pragma unroll
-                for (int term = 0; term < 2; ++term)
-                  tc_mma_f8(tmem + st * N, dk + ((h * 64 + ks * 32) >> 4),
-                            dq0 + (((term * 2 + h) * (N * 64) + ks * 32) >> 4), p.idesc_qk,
-                            (h | ks | term) != 0);
+                for (int term = 0; term < (kQJoin<N> ? 1 : 2); ++term)
+                  tc_mma_f8(tmem + st * kSW<N>, dk + ((h * 64 + ks * 32) >> 4),
+                            dq0 + ((h * (2 * N * 64) + term * (N * 64) + ks * 32) >> 4),
+                            p.idesc_qk, (h | ks | term) != 0);
             tc_commit(bar_qk + st);
             tc_commit(bar_kfree + st);  // the tensor core is done with the K codes
             ++qk_next;
@@ -427,8 +440,9 @@ __global__ void __launch_bounds__(kThreads, 2)
             if (!wait(bar_vfull + rp, (pp / kVP) & 1)) { ok = false; break; }
             tc_fence_after();
             const uint64_t av = dv0 + static_cast<uint32_t>(rp * (8192 >> 4));
-            tc_mma_f16(tmem + 2 * N, av, dp, idesc_pv, n > sc0 || pp > 0);
-            tc_mma_f16(tmem + 2 * N, av + (4096 >> 4), dp + ((2 * kPLbo) >> 4), idesc_pv, true);
+            tc_mma_f16(tmem + 2 * kSW<N>, av, dp, idesc_pv, n > sc0 || pp > 0);
+            tc_mma_f16(tmem + 2 * kSW<N>, av + (4096 >> 4), dp + ((2 * kPLbo) >> 4), idesc_pv,
+                       true);
             tc_commit(bar_vfree + rp);
             dp += (4 * kPLbo) >> 4;
           }
@@ -522,7 +536,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         // c = qi * G + h is visible from c = d0 * G on (none once dead)
         const int d0 = vpage && !dead ? pos - (Lc - p.qlen + 1) + 1 : N;
         const int cmin = max(min(d0, N), 0) << lgG;
-        const uint32_t sa = tmem + lane_base + st * N;  // this step's scores
+        const uint32_t sa = tmem + lane_base + st * kSW<N>;  // this step's scores
         // N = 32 scores are read from TMEM 16 columns at a time, up to three
         // times a step, rather than held (they would not fit beside the
         // running sums); N = 16 are read once and kept
@@ -534,12 +548,23 @@ __global__ void __launch_bounds__(kThreads, 2)
             return;
           }
           c0 = c0 < 0 ? 0 : c0;
-          uint32_t r[16];
-          tmem_ld16(sa + c0, r);
-          tmem_ld_wait();
+          if constexpr (kQJoin<N>) {
+            uint32_t rh[16], rl[16];  // from q hi, from q lo
+            tmem_ld16(sa + c0, rh);
+            tmem_ld16(sa + N + c0, rl);
+            tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            z[i] = c0 + i >= cmin ? __uint_as_float(r[i]) * f : NEG_INF;
+            for (int i = 0; i < 16; ++i)
+              z[i] = c0 + i >= cmin ? (__uint_as_float(rh[i]) + __uint_as_float(rl[i])) * f
+                                    : NEG_INF;
+          } else {
+            uint32_t r[16];
+            tmem_ld16(sa + c0, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              z[i] = c0 + i >= cmin ? __uint_as_float(r[i]) * f : NEG_INF;
+          }
           if (N == 16) {
 #pragma unroll
             for (int i = 0; i < 16; ++i) zk[i] = z[i];
@@ -644,7 +669,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                   make_uint4(lw[0], lw[1], lw[2], lw[3]);
             }
           }
-          if (resc) gtc_rescale_o<N>(tmem + lane_base + 2 * N, asm_, beta, rescale);
+          if (resc) gtc_rescale_o<N>(tmem + lane_base + 2 * kSW<N>, asm_, beta, rescale);
         }
         // the score buffer is read for the last time
         tc_fence_before();
@@ -681,8 +706,8 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
         for (int c0 = 0; c0 < N; c0 += 16) {
           uint32_t rh[16], rl[16];  // O^T from P' hi and from P' lo
-          tmem_ld16(tmem + lane_base + 2 * N + c0, rh);
-          tmem_ld16(tmem + lane_base + 3 * N + c0, rl);
+          tmem_ld16(tmem + lane_base + 2 * kSW<N> + c0, rh);
+          tmem_ld16(tmem + lane_base + 2 * kSW<N> + N + c0, rl);
           tmem_ld_wait();
 #pragma unroll
           for (int i = 0; i < 16; ++i)
@@ -769,7 +794,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
   __syncthreads();
   tc_fence_after();
-  if (warp == 8) tmem_dealloc(tmem, kTmemCols);
+  if (warp == 8) tmem_dealloc(tmem, kTmemCols<N>);
 }
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
@@ -840,7 +865,8 @@ cudaError_t launch_decode_gqa_tc(const DecodeShape& s, const DecodeArgs& a, cuda
   p.bs = s.bs;
   p.max_blocks = s.max_blocks;
   p.num_blocks = a.num_blocks;
-  p.idesc_qk = tc_idesc(a.fmt == FP8PA_E5M2 ? 1 : 0, 0, 0, 0, 128, N);
+  // q hi | lo as 2N columns where the kernel joins them (N = 16)
+  p.idesc_qk = tc_idesc(a.fmt == FP8PA_E5M2 ? 1 : 0, 0, 0, 0, 128, N == 16 ? 2 * N : N);
   p.qk_scale_log2 = a.sm_scale * 1.4426950408889634f;
   cudaLaunchAttribute pdl[1];
   pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
