@@ -154,24 +154,6 @@ template <int FMT>
 constexpr int kVExp = FMT == FP8PA_E4M3 ? 8 : 0;
 
 
-// Wait for phase `parity` of `bar`; false once another role has given up
-// (abort flag set) or after the wait limit, which records a timeout and sets
-// the flag for the others.  The waiting loop is out of line: the kernel's
-// many wait sites then add little code, and the roles' loops stay small
-// enough for the instruction caches.
-__device__ __noinline__ bool gtc_wait_slow(uint64_t* bar, uint32_t parity, int* abort_flag,
-                                           uint32_t* err) {
-  if (*reinterpret_cast<volatile int*>(abort_flag)) return false;
-  if (mbar_wait_bounded(bar, parity, kWaitLimitCycles)) return true;
-  raise_error(err, FP8PA_DEVERR_TIMEOUT);
-  *reinterpret_cast<volatile int*>(abort_flag) = 1;
-  return false;
-}
-__device__ __forceinline__ bool gtc_wait(uint64_t* bar, uint32_t parity, int* abort_flag,
-                                         uint32_t* err) {
-  return mbar_try_wait(bar, parity) || gtc_wait_slow(bar, parity, abort_flag, err);
-}
-
 // Both N-column halves of O^T (from P' hi and from P' lo) in this thread's
 // TMEM lane times beta * (alpha[c] if `rescale`), out of line: it runs only
 // when a running maximum or the V-scale exponent moves.
@@ -297,10 +279,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     b = lo;
   };
   auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
-    return gtc_wait(bar, parity, abort_flag, p.err);
+    return tc_wait(bar, parity, abort_flag, p.err);
   };
   auto wait_warp = [&](uint64_t* bar, uint32_t parity) -> bool {
-    return __all_sync(0xffffffffu, gtc_wait(bar, parity, abort_flag, p.err));
+    return __all_sync(0xffffffffu, tc_wait(bar, parity, abort_flag, p.err));
   };
 
   int sc = 0;  // steps done by this CTA (every role keeps its own count)

@@ -229,12 +229,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
   // bounded wait; on expiry the whole CTA gives up (flag, then drains)
   auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
-    if (mbar_try_wait(bar, parity)) return true;
-    if (*reinterpret_cast<volatile int*>(abort_flag)) return false;
-    if (mbar_wait_bounded(bar, parity, kWaitLimitCycles)) return true;
-    raise_error(p.err, FP8PA_DEVERR_TIMEOUT);
-    *reinterpret_cast<volatile int*>(abort_flag) = 1;
-    return false;
+    return tc_wait(bar, parity, abort_flag, p.err);
   };
   // the same, with one answer for the whole warp (tcgen05.ld/st and the
   // warp-level arrivals need every lane to take the same path)

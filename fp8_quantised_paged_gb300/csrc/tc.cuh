@@ -180,4 +180,22 @@ __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
+// Wait for phase `parity` of `bar` on behalf of a role of a warp-specialised
+// CTA: false once another role has given up (abort flag set) or after the
+// wait limit, which records a timeout and sets the flag for the others.
+// The waiting loop is out of line, so that the many wait sites of a kernel
+// add little code and its roles' loops stay within the instruction caches.
+__device__ __noinline__ inline bool tc_wait_slow(uint64_t* bar, uint32_t parity, int* abort_flag,
+                                                 uint32_t* err) {
+  if (*reinterpret_cast<volatile int*>(abort_flag)) return false;
+  if (mbar_wait_bounded(bar, parity, kWaitLimitCycles)) return true;
+  raise_error(err, FP8PA_DEVERR_TIMEOUT);
+  *reinterpret_cast<volatile int*>(abort_flag) = 1;
+  return false;
+}
+__device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity, int* abort_flag,
+                                        uint32_t* err) {
+  return mbar_try_wait(bar, parity) || tc_wait_slow(bar, parity, abort_flag, err);
+}
+
 }  // namespace fp8pa
