@@ -504,11 +504,13 @@ def mla_on_tensor_cores(w) -> bool:
 def chunk_on_tensor_cores(w, q_len: int) -> bool:
     """A causal chunk on the grouped-query layout runs the tcgen05 kernel for
     FP8 codes with one scale per (token, KV head), head_dim 128, block sizes
-    16/32/64 and 16 or 32 (query, head) columns per KV head."""
-    n = (w.n_q_heads // w.n_kv_heads) * q_len
+    16/32/64, when some qw dividing q_len gives 16 or 32 (query, head)
+    columns per KV head."""
+    g = w.n_q_heads // w.n_kv_heads
     return (not w.mla and w.fmt != W.INT8 and w.scale_mode == W.SCALE_TOKEN_HEAD
             and w.head_dim == 128 and w.head_dim_v == 128 and w.block_size in (16, 32, 64)
-            and 2 <= q_len <= 8 and n in (16, 32))
+            and 2 <= q_len <= 8 and w.n_q_heads % w.n_kv_heads == 0
+            and any(q_len % qw == 0 and g * qw in (16, 32) for qw in range(1, q_len + 1)))
 
 
 def split_kernel_name(w, q_len: int = 1):

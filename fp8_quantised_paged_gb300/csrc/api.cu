@@ -167,10 +167,11 @@ struct DecodePath {
   int status;
 };
 
-// Validate the decode shapes (pointers are checked by the caller) and
-// choose the kernel family.
-DecodePath decode_path(int batch, int hq, int hkv, int d, int dv, int bs, int max_blocks, int fmt,
-                       int mode, int gs, int num_blocks, int out_dtype) {
+// Validate the decode shapes of `batch` virtual requests (requests x q_len
+// queries; pointers are checked by the caller) and choose the kernel family.
+DecodePath decode_path(int batch, int q_len, int hq, int hkv, int d, int dv, int bs,
+                       int max_blocks, int fmt, int mode, int gs, int num_blocks,
+                       int out_dtype) {
   DecodePath r{};
   r.status = FP8PA_OK;
   DecodeShape& s = r.shape;
@@ -182,7 +183,7 @@ DecodePath decode_path(int batch, int hq, int hkv, int d, int dv, int bs, int ma
   s.bs = bs;
   s.max_blocks = max_blocks;
   s.mla = 0;
-  s.qlen = 1;
+  s.qlen = q_len;
   s.gqa_tc = 0;
   if ((fmt != FP8PA_E4M3 && fmt != FP8PA_E5M2 && fmt != FP8PA_INT8) ||
       (mode != FP8PA_SCALE_TOKEN_HEAD && mode != FP8PA_SCALE_CHANNEL_STATIC &&
@@ -197,6 +198,8 @@ DecodePath decode_path(int batch, int hq, int hkv, int d, int dv, int bs, int ma
     r.status = FP8PA_ERR_BAD_SHAPE;
     return r;
   }
+  // chunks with G x qw = 16 or 32 (query, head) columns run on the tensor cores
+  s.gqa_tc = gqa_tc_eligible(fmt, mode, d, dv, bs, hq, hkv, q_len) ? 1 : 0;
   if (static_cast<long long>(num_blocks) * hkv * bs >= (1ll << 31) ||
       static_cast<long long>(max_blocks) * bs >= (1ll << 31) ||
       static_cast<long long>(batch) * max_blocks * bs * hkv >= (1ll << 31)) {
@@ -212,7 +215,8 @@ DecodePath decode_path(int batch, int hq, int hkv, int d, int dv, int bs, int ma
     s.mla_tc = (fmt != FP8PA_INT8 && hq % 64 == 0) ? 1 : 0;
     return r;
   }
-  if ((d != 64 && d != 128) || dv != d || (bs != 16 && bs != 32 && bs != 64) || hq / hkv > 8 ||
+  if ((d != 64 && d != 128) || dv != d || (bs != 16 && bs != 32 && bs != 64) ||
+      (hq / hkv > 8 && !s.gqa_tc) ||
       mode == FP8PA_SCALE_TOKEN_GROUP ||
       (mode == FP8PA_SCALE_MX_BLOCK && ((gs != 16 && gs != 32) || fmt == FP8PA_INT8)))
     r.status = FP8PA_ERR_UNSUPPORTED;
@@ -234,12 +238,10 @@ int attention_prepare(const void* q, const uint8_t* k_cache, const uint8_t* v_ca
                       DecodeArgs* a) {
   if (q_len <= 0 || batch < 0) return FP8PA_ERR_BAD_SHAPE;
   if (static_cast<long long>(batch) * q_len >= (1ll << 31)) return FP8PA_ERR_UNSUPPORTED;
-  *path = decode_path(batch * q_len, n_q_heads, n_kv_heads, head_dim, head_dim_v, block_size,
-                      max_blocks_per_seq, fmt, scale_mode, group_size, num_blocks, out_dtype);
+  *path = decode_path(batch * q_len, q_len, n_q_heads, n_kv_heads, head_dim, head_dim_v,
+                      block_size, max_blocks_per_seq, fmt, scale_mode, group_size, num_blocks,
+                      out_dtype);
   if (path->status != FP8PA_OK) return path->status;
-  path->shape.qlen = q_len;
-  path->shape.gqa_tc = gqa_tc_eligible(fmt, scale_mode, head_dim, head_dim_v, block_size,
-                                       n_q_heads, n_kv_heads, q_len) ? 1 : 0;
   if (batch == 0) return FP8PA_OK;
   if (!q || !k_cache || !k_scale || !block_tables || !seq_lens || !out || !workspace)
     return FP8PA_ERR_NULL_POINTER;
@@ -491,13 +493,10 @@ size_t fp8pa_multiquery_workspace_bytes(int batch, int q_len, int n_q_heads, int
   size_t need = 0;
   for (int m = 0; m < (mla ? 2 : 4); ++m)
     for (int fmt = FP8PA_E4M3; fmt <= FP8PA_INT8; ++fmt) {
-      DecodePath path = decode_path(batch * q_len, n_q_heads, n_kv_heads, head_dim, head_dim_v,
-                                    block_size, max_blocks_per_seq, fmt, modes[m],
+      DecodePath path = decode_path(batch * q_len, q_len, n_q_heads, n_kv_heads, head_dim,
+                                    head_dim_v, block_size, max_blocks_per_seq, fmt, modes[m],
                                     mla ? 64 : 16, 1, FP8PA_OUT_BF16);
       if (path.status != FP8PA_OK) continue;
-      path.shape.qlen = q_len;
-      path.shape.gqa_tc = gqa_tc_eligible(fmt, modes[m], head_dim, head_dim_v, block_size,
-                                          n_q_heads, n_kv_heads, q_len) ? 1 : 0;
       path.shape.workers = decode_workers(path.shape, fmt, modes[m], dev);
       const size_t n = decode_workspace_bytes(path.shape);
       need = n > need ? n : need;

@@ -101,7 +101,7 @@ struct GtcParams {
   float* part_ml;
   float* part_o;
   uint32_t* err;
-  int B, hq, hkv, G, qlen, bs, max_blocks, num_blocks;
+  int B, hq, hkv, G, qlen, qw, bs, max_blocks, num_blocks;  // qw queries per planned request
   uint32_t idesc_qk;
   float qk_scale_log2;
 };
@@ -268,7 +268,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *tmem_slot;  // scores: columns b * N; O^T: columns 2N ..
+  const uint32_t tmem = *tmem_slot;  // two score buffers, then O^T
 
   auto locate = [&](long u, int& b) {
     int lo = 0, hi = p.B;
@@ -299,9 +299,12 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int cap = p.max_blocks * p.bs;
     bool bad;
     // the chunk's last query sees the most tokens; query i sees Lc - (n - 1 - i)
-    const int Lmax = visible_len(p.seq_lens, b * p.qlen + p.qlen - 1, p.qlen, cap, &bad);
+    // planned request b: queries q0 .. q0 + qw - 1 of the chunk of request
+    // breal; its last query sees the most tokens
+    const int breal = (b * p.qw) / p.qlen, q0 = (b * p.qw) % p.qlen;
+    const int Lmax = visible_len(p.seq_lens, b * p.qw + p.qw - 1, p.qlen, cap, &bad);
     const int npages = (Lmax + p.bs - 1) / p.bs;
-    const long brow = static_cast<long>(b) * p.max_blocks;
+    const long brow = static_cast<long>(breal) * p.max_blocks;  // the request's block table
 
     // q of the N (query, head) columns -> two E4M3 terms after a power-of-two
     // normaliser (the largest |q| just below 2^8), 64-byte-swizzled halves
@@ -310,7 +313,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     for (int c = tid; c < N * kD / 8; c += kThreads) {
       const int hq = c / (kD / 8), qi = hq / p.G, h = hq % p.G;
       const uint16_t* src =
-          p.q + ((static_cast<long>(b) * p.qlen + qi) * p.hq + kvh * p.G + h) * kD;
+          p.q + ((static_cast<long>(b) * p.qw + qi) * p.hq + kvh * p.G + h) * kD;
       const uint4 w = __ldg(reinterpret_cast<const uint4*>(src) + c % (kD / 8));
       const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
@@ -330,7 +333,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     for (int c = tid; c < N * kD / 8; c += kThreads) {
       const int hq = c / (kD / 8), qi = hq / p.G, h = hq % p.G;
       const uint16_t* src =
-          p.q + ((static_cast<long>(b) * p.qlen + qi) * p.hq + kvh * p.G + h) * kD;
+          p.q + ((static_cast<long>(b) * p.qw + qi) * p.hq + kvh * p.G + h) * kD;
       const uint4 w = __ldg(reinterpret_cast<const uint4*>(src) + c % (kD / 8));
       const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
       float x[8];
@@ -495,7 +498,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       // =================================================== score warps
       const int t = tid;  // token of the step, TMEM lane; also the dv row of O^T
       const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-      const int Lc = min(p.seq_lens[b], cap);
+      const int Lc = min(p.seq_lens[breal], cap);
       float lt[N];  // this token's running sums of p per column
 #pragma unroll
       for (int c = 0; c < N; ++c) lt[c] = 0.f;
@@ -514,9 +517,9 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (!dead && !wait_warp(bar_qk + st, (n >> 1) & 1)) dead = true;
         tc_fence_after();
         const float f = zs * sk;
-        // query qi sees pos < Lc - (qlen - 1 - qi), i.e. qi >= d0: column
-        // c = qi * G + h is visible from c = d0 * G on (none once dead)
-        const int d0 = vpage && !dead ? pos - (Lc - p.qlen + 1) + 1 : N;
+        // query q0 + qi sees pos < Lc - (qlen - 1 - q0 - qi), i.e. qi >= d0:
+        // column c = qi * G + h is visible from c = d0 * G on (none once dead)
+        const int d0 = vpage && !dead ? pos - (Lc - p.qlen + 1) + 1 - q0 : N;
         const int cmin = max(min(d0, N), 0) << lgG;
         const uint32_t sa = tmem + lane_base + st * kSW<N>;  // this step's scores
         // N = 32 scores are read from TMEM 16 columns at a time, up to three
@@ -789,12 +792,19 @@ void* pick_gtc(int fmt) {
 
 }  // namespace
 
+// Queries per planned request: the largest divisor qw of q_len with
+// G x qw = 16 or 32 columns (a chunk longer than that runs as several
+// planned requests of qw queries), 0 if there is none.
+int gqa_tc_qw(int G, int qlen) {
+  for (int qw = qlen; qw >= 1; --qw)
+    if (qlen % qw == 0 && (G * qw == 16 || G * qw == 32)) return qw;
+  return 0;
+}
+
 bool gqa_tc_eligible(int fmt, int mode, int d, int dv, int bs, int hq, int hkv, int qlen) {
-  // G x q_len columns; G (a power of two here) divides 16 or 32, q_len <= 8
-  const int n = (hq / hkv) * qlen;
   return (fmt == FP8PA_E4M3 || fmt == FP8PA_E5M2) && mode == FP8PA_SCALE_TOKEN_HEAD && d == kD &&
          dv == kD && (bs == 16 || bs == 32 || bs == 64) && qlen >= 2 && qlen <= 8 &&
-         (n == 16 || n == 32);
+         hq % hkv == 0 && gqa_tc_qw(hq / hkv, qlen) > 0;
 }
 
 // Ranges of 128-token steps: two CTAs per SM, one per KV head of a range.
@@ -804,7 +814,7 @@ int gqa_tc_workers(const DecodeShape& s, int device) {
 }
 
 cudaError_t launch_decode_gqa_tc(const DecodeShape& s, const DecodeArgs& a, cudaStream_t stream) {
-  const int G = s.hq / s.hkv, N = G * s.qlen, qw = s.qlen, bp = s.batch / qw;
+  const int G = s.hq / s.hkv, qw = gqa_tc_qw(G, s.qlen), N = G * qw, bp = s.batch / qw;
   void* kfn = N == 32 ? pick_gtc<32>(a.fmt) : pick_gtc<16>(a.fmt);
   const int smem = N == 32 ? Smem<32>::kBytes : Smem<16>::kBytes;
   cudaError_t e = ensure_smem_attr(kfn, smem);
@@ -844,6 +854,7 @@ cudaError_t launch_decode_gqa_tc(const DecodeShape& s, const DecodeArgs& a, cuda
   p.hkv = s.hkv;
   p.G = G;
   p.qlen = s.qlen;
+  p.qw = qw;
   p.bs = s.bs;
   p.max_blocks = s.max_blocks;
   p.num_blocks = a.num_blocks;

@@ -104,7 +104,9 @@ struct DecodeShape {
 // Query warps per KV head in the grouped-query split kernel: a causal chunk of
 // up to 8 queries has its queries' warps walk the same pages in one CTA (one
 // DRAM read per page); longer chunks run one virtual request per query.
+int gqa_tc_qw(int G, int qlen);
 inline int gqa_qw(const DecodeShape& s) {
+  if (s.gqa_tc) return gqa_tc_qw(s.hq / s.hkv, s.qlen);
   return (!s.mla && s.qlen > 1 && s.qlen <= 8) ? s.qlen : 1;
 }
 

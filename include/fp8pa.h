@@ -299,6 +299,11 @@ int fp8pa_paged_decode_attention(const void* q, const uint8_t* k_cache, const ui
  *
  * q            bf16 [batch][q_len][n_q_heads][head_dim].
  * out          [batch][q_len][n_q_heads][head_dim_v], bf16 or f32.
+ *              Chunks of q_len 2..8 on the GQA layout with E4M3/E5M2 codes,
+ *              TOKEN_HEAD scales, head_dim 128 and G = n_q_heads/n_kv_heads
+ *              such that G x qw is 16 or 32 for some qw dividing q_len run
+ *              on the tensor cores, qw queries at a time; those also accept
+ *              G up to 32.
  * seq_lens     i32 [batch], the cached length including the whole chunk.
  *              A request shorter than q_len (or outside [0, cap]) sets
  *              FP8PA_DEVERR_SEQ_LEN; its rows that would see no token are 0.

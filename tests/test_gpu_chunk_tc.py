@@ -1,11 +1,12 @@
 """GPU parity of causal chunks on the grouped-query layout where they run
 on the tensor-core kernel (FP8 codes, one scale per token and KV head,
-head_dim 128, G x q_len = 16 or 32 columns): every (request, query) row
-against the FP64 oracle over its visible prefix, seq_lens[b] - (q_len - 1 - i)
-tokens ("Llama 3 70B FP8 deployment", dpshk.com, sec. 3.3: chunked prefill).
-Block sizes 16, 32 and 64, both FP8 formats, 2, 4 and 8 query heads per KV
-head, ragged lengths that start steps mid-page and end them mid-step, and
-every kind of split."""
+head_dim 128, G x qw = 16 or 32 columns for qw queries of the chunk, qw the
+largest such divisor of q_len): every (request, query) row against the FP64
+oracle over its visible prefix, seq_lens[b] - (q_len - 1 - i) tokens ("Llama
+3 70B FP8 deployment", dpshk.com, sec. 3.3: chunked prefill).  Block sizes
+16, 32 and 64, both FP8 formats, 2 to 32 query heads per KV head, chunks
+taken whole or as 2, 3 or 8 planned requests of qw queries, ragged lengths
+that start steps mid-page and end them mid-step, and every kind of split."""
 import numpy as np
 import pytest
 import torch
@@ -24,6 +25,11 @@ CASES = [
     ("g4_q8_bs16_e5m2", [900, 8, 300], 12, 3, 16, E5, 8),
     ("g2_q8_bs32_e4m3", [640, 1300, 33], 8, 4, 32, E4, 8),
     ("g8_q4_hkv1_bs64_e5m2", [2050, 777], 8, 1, 64, E5, 4),
+    # chunks split into planned requests of qw < q_len queries
+    ("g8_q8_qw4_bs16_e4m3", [700, 129, 1030, 9], 16, 2, 16, E4, 8),
+    ("g16_q4_qw2_bs32_e5m2", [513, 77, 300], 32, 2, 32, E5, 4),
+    ("g32_q3_qw1_bs64_e4m3", [400, 65, 130], 32, 1, 64, E4, 3),
+    ("g16_q3_qw1_bs16_e5m2", [260, 33, 3], 16, 1, 16, E5, 3),
 ]
 
 
