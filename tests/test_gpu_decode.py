@@ -267,9 +267,17 @@ def test_full_llama70b_layer_int8_sampled(F):
 
 @pytest.mark.slow
 def test_full_llama70b_layer_chunk4_sampled(F):
-    """The bench's --q-len 4 launch (a causal chunk of 4 queries per request,
-    its query warps sharing pages), checked on sampled requests."""
+    """The bench's --q-len 4 launch (a causal chunk of 4 queries per request:
+    the tensor-core kernel with all 4 queries x 8 heads on the MMA columns),
+    checked on sampled requests."""
     _full_size_sampled(F, _llama_variant(tag="_chunk4"), sample=(0, 5), q_len=4)
+
+
+@pytest.mark.slow
+def test_full_llama70b_layer_chunk8_sampled(F):
+    """The bench's --q-len 8 launch (each chunk planned as two requests of 4
+    queries on the tensor-core kernel), checked on sampled requests."""
+    _full_size_sampled(F, _llama_variant(tag="_chunk8"), sample=(2, 11), q_len=8)
 
 
 def test_bounded_wait_gives_up_and_reports(F):
