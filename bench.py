@@ -523,7 +523,8 @@ def split_kernel_name(w, q_len: int = 1):
 
 def split_roofline(w, acc, split_avg_ms, pk, traffic_json, q_len: int = 1):
     kname, src = split_kernel_name(w, q_len)
-    traffic = traffic_per_launch(traffic_json, w.name, src)
+    # a causal chunk's capture is recorded under the workload's name + _q<len>
+    traffic = traffic_per_launch(traffic_json, w.name if q_len == 1 else f"{w.name}_q{q_len}", src)
     if w.mla:
         # a dense contraction: tensor-bound; against the measured dense bf16
         # rate (the FP8 QK^T half could count against twice that: bf16 is
