@@ -27,8 +27,10 @@
 //    builder warps; B = P as bf16 hi + lo; three MMAs per step (hi.hi, hi.lo,
 //    lo.hi) keep ~16 significant bits on both sides with the full FP32 range.
 //  * Roles: warps 0-3 score, softmax and write the partials; warps 4-7 build
-//    V^; lane 0 of warp 8 issues the copies and the MMAs.  Handshakes are
-//    mbarriers; every wait is bounded.  Pieces are merged by merge.cu.
+//    V^; lane 0 of warp 8 issues the MMAs; warp 9 issues a pair's copies (a
+//    lane per latent group and page) as soon as the stage is free, with the
+//    block ids read beforehand.  Handshakes are mbarriers; every wait is
+//    bounded.  Pieces are merged by merge.cu.
 #include <float.h>
 
 #include "common.cuh"
@@ -43,7 +45,7 @@ namespace {
 constexpr int kDk = 576, kDv = 512, kBs = 64, kGroups = 9;
 constexpr int kH = 64;              // query heads per CTA: N of every MMA
 constexpr int kT = 128;             // tokens per step (a page pair)
-constexpr int kThreads = 9 * 32;    // 4 score warps, 4 builder warps, 1 issuing warp
+constexpr int kThreads = 10 * 32;   // 4 score warps, 4 builder warps, 1 issuing warp, 1 copying warp
 constexpr int kNB = 3;              // score buffers in TMEM (64 columns each)
 constexpr int kVS = 4;              // V^ ring slots (16 tokens each), handed over in pairs
 constexpr int kVD = kVS / 2;        // double slots
@@ -243,7 +245,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   int quse[kNB] = {0, 0, 0};         // completions of each score buffer
   int vd = 0;                        // issuer: V^ double slots consumed
   int fills_b = 0, fills_s = 0;      // V^ double slots filled by builders / score warps
-  bool issued_tma = false;           // issuer: a copy may be in flight
 
   long u = u0;
   const long uend = u0 + n_units;
@@ -389,46 +390,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           dpl[ks] = tc_desc(p_a + kPTerm + ks * 2048, 1024, 128, 0);
         }
         for (long uu = seg_begin; uu < seg_end; ++uu) {
-          const int j = static_cast<int>(uu - first_u);
-          if (pc > 0 && !wait(bar_stage, (pc - 1) & 1)) break;
-          int blk[2];
-          uint32_t bytes = 0;
-          for (int pg = 0; pg < 2; ++pg) {
-            const int pi = 2 * j + pg;
-            blk[pg] = pi < npages ? __ldg(p.block_tables + brow + pi) : -1;
-            if (pi < npages && (blk[pg] < 0 || blk[pg] >= p.num_blocks)) {
-              raise_error(p.err, FP8PA_DEVERR_BLOCK_RANGE);
-              blk[pg] = -1;
-            }
-            if (blk[pg] >= 0) bytes += kGroups * (kTile / 2) + (SEG ? 16 : kPageScales);
-          }
-          mbar_arrive_expect_tx(bar_full, bytes);
-          for (int pg = 0; pg < 2; ++pg) {
-            if (blk[pg] < 0) continue;
-            for (int g = 0; g < kGroups; ++g)
-              tma_load_2d(codes + g * kTile + pg * (kTile / 2), &tm_lat, g * 64, blk[pg] * kBs,
-                          bar_full);
-            if (SEG)
-              bulk_load(reinterpret_cast<uint8_t*>(scl) + pg * 16,
-                        p.scale + static_cast<long>(blk[pg]) * 4, 16, bar_full);
-            else
-              bulk_load(reinterpret_cast<uint8_t*>(scl) + pg * kPageScales,
-                        p.scale + static_cast<long>(blk[pg]) * kBs * kGroups, kPageScales,
-                        bar_full);
-          }
-          issued_tma = true;
-          // the next pair's pages into L2 while this one is worked on
-          if (uu + 1 < seg_end) {
-            for (int pg = 0; pg < 2; ++pg) {
-              const int pi = 2 * (j + 1) + pg;
-              if (pi >= npages) continue;
-              const int nb = __ldg(p.block_tables + brow + pi);
-              if (nb >= 0 && nb < p.num_blocks)
-                prefetch_l2(p.cache + static_cast<long>(nb) * kBs * kDk, kBs * kDk);
-            }
-          }
           if (!wait(bar_full, pc & 1)) break;
-          issued_tma = false;
           tc_fence_after();
           // ---- QK^T: group g into score buffer g % kNB
           bool qok = true;
@@ -485,6 +447,62 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (*reinterpret_cast<volatile int*>(abort_flag)) break;
         }
       }
+    } else if (warp == 9) {
+      // =================================================== copying warp
+      // Pair j of the segment into the stage once the tensor core, the score
+      // warps and the builders are done with the previous pair: lane l < 18
+      // copies group l % 9 of page l / 9, lanes 18 and 19 the two pages'
+      // scales; lanes 20 and 21 prefetch the next pair's pages into L2.  The
+      // block ids are read before the wait (block tables are inputs).
+      const int pg = lane < 18 ? lane / 9 : (lane < 22 ? (lane - 18) & 1 : -1);
+      int last = -1;  // the last pair whose copy went out
+      for (long uu = seg_begin; uu < seg_end; ++uu) {
+        const int j = static_cast<int>(uu - first_u);
+        int blk = -1;
+        if (lane < 20) {
+          const int pi = 2 * j + pg;
+          if (pi < npages) {
+            blk = __ldg(p.block_tables + brow + pi);
+            if (blk < 0 || blk >= p.num_blocks) {
+              if (lane == 0 || lane == 9) raise_error(p.err, FP8PA_DEVERR_BLOCK_RANGE);
+              blk = -1;
+            }
+          }
+        }
+        uint32_t bytes = 0;
+#pragma unroll
+        for (int q = 0; q < 2; ++q)
+          if (__shfl_sync(0xffffffffu, blk, 9 * q) >= 0)
+            bytes += kGroups * (kTile / 2) + (SEG ? 16 : kPageScales);
+        if (pc > 0 && !wait_warp(bar_stage, (pc - 1) & 1)) break;
+        if (lane == 0) mbar_arrive_expect_tx(bar_full, bytes);
+        __syncwarp();
+        if (blk >= 0) {
+          if (lane < 18) {
+            const int g = lane % 9;
+            tma_load_2d(codes + g * kTile + pg * (kTile / 2), &tm_lat, g * 64, blk * kBs, bar_full);
+          } else if (SEG) {
+            bulk_load(reinterpret_cast<uint8_t*>(scl) + pg * 16,
+                      p.scale + static_cast<long>(blk) * 4, 16, bar_full);
+          } else {
+            bulk_load(reinterpret_cast<uint8_t*>(scl) + pg * kPageScales,
+                      p.scale + static_cast<long>(blk) * kBs * kGroups, kPageScales, bar_full);
+          }
+        }
+        last = pc;
+        if (lane >= 20 && lane < 22 && uu + 1 < seg_end) {
+          const int pi = 2 * (j + 1) + pg;
+          if (pi < npages) {
+            const int nb = __ldg(p.block_tables + brow + pi);
+            if (nb >= 0 && nb < p.num_blocks)
+              prefetch_l2(p.cache + static_cast<long>(nb) * kBs * kDk, kBs * kDk);
+          }
+        }
+        ++pc;
+      }
+      // the last copy lands before anything is freed (it normally has: the
+      // pair was consumed; a waited phase reads as complete)
+      if (last >= 0) (void)mbar_wait_bounded(bar_full, last & 1, kWaitLimitCycles);
     } else if (warp < 4) {
       // =================================================== score warps
       const int t = tid;  // token of the pair, TMEM lane
@@ -714,7 +732,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // ---- drain and free: no copy or MMA may still be in flight
   if (warp == 8 && lane == 0) {
-    if (issued_tma) (void)mbar_wait_bounded(bar_full, pc & 1, kWaitLimitCycles);
     tc_commit(bar_drain);  // arrives once every MMA issued so far has completed
     (void)mbar_wait_bounded(bar_drain, 0, kWaitLimitCycles);
   }
