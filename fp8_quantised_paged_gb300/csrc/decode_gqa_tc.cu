@@ -521,6 +521,9 @@ __global__ void __launch_bounds__(kThreads, 2)
         // column c = qi * G + h is visible from c = d0 * G on (none once dead)
         const int d0 = vpage && !dead ? pos - (Lc - p.qlen + 1) + 1 - q0 : N;
         const int cmin = max(min(d0, N), 0) << lgG;
+        // every column of every token of the warp visible: the usual case
+        // (only a request's last step masks), and then no compare per column
+        const bool open = __all_sync(0xffffffffu, cmin == 0);
         const uint32_t sa = tmem + lane_base + st * kSW<N>;  // this step's scores
         // N = 32 scores are read from TMEM 16 columns at a time, up to three
         // times a step, rather than held (they would not fit beside the
@@ -540,15 +543,21 @@ __global__ void __launch_bounds__(kThreads, 2)
             tmem_ld_wait();
 #pragma unroll
             for (int i = 0; i < 16; ++i)
-              z[i] = c0 + i >= cmin ? (__uint_as_float(rh[i]) + __uint_as_float(rl[i])) * f
-                                    : NEG_INF;
+              z[i] = (__uint_as_float(rh[i]) + __uint_as_float(rl[i])) * f;
+            if (!open) {
+#pragma unroll
+              for (int i = 0; i < 16; ++i) z[i] = c0 + i >= cmin ? z[i] : NEG_INF;
+            }
           } else {
             uint32_t r[16];
             tmem_ld16(sa + c0, r);
             tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-              z[i] = c0 + i >= cmin ? __uint_as_float(r[i]) * f : NEG_INF;
+            for (int i = 0; i < 16; ++i) z[i] = __uint_as_float(r[i]) * f;
+            if (!open) {
+#pragma unroll
+              for (int i = 0; i < 16; ++i) z[i] = c0 + i >= cmin ? z[i] : NEG_INF;
+            }
           }
           if (N == 16) {
 #pragma unroll
