@@ -503,10 +503,18 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
       for (int c = 0; c < N; ++c) lt[c] = 0.f;
       bool dead = false;
+      // A poll of an mbarrier costs ~170 cycles of latency even on a phase
+      // already complete, so each of the step's three is issued ahead of its
+      // use (the next step's K copy at the end of this step), and a phase seen
+      // complete by every lane is not waited on.
+      bool kr = mbar_test_wait(bar_kfull + (sc & 1), (sc >> 1) & 1);
       for (int k = 0; k < nsteps; ++k) {
         const int n = sc, st = n & 1;
         const int j = static_cast<int>(seg_begin + k - first_u);
-        if (!dead && !wait_warp(bar_kfull + st, (n >> 1) & 1)) dead = true;
+        const bool qr = mbar_test_wait(bar_qk + st, (n >> 1) & 1);
+        const bool pr = k < 2 || mbar_test_wait(bar_pv + (n & 1), ((n >> 1) - 1) & 1);
+        if (!dead && !__all_sync(0xffffffffu, kr) && !wait_warp(bar_kfull + st, (n >> 1) & 1))
+          dead = true;
         const int pos = j * kT + t;
         const bool vpage = kblk[st * 8 + (t >> lgbs)] >= 0;
         const float* scl = reinterpret_cast<const float*>(kstages + st * SM::kKStage + kTile);
@@ -514,7 +522,8 @@ __global__ void __launch_bounds__(kThreads, 2)
         const float sv = vpage && pos < Lmax ? scl[kT + t] : 0.f;
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_kfree + st);
-        if (!dead && !wait_warp(bar_qk + st, (n >> 1) & 1)) dead = true;
+        if (!dead && !__all_sync(0xffffffffu, qr) && !wait_warp(bar_qk + st, (n >> 1) & 1))
+          dead = true;
         tc_fence_after();
         const float f = zs * sk;
         // query q0 + qi sees pos < Lc - (qlen - 1 - q0 - qi), i.e. qi >= d0:
@@ -628,7 +637,9 @@ __global__ void __launch_bounds__(kThreads, 2)
         // P.V(n - 1) and P.V(n), so only then does this step wait for the
         // previous one (a step's P.V overlaps the next step's scores)
         const bool resc = k > 0 && (rescale || beta != 1.f);
-        if (k > 1 && !dead && !wait_warp(bar_pv + (n & 1), ((n >> 1) - 1) & 1)) dead = true;
+        if (k > 1 && !dead && !__all_sync(0xffffffffu, pr) &&
+            !wait_warp(bar_pv + (n & 1), ((n >> 1) - 1) & 1))
+          dead = true;
         if (resc && !dead && !wait_warp(bar_pv + ((n - 1) & 1), ((n - 1) >> 1) & 1)) dead = true;
         if (!dead) {
           tc_fence_after();
@@ -673,6 +684,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_pready + (n & 1));
+        if (k + 1 < nsteps) kr = mbar_test_wait(bar_kfull + ((n + 1) & 1), ((n + 1) >> 1) & 1);
         ++sc;
       }
       // ---- segment end: the piece of (request b, KV head kvh)
