@@ -650,17 +650,39 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
           for (int c0 = 0; c0 < N; c0 += 16) {
             float z[16];
-            scores16(c0 + again, z);
+            if constexpr (kQJoin<N>) {
+              scores16(c0 + again, z);  // the kept scores
 #pragma unroll
-            for (int i = 0; i < 16; i += 4) {
-              const float4 m4 = *reinterpret_cast<const float4*>(msm + c0 + i);
-              const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const float pv = ex2(z[i + e] - mm[e]);
-                lt[c0 + i + e] += pv;
-                z[i + e] = pv * pf;
+              for (int i = 0; i < 16; i += 4) {
+                const float4 m4 = *reinterpret_cast<const float4*>(msm + c0 + i);
+                z[i] -= m4.x;
+                z[i + 1] -= m4.y;
+                z[i + 2] -= m4.z;
+                z[i + 3] -= m4.w;
               }
+            } else {
+              // read again: the score times its scale less the maximum, one FMA
+              uint32_t r[16];
+              tmem_ld16(sa + c0, r);
+              tmem_ld_wait();
+#pragma unroll
+              for (int i = 0; i < 16; i += 4) {
+                const float4 m4 = *reinterpret_cast<const float4*>(msm + c0 + i);
+                z[i] = fmaf(__uint_as_float(r[i]), f, -m4.x);
+                z[i + 1] = fmaf(__uint_as_float(r[i + 1]), f, -m4.y);
+                z[i + 2] = fmaf(__uint_as_float(r[i + 2]), f, -m4.z);
+                z[i + 3] = fmaf(__uint_as_float(r[i + 3]), f, -m4.w);
+              }
+              if (!open) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) z[i] = c0 + i >= cmin ? z[i] : NEG_INF;
+              }
+            }
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float pv = ex2(z[i]);
+              lt[c0 + i] += pv;
+              z[i] = pv * pf;
             }
 #pragma unroll
             for (int g = 0; g < 2; ++g) {
