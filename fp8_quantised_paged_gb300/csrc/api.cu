@@ -134,8 +134,22 @@ __global__ void __launch_bounds__(32) bounded_wait_selftest_kernel(long long lim
 
 }  // namespace
 
+bool encode_tensor_map_2d_f32(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows,
+                              uint32_t box_inner, uint32_t box_rows) {
+  return encode_tensor_map_2d(map, base, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, inner, rows,
+                              box_inner, box_rows, CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
 bool encode_tensor_map_2d_u8(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows,
                              uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle swz) {
+  return encode_tensor_map_2d(map, base, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, inner, rows, box_inner,
+                              box_rows, swz);
+}
+
+// A row-major 2-D tensor of `rows` rows of `inner` elements of `esize` bytes.
+bool encode_tensor_map_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dtype,
+                          uint32_t esize, uint64_t inner, uint64_t rows, uint32_t box_inner,
+                          uint32_t box_rows, CUtensorMapSwizzle swz) {
   static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
   if (!encode) {
     void* fn = nullptr;
@@ -147,10 +161,10 @@ bool encode_tensor_map_2d_u8(CUtensorMap* map, const void* base, uint64_t inner,
     encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
   }
   cuuint64_t dims[2] = {inner, rows};
-  cuuint64_t strides[1] = {inner};
+  cuuint64_t strides[1] = {inner * esize};
   cuuint32_t box[2] = {box_inner, box_rows};
   cuuint32_t estr[2] = {1, 1};
-  const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims,
+  const CUresult r = encode(map, dtype, 2, const_cast<void*>(base), dims,
                             strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
                             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;

@@ -58,6 +58,14 @@ constexpr int kTile = kT * kD;      // a step's K or V codes: 128 rows x 128 B, 
 // columns by two MMAs.
 template <int N>
 constexpr bool kQJoin = N == 16;
+// With N = 16 the issuing thread sets the step: it polls each barrier ahead
+// of use (a poll costs ~170 cycles of latency even on a completed phase),
+// its P.V pairs are unrolled, and the copy warp gathers the scale rows of 4
+// pages per copy, so the next step's K codes land sooner.  Measured on the
+// 32-column kernel, whose step the score warps set, the same changes were
+// slower, so it keeps the plain forms.
+template <int N>
+constexpr bool kFastIssue = N == 16;
 // TMEM columns: two score buffers (2N or N wide), then O^T as 2N (from P'
 // hi, from P' lo)
 template <int N>
@@ -177,6 +185,7 @@ __device__ __noinline__ void gtc_rescale_o(uint32_t ta, const float* alpha, floa
 template <int FMT, int N>
 __global__ void __launch_bounds__(kThreads, 2)
     gqa_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                  const __grid_constant__ CUtensorMap tm_ks, const __grid_constant__ CUtensorMap tm_vs,
                   const GtcParams p) {
   using SM = Smem<N>;
   extern __shared__ uint8_t smem_raw[];
@@ -246,6 +255,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     fence_barrier_init();
     prefetch_tensormap(&tm_k);
     prefetch_tensormap(&tm_v);
+    if (kFastIssue<N>) {
+      prefetch_tensormap(&tm_ks);
+      prefetch_tensormap(&tm_vs);
+    }
   }
   __syncthreads();
   griddep_wait();
@@ -387,15 +400,26 @@ __global__ void __launch_bounds__(kThreads, 2)
           // QK^T of this step (if not issued yet), and of the next one too if
           // its K codes have landed, into score buffer step & 1; P.V of this
           // step does not wait for the next step's copies
-          while (qk_next < nend &&
-                 (qk_next == n ||
-                  (qk_next == n + 1 &&
-                   mbar_test_wait(bar_kfull + (qk_next & 1), (qk_next >> 1) & 1)))) {
+          while (qk_next < nend && qk_next <= n + 1) {
             const int m = qk_next, st = m & 1;
-            if (!wait(bar_kfull + st, (m >> 1) & 1) ||
-                (m >= 2 && !wait(bar_sfree + st, ((m >> 1) - 1) & 1))) {
-              ok = false;
-              break;
+            if constexpr (kFastIssue<N>) {
+              // both polls go out before either answer is used; a phase seen
+              // complete is not waited on again
+              const bool kr = mbar_test_wait(bar_kfull + st, (m >> 1) & 1);
+              const bool sr = m < 2 || mbar_test_wait(bar_sfree + st, ((m >> 1) - 1) & 1);
+              if (m > n && !(kr && sr)) break;
+              if ((!kr && !wait(bar_kfull + st, (m >> 1) & 1)) ||
+                  (!sr && !wait(bar_sfree + st, ((m >> 1) - 1) & 1))) {
+                ok = false;
+                break;
+              }
+            } else {
+              if (m > n && !mbar_test_wait(bar_kfull + st, (m >> 1) & 1)) break;
+              if (!wait(bar_kfull + st, (m >> 1) & 1) ||
+                  (m >= 2 && !wait(bar_sfree + st, ((m >> 1) - 1) & 1))) {
+                ok = false;
+                break;
+              }
             }
             tc_fence_after();
             const uint64_t dk = dk0 + ((st * SM::kKStage) >> 4);
@@ -416,13 +440,18 @@ __global__ void __launch_bounds__(kThreads, 2)
           // ---- P.V: O^T[:, hi | lo] += V^[slot]^T P'[k-step, hi | lo], a
           // pair of 16-token slots per hand-over.  A step uses the ring's two
           // pairs twice, so pair pp % 2 is in phase pp / 2.
+          // (with kFastIssue: the pairs unrolled, pair pp + 1's hand-over polled
+          // before pair pp's MMAs go out)
+          bool nx = kFastIssue<N> && mbar_test_wait(bar_vfull, 0);  // pair 0
           if (!wait(bar_pready + (n & 1), (n >> 1) & 1)) { ok = false; break; }
           tc_fence_after();
           uint64_t dp = dp0 + (((n & 1) * SM::kPBuf) >> 4);  // P' buffer of the step
-#pragma unroll 1
+#pragma unroll(kFastIssue<N> ? kT / 32 : 1)
           for (int pp = 0; pp < kT / 32; ++pp) {
             const int rp = pp & (kVP - 1);
-            if (!wait(bar_vfull + rp, (pp / kVP) & 1)) { ok = false; break; }
+            if (!nx && !wait(bar_vfull + rp, (pp / kVP) & 1)) { ok = false; break; }
+            if (kFastIssue<N> && pp + 1 < kT / 32)
+              nx = mbar_test_wait(bar_vfull + ((pp + 1) & (kVP - 1)), ((pp + 1) / kVP) & 1);
             tc_fence_after();
             const uint64_t av = dv0 + static_cast<uint32_t>(rp * (8192 >> 4));
             tc_mma_f16(tmem + 2 * kSW<N>, av, dp, idesc_pv, n > sc0 || pp > 0);
@@ -465,10 +494,25 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (n >= 2 && !wait_warp(bar_kfree + st, ((n >> 1) - 1) & 1)) break;
         if (lane < 8) kblk[st * 8 + lane] = blk;  // for the score warps
         __syncwarp();
-        if (lane == 0) mbar_arrive_expect_tx(bar_kfull + st, pages * (p.bs * kD + 2 * p.bs * 4));
+        // scales: with kFastIssue and block 16 or 32, the rows (bs floats)
+        // of 4 pages per copy, every page slot of the step (a missing page
+        // reads row 0, unused); otherwise each page's row
+        const bool gather = kFastIssue<N> && p.bs <= 32;
+        const uint32_t sbytes = gather ? 2 * kT * 4 : pages * 2 * p.bs * 4;
+        if (lane == 0) mbar_arrive_expect_tx(bar_kfull + st, pages * p.bs * kD + sbytes);
         __syncwarp();
-        if (blk >= 0) {
-          tma_load_2d(dst + lane * p.bs * kD, &tm_k, 0, row, bar_kfull + st);
+        if (blk >= 0) tma_load_2d(dst + lane * p.bs * kD, &tm_k, 0, row, bar_kfull + st);
+        if (gather) {
+          const int srow = blk >= 0 ? blk * p.hkv + kvh : 0;  // the page's row of the scale maps
+          int r4[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) r4[i] = __shfl_sync(0xffffffffu, srow, ((lane >> 1) & 7) * 4 + i);
+          if (lane < 2 * (up / 4)) {  // lane 2g: K scales of pages 4g..4g+3, lane 2g+1: V
+            uint8_t* sd = dst + kTile + (lane & 1) * kT * 4 + (lane >> 1) * 4 * p.bs * 4;
+            tma_gather4_2d(sd, (lane & 1) ? &tm_vs : &tm_ks, 0, r4[0], r4[1], r4[2], r4[3],
+                           bar_kfull + st);
+          }
+        } else if (blk >= 0) {
           bulk_load(dst + kTile + lane * p.bs * 4, p.k_scale + row, p.bs * 4, bar_kfull + st);
           bulk_load(dst + kTile + kT * 4 + lane * p.bs * 4, p.v_scale + row, p.bs * 4,
                     bar_kfull + st);
@@ -865,11 +909,15 @@ cudaError_t launch_decode_gqa_tc(const DecodeShape& s, const DecodeArgs& a, cuda
   // room for two CTAs per SM
   e = cudaFuncSetAttribute(kfn, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
   if (e != cudaSuccess) return e;
-  CUtensorMap tmk, tmv;
+  CUtensorMap tmk, tmv, tmks, tmvs;
   const uint64_t rows = static_cast<uint64_t>(a.num_blocks) * s.hkv * s.bs;
-  // a page's rows of one KV head, whole (128 bytes), 128-byte swizzled
+  // a page's rows of one KV head, whole (128 bytes), 128-byte swizzled; the
+  // scales as rows of one page of one KV head (bs floats), gathered 4 at a
+  // time by the N = 16 kernel
   if (!encode_tensor_map_2d_u8(&tmk, a.k_cache, kD, rows, kD, s.bs, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_tensor_map_2d_u8(&tmv, a.v_cache, kD, rows, kD, s.bs, CU_TENSOR_MAP_SWIZZLE_128B))
+      !encode_tensor_map_2d_u8(&tmv, a.v_cache, kD, rows, kD, s.bs, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_tensor_map_2d_f32(&tmks, a.k_scale, s.bs, rows / s.bs, s.bs, 1) ||
+      !encode_tensor_map_2d_f32(&tmvs, a.v_scale, s.bs, rows / s.bs, s.bs, 1))
     return cudaErrorInvalidValue;
   char* ws = static_cast<char*>(a.workspace);
   int* plan = reinterpret_cast<int*>(ws);
@@ -915,7 +963,7 @@ cudaError_t launch_decode_gqa_tc(const DecodeShape& s, const DecodeArgs& a, cuda
   cfg.attrs = pdl;
   cfg.numAttrs = 1;
   if (g_split_ev_start) cudaEventRecord(g_split_ev_start, stream);
-  void* args[] = {&tmk, &tmv, &p};
+  void* args[] = {&tmk, &tmv, &tmks, &tmvs, &p};
   e = cudaLaunchKernelExC(&cfg, kfn, args);
   if (e != cudaSuccess) return e;
   if (g_split_ev_stop) cudaEventRecord(g_split_ev_stop, stream);

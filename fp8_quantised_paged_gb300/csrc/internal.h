@@ -169,8 +169,13 @@ cudaError_t ensure_smem_attr(const void* fn, int smem);
 int ctas_per_sm(const void* fn, int threads, int smem);
 
 // Tensor-map encoder from the driver (resolved once through the runtime).
+bool encode_tensor_map_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dtype,
+                          uint32_t esize, uint64_t inner, uint64_t rows, uint32_t box_inner,
+                          uint32_t box_rows, CUtensorMapSwizzle swz);
 bool encode_tensor_map_2d_u8(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows,
                              uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle swz);
+bool encode_tensor_map_2d_f32(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows,
+                              uint32_t box_inner, uint32_t box_rows);
 
 extern int g_decode_workers_override;
 extern cudaEvent_t g_split_ev_start, g_split_ev_stop;

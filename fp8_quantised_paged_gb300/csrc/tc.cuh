@@ -149,6 +149,19 @@ __device__ __forceinline__ float warp_max_f32(float v) {
   return m;
 }
 
+// Four rows (y0..y3, any order, one-row box of the map) of a 2-D tensor
+// map into consecutive box-sized pieces of shared memory, completing on `bar`
+// (tx bytes = 4 boxes).  x must be a multiple of 16 bytes of elements.
+__device__ __forceinline__ void tma_gather4_2d(void* smem_dst, const CUtensorMap* map, int x,
+                                               int y0, int y1, int y2, int y3, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3),
+      "r"(smem_u32(bar))
+      : "memory");
+}
+
 // Byte permute with the sign-replicating selector form (selector nibbles
 // with bit 3 set copy the sign bit of the chosen byte into all eight bits).
 __device__ __forceinline__ uint32_t prmt_sign(uint32_t a, uint32_t sel) {
