@@ -16,10 +16,13 @@
 //
 // A group of lanes per (token, kv head, K-or-V) row, several rows per warp.
 // Each lane owns 8 contiguous values per 16-byte chunk (one 16-byte load, one
-// 8-byte code store).  The divisions are IEEE
-// fp32 round-to-nearest (__fdiv_rn) and the FP8 cast is the hardware
-// cvt.rn.satfinite (INT8: cvt.rni), so codes and scales are bit-exact with
-// the definition.
+// 8-byte code store).  Every quotient is the IEEE fp32 round-to-nearest one
+// (__fdiv_rn for the scales and static channel scales; for per-token and
+// per-group scales a reciprocal per scale and a corrected product, see
+// quot_rn) and the FP8 cast is the hardware cvt.rn.satfinite (INT8:
+// cvt.rni), so codes and scales are bit-exact with the definition.
+#include <float.h>
+
 #include "common.cuh"
 #include "internal.h"
 #include "plan.cuh"
@@ -29,6 +32,35 @@ namespace fp8pa {
 namespace {
 
 constexpr int kAppendWarps = 8;
+
+// x / s rounded to nearest even, given r = rn(1 / s): y = rn(x r) lies within
+// two units in the last place of x / s, the residual y s - x is exact in one
+// fma, and one more fma adds its correction (the final correction step of
+// Markstein's division, "Computation of elementary functions on the IBM
+// RISC System/6000 processor", IBM J. Res. Dev. 34(1), 1990).  Checked
+// exhaustively against IEEE x / s for the scales this file forms,
+// s = max(rn(m / FMAX), 1e-12) with m a bf16 absmax and FMAX 448, 57344 or
+// 127, over every bf16 m and every bf16 x with |x| <= m: equal bit for bit,
+// except where x is an fp32 subnormal and the residual underflows; both
+// quotients are then below 2^-73, so every FP8 and INT8 code is zero (of
+// x's sign) either way.  Signed zeros come out as x / s gives them.  An
+// infinite scale (an infinite input) takes __fdiv_rn instead.
+__device__ __forceinline__ float quot_rn(float x, float s, float r) {
+  const float y = __fmul_rn(x, r);
+  const float e = fmaf(y, s, -x);
+  return fmaf(-e, r, y);
+}
+
+// The absmax scale max(rn(m / FMAX), 1e-12) of a row or group whose bf16
+// absmax is m, by the same corrected product with the constant rn(1 / FMAX)
+// (equal to IEEE m / FMAX for every finite bf16 m, checked exhaustively);
+// an infinite m gives an infinite scale, as the division does.
+template <int FMT>
+__device__ __forceinline__ float scale_of(float m) {
+  constexpr float kFmax = code_max<FMT>();
+  constexpr float kRcp = 1.0f / kFmax;
+  return m <= FLT_MAX ? fmaxf(quot_rn(m, kFmax, kRcp), 1e-12f) : m;
+}
 
 __device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float (&f)[8]) {
   const uint32_t w[4] = {u.x, u.y, u.z, u.w};
@@ -51,9 +83,10 @@ __device__ __forceinline__ int chunk_of(int sl, int r) {
 }
 
 // Row `row` of the call: its (K-or-V, head) index `rem` (-1 past the end), its
-// slot, and its values (zeros where the lane has no chunk).
+// slot, and its bf16 words (zeros where the lane has no chunk), left packed
+// so that nothing waits on the loads until the row is stored.
 template <int LPR, int R, bool CONSEC = false>
-__device__ __forceinline__ void load_row(const AppendArgs& a, long row, int sl, float (&v)[R][8],
+__device__ __forceinline__ void load_row(const AppendArgs& a, long row, int sl, uint4 (&w)[R],
                                          int& rem, int& slot) {
   const int per_tok = a.hkv * a.ntens;
   const bool in = row < static_cast<long>(a.num_tokens) * per_tok;
@@ -70,12 +103,8 @@ __device__ __forceinline__ void load_row(const AppendArgs& a, long row, int sl, 
 #pragma unroll
   for (int r = 0; r < R; ++r) {
     const int ci = chunk_of<LPR, R, CONSEC>(sl, r);
-    if (in && ci < nch) {
-      bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>(x + ci * 8)), v[r]);
-    } else {
-#pragma unroll
-      for (int e = 0; e < 8; ++e) v[r][e] = 0.0f;
-    }
+    w[r] = (in && ci < nch) ? __ldg(reinterpret_cast<const uint4*>(x + ci * 8))
+                            : make_uint4(0u, 0u, 0u, 0u);
   }
 }
 
@@ -83,7 +112,7 @@ __device__ __forceinline__ void load_row(const AppendArgs& a, long row, int sl, 
 // shuffles, also for rows that are skipped: past the end, a negative slot,
 // or a slot past the pool).
 template <int FMT, int MODE, int LPR, int R, bool CONSEC = false>
-__device__ __forceinline__ void store_row(const AppendArgs& a, const float (&v)[R][8], int rem,
+__device__ __forceinline__ void store_row(const AppendArgs& a, const uint4 (&w)[R], int rem,
                                           int slot, int sl) {
   // per-group modes need the chunks of a group on consecutive lanes
   static_assert(!CONSEC || MODE == FP8PA_SCALE_TOKEN_HEAD || MODE == FP8PA_SCALE_CHANNEL_STATIC,
@@ -102,6 +131,9 @@ __device__ __forceinline__ void store_row(const AppendArgs& a, const float (&v)[
   uint8_t* dst = live ? (which ? a.cache[1] : a.cache[0]) + crow * a.d : nullptr;
   float* scl = which ? a.scale[1] : a.scale[0];
 
+  float v[R][8];
+#pragma unroll
+  for (int r = 0; r < R; ++r) bf16x8_to_f32(w[r], v[r]);
   float cmax[R];
 #pragma unroll
   for (int r = 0; r < R; ++r) {
@@ -109,16 +141,20 @@ __device__ __forceinline__ void store_row(const AppendArgs& a, const float (&v)[
 #pragma unroll
     for (int e = 0; e < 8; ++e) cmax[r] = fmaxf(cmax[r], fabsf(v[r][e]));
   }
-  float s[R];
+  float s[R], rs[R];  // scales and (per-token and per-group modes) their reciprocals
   if constexpr (MODE == FP8PA_SCALE_TOKEN_HEAD) {
     float m = 0.0f;
 #pragma unroll
     for (int r = 0; r < R; ++r) m = fmaxf(m, cmax[r]);
 #pragma unroll
     for (int o = LPR / 2; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    const float sc = fmaxf(__fdiv_rn(m, kFmax), 1e-12f);
+    const float sc = scale_of<FMT>(m);
+    const float rc = __frcp_rn(sc);
 #pragma unroll
-    for (int r = 0; r < R; ++r) s[r] = sc;
+    for (int r = 0; r < R; ++r) {
+      s[r] = sc;
+      rs[r] = rc;
+    }
     if (live && sl == 0) scl[crow] = sc;
   } else if constexpr (MODE == FP8PA_SCALE_TOKEN_GROUP) {
     const int lpg = a.gs / 8;  // lanes per group: a power of two <= LPR
@@ -127,7 +163,8 @@ __device__ __forceinline__ void store_row(const AppendArgs& a, const float (&v)[
     for (int r = 0; r < R; ++r) {
       float m = cmax[r];
       for (int o = 1; o < lpg; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-      s[r] = fmaxf(__fdiv_rn(m, kFmax), 1e-12f);
+      s[r] = scale_of<FMT>(m);
+      rs[r] = __frcp_rn(s[r]);
       const int ci = sl + LPR * r;
       if (live && ci < nch && (sl & (lpg - 1)) == 0)
         scl[crow * ngroups + (ci * 8) / a.gs] = s[r];
@@ -153,13 +190,14 @@ __device__ __forceinline__ void store_row(const AppendArgs& a, const float (&v)[
   }
   if (!live) return;
 
+  uint2 pk[R];
 #pragma unroll
   for (int r = 0; r < R; ++r) {
     const int ci = chunk_of<LPR, R, CONSEC>(sl, r);
-    if (ci >= nch) continue;
     float q[8];
     if constexpr (MODE == FP8PA_SCALE_CHANNEL_STATIC) {
-      const float4* sp = reinterpret_cast<const float4*>(scl + h * a.d + ci * 8);
+      // a lane past the row's last chunk reads chunk 0's scales (unused)
+      const float4* sp = reinterpret_cast<const float4*>(scl + h * a.d + (ci < nch ? ci : 0) * 8);
       const float4 s0 = __ldg(sp), s1 = __ldg(sp + 1);
       const float sc[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
 #pragma unroll
@@ -167,14 +205,33 @@ __device__ __forceinline__ void store_row(const AppendArgs& a, const float (&v)[
     } else if constexpr (MODE == FP8PA_SCALE_MX_BLOCK) {
 #pragma unroll
       for (int e = 0; e < 8; ++e) q[e] = v[r][e] * s[r];
-    } else {
+    } else if (s[r] <= FLT_MAX) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) q[e] = quot_rn(v[r][e], s[r], rs[r]);
+    } else {  // an infinite input made the scale infinite
 #pragma unroll
       for (int e = 0; e < 8; ++e) q[e] = __fdiv_rn(v[r][e], s[r]);
     }
-    uint2 packed;
-    packed.x = f32x2_to_codes2<FMT>(q[0], q[1]) | (f32x2_to_codes2<FMT>(q[2], q[3]) << 16);
-    packed.y = f32x2_to_codes2<FMT>(q[4], q[5]) | (f32x2_to_codes2<FMT>(q[6], q[7]) << 16);
-    *reinterpret_cast<uint2*>(dst + ci * 8) = packed;
+    pk[r].x = f32x2_to_codes2<FMT>(q[0], q[1]) | (f32x2_to_codes2<FMT>(q[2], q[3]) << 16);
+    pk[r].y = f32x2_to_codes2<FMT>(q[4], q[5]) | (f32x2_to_codes2<FMT>(q[6], q[7]) << 16);
+  }
+  if constexpr (CONSEC && R % 2 == 0) {
+    // Two chunks per 16-byte store: ci is even, head_dim a multiple of 16
+    // and the cache 16-byte aligned, so the store is aligned and, with ci
+    // inside the row, so is ci + 1.
+#pragma unroll
+    for (int r = 0; r < R; r += 2) {
+      const int ci = chunk_of<LPR, R, CONSEC>(sl, r);
+      if (ci + 1 < nch)
+        *reinterpret_cast<uint4*>(dst + ci * 8) =
+            make_uint4(pk[r].x, pk[r].y, pk[r + 1].x, pk[r + 1].y);
+    }
+  } else {
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      const int ci = chunk_of<LPR, R, CONSEC>(sl, r);
+      if (ci < nch) *reinterpret_cast<uint2*>(dst + ci * 8) = pk[r];
+    }
   }
 }
 
@@ -185,10 +242,10 @@ template <int FMT, int MODE, int LPR, int R>
 __device__ __forceinline__ void append_step(const AppendArgs& a, long warp, int lane) {
   constexpr int SG = 32 / LPR;
   const int sg = lane / LPR, sl = lane % LPR;
-  float v[R][8];
+  uint4 w[R];
   int rem, slot;
-  load_row<LPR, R>(a, warp * SG + sg, sl, v, rem, slot);
-  store_row<FMT, MODE, LPR, R>(a, v, rem, slot, sl);
+  load_row<LPR, R>(a, warp * SG + sg, sl, w, rem, slot);
+  store_row<FMT, MODE, LPR, R>(a, w, rem, slot, sl);
 }
 
 template <int FMT, int MODE, int LPR, int R>
@@ -201,12 +258,12 @@ __global__ void __launch_bounds__(kAppendWarps * 32) append_kernel(AppendArgs a)
 
 // Many rows (a prefill): a persistent grid whose warps stride over the
 // steps of rows with a ring of kStreamDepth steps in registers -- a step's
-// loads are issued kStreamDepth - 1 steps before the warp works on it, so
-// loads stay in flight while the warp scales and rounds.  The kernel is
-// bound by instruction issue (two IEEE divisions' worth of work per value
-// for bit-exact codes), so its rows are spread over few lanes, each with
-// several 16-byte chunks, to share every row's index arithmetic.
-constexpr int kStreamDepth = 2;
+// loads are issued kStreamDepth - 1 steps before the warp works on it, and
+// its words stay packed until then, so loads stay in flight while the warp
+// scales and rounds.  Rows are spread over few lanes, each with several
+// consecutive 16-byte chunks (stored as 16-byte code words), to share every
+// row's index arithmetic.
+constexpr int kStreamDepth = 3;
 
 template <int FMT, int MODE, int LPR, int R, bool CONSEC>
 __global__ void __launch_bounds__(kAppendWarps * 32) append_stream_kernel(AppendArgs a) {
@@ -217,7 +274,7 @@ __global__ void __launch_bounds__(kAppendWarps * 32) append_stream_kernel(Append
   const long nsteps = (static_cast<long>(a.num_tokens) * a.hkv * a.ntens + SG - 1) / SG;
   const long stride = static_cast<long>(gridDim.x) * kAppendWarps;
   const long first = static_cast<long>(blockIdx.x) * kAppendWarps + (threadIdx.x >> 5);
-  float v[P][R][8];
+  uint4 v[P][R];
   int rem[P], slot[P];
 #pragma unroll
   for (int p = 0; p < P; ++p)

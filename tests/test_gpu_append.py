@@ -188,3 +188,41 @@ def test_every_finite_bf16_pattern_mx_blocks(F, fmt, gs):
     oracle.kv_append_quant(x, None, slots, fmt, W.SCALE_MX_BLOCK, gs, okc, None, oke, None, bs)
     _assert_codes_equal(kc.cpu().numpy(), okc, "codes")
     assert np.array_equal(ke.cpu().numpy(), oke), "exponents"
+
+
+@pytest.mark.parametrize("fmt", [W.E4M3, W.E5M2, W.INT8])
+@pytest.mark.parametrize("mode", [W.SCALE_TOKEN_HEAD, W.SCALE_TOKEN_GROUP])
+def test_bulk_rows_every_finite_bf16_pattern(F, fmt, mode):
+    """A call of more than 16K rows (the persistent streaming kernel) whose
+    rows hold every finite bf16 value many times over, in shuffled rows and
+    slots, with -0.0 entries and all-zero rows among them: codes and scales
+    bit-exact with the oracle."""
+    from gpu_util import DEV, to_dev_bf16
+    d, hkv, bs, gs = 128, 8, 16, 32
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    fin = bits[np.isfinite(W.bf16_bits_to_f32(bits))]
+    rng = np.random.default_rng(7)
+    n = 2304                                  # tokens: 2304 x 8 heads x (K, V) rows
+    vals = np.concatenate([rng.permutation(fin) for _ in range(2 * n * hkv * d // fin.size + 1)])
+    x = vals[:2 * n * hkv * d].reshape(2, n, hkv, d).copy()
+    x[0, 5] = 0x8000                          # a token of -0.0 rows
+    x[1, 9, 3] = 0                            # an all-zero row
+    nb = n // bs + 3
+    slots = rng.permutation(nb * bs)[:n].astype(np.int32)
+    ng = d // gs if mode == W.SCALE_TOKEN_GROUP else 1
+    kc = torch.zeros((nb, hkv, bs, d), dtype=torch.uint8, device=DEV)
+    vc = torch.zeros_like(kc)
+    ks = torch.zeros((nb, hkv, bs, ng), dtype=torch.float32, device=DEV)
+    vs = torch.zeros_like(ks)
+    F.kv_append_quant(to_dev_bf16(x[0]), to_dev_bf16(x[1]), torch.from_numpy(slots).to(DEV), kc,
+                      vc, ks, vs, fmt=fmt, scale_mode=mode, group_size=gs)
+    assert F.get_device_error() == 0
+    okc = np.zeros((nb, hkv, bs, d), np.uint8)
+    ovc = okc.copy()
+    oks = np.zeros((nb, hkv, bs, ng), np.float32)
+    ovs = oks.copy()
+    assert oracle.kv_append_quant(x[0], x[1], slots, fmt, mode, gs, okc, ovc, oks, ovs, bs) == 0
+    _assert_codes_equal(kc.cpu().numpy(), okc, "k codes")
+    _assert_codes_equal(vc.cpu().numpy(), ovc, "v codes")
+    assert np.array_equal(ks.cpu().numpy().view(np.uint32), oks.view(np.uint32)), "k scales"
+    assert np.array_equal(vs.cpu().numpy().view(np.uint32), ovs.view(np.uint32)), "v scales"
