@@ -199,6 +199,7 @@ DecodePath decode_path(int batch, int q_len, int hq, int hkv, int d, int dv, int
   s.mla = 0;
   s.qlen = q_len;
   s.gqa_tc = 0;
+  s.gs = gs;
   if ((fmt != FP8PA_E4M3 && fmt != FP8PA_E5M2 && fmt != FP8PA_INT8) ||
       (mode != FP8PA_SCALE_TOKEN_HEAD && mode != FP8PA_SCALE_CHANNEL_STATIC &&
        mode != FP8PA_SCALE_TOKEN_GROUP && mode != FP8PA_SCALE_MX_BLOCK &&

@@ -50,6 +50,9 @@ constexpr int kMaxWarps = 8;  // warps per CTA: one per KV head of the CTA's hea
 // KV head.  The high and low f16 parts of q then share one MMA: the high
 // parts in head columns 0..G-1, the low parts in columns G..2G-1.
 constexpr int kModeStaticPacked = 16;
+// MX block mode with blocks of 32 dims (FP8PA_SCALE_MX_BLOCK itself runs the
+// kernel for blocks of 16): the block size is a compile-time constant.
+constexpr int kModeMx32 = 17;
 
 __device__ __forceinline__ int ld_i32(const int* p) { return *reinterpret_cast<const volatile int*>(p); }
 
@@ -84,46 +87,18 @@ struct GqaParams {
 };
 
 // MX block mode helpers.  2^k for an integer k <= 0 as an f16 bit pattern in
-// both halves (f16 subnormals down to 2^-24, then 0).
+// both halves: the fp32 power of two rounded to f16 (exact down to the
+// subnormal 2^-24; 2^-25 and below round to 0).
 __device__ __forceinline__ uint32_t h2_pow2(int k) {
-  const uint32_t h =
-      k >= -14 ? static_cast<uint32_t>(k + 15) << 10 : (k >= -24 ? 1u << (k + 24) : 0u);
-  return h | (h << 16);
+  const float f = __int_as_float((max(k, -126) + 127) << 23);
+  const __half2 h = __floats2half2_rn(f, f);
+  return *reinterpret_cast<const uint32_t*>(&h);
 }
 __device__ __forceinline__ uint32_t hmul2_bits(uint32_t a, uint32_t b) {
   const __half2 r = __hmul2(*reinterpret_cast<const __half2*>(&a),
                             *reinterpret_cast<const __half2*>(&b));
   return *reinterpret_cast<const uint32_t*>(&r);
 }
-// The E8M0 exponent bytes of one token (nb = 2, 4 or 8 of them).
-struct ExpRow {
-  uint32_t w0, w1;
-  __device__ __forceinline__ int byte(int k) const {
-    return static_cast<int>(((k < 4 ? w0 : w1) >> (8 * (k & 3))) & 0xFFu);
-  }
-  __device__ __forceinline__ int max_byte() const {
-    uint32_t m = __vmaxu4(w0, w1);
-    m = __vmaxu4(m, m >> 16);
-    m = __vmaxu4(m, m >> 8);
-    return static_cast<int>(m & 0xFFu);
-  }
-};
-__device__ __forceinline__ ExpRow exp_row(const uint8_t* base, int t, int nb) {
-  ExpRow r;
-  if (nb == 8) {
-    const uint2 x = *reinterpret_cast<const uint2*>(base + t * 8);
-    r.w0 = x.x;
-    r.w1 = x.y;
-  } else if (nb == 4) {
-    r.w0 = *reinterpret_cast<const uint32_t*>(base + t * 4);
-    r.w1 = 0u;
-  } else {
-    r.w0 = *reinterpret_cast<const uint16_t*>(base + t * 2);
-    r.w1 = 0u;
-  }
-  return r;
-}
-
 // Shared-memory layout for `w` warps (each with its own NST-stage ring of
 // 16-token slices of K and V); SCB = scale bytes per token per tensor in the
 // ring (4 for one fp32 scale, D/16 for the largest count of E8M0 block
@@ -176,7 +151,8 @@ __global__ void __launch_bounds__(kMaxWarps * 32)
   constexpr bool SEG = (MODE == FP8PA_SCALE_SEGMENT);  // one scale per (page, KV head)
   constexpr bool TOKSC = (MODE == FP8PA_SCALE_TOKEN_HEAD) || SEG;
   constexpr bool PK = (MODE == kModeStaticPacked);
-  constexpr bool MX = (MODE == FP8PA_SCALE_MX_BLOCK);
+  constexpr bool MX = (MODE == FP8PA_SCALE_MX_BLOCK) || (MODE == kModeMx32);
+  constexpr int GS = MODE == kModeMx32 ? 32 : 16;  // MX: dims per block exponent
   constexpr bool DYN = TOKSC || MX;  // per-token scales: q stays exact in f16
   constexpr int SCB = SEG ? 1 : (TOKSC ? 4 : (MX ? D / 16 : 0));
   constexpr int XS = MxTable<D>::kStride;
@@ -189,7 +165,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32)
   constexpr int KCH = D / 64;  // 16-byte K chunks per row per thread
   constexpr int VW = D / 32;   // V words per token per thread
   constexpr int MT = D / 16;   // dv tiles of 16
-  const int nbx = MX ? D / p.gs : 0;  // exponent bytes per token (MX)
+  constexpr int nbx = MX ? D / GS : 0;  // exponent bytes per token (MX)
   const uint32_t TX = 2 * PAGE + (SEG ? 2 * 16 : (TOKSC ? 2 * 16 * 4 : (MX ? 2 * 16 * nbx : 0)));
 
   extern __shared__ uint8_t smem_raw[];
@@ -475,16 +451,33 @@ __global__ void __launch_bounds__(kMaxWarps * 32)
         // words its fragments need.
         __syncwarp();  // the previous tile's reads are done
         {
-          const ExpRow e = exp_row(lane < 16 ? kex : vex, r0 + (lane & 15), nbx);
-          const int em = e.max_byte();
+          const uint8_t* eb = (lane < 16 ? kex : vex) + (r0 + (lane & 15)) * nbx;
+          uint32_t w[2];
+          if constexpr (nbx == 8) {
+            const uint2 x = *reinterpret_cast<const uint2*>(eb);
+            w[0] = x.x;
+            w[1] = x.y;
+          } else if constexpr (nbx == 4) {
+            w[0] = *reinterpret_cast<const uint32_t*>(eb);
+            w[1] = 0u;
+          } else {
+            w[0] = *reinterpret_cast<const uint16_t*>(eb);
+            w[1] = 0u;
+          }
+          auto ebyte = [&](int k) {
+            return static_cast<int>(__byte_perm(w[k >> 2], 0u, 0x4440u | (k & 3)));
+          };
+          int em = 0;
+#pragma unroll
+          for (int k = 0; k < nbx; ++k) em = max(em, ebyte(k));
           uint32_t* row = xt + lane * XS;
 #pragma unroll
-          for (int k = 0; k < D / 16; ++k)
-            if (k < nbx) row[k] = h2_pow2(e.byte(k) - em);
+          for (int k = 0; k < nbx; ++k) row[k] = h2_pow2(ebyte(k) - em);
           row[D / 16] = __float_as_uint(exp2i(em - 127));
         }
         __syncwarp();
-        const int kb0 = (c * (D / 4)) / p.gs, kb1 = (c * (D / 4) + D / 4 - 1) / p.gs;
+        constexpr int kbs = D / 4;  // dims of a lane's K words (c * kbs ..)
+        const int kb0 = (c * kbs) / GS, kb1 = (c * kbs + kbs - 1) / GS;
         fk0a = xt[g * XS + kb0];
         fk0b = xt[g * XS + kb1];
         fk1a = xt[(g + 8) * XS + kb0];
@@ -502,7 +495,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32)
         codes4_to_f16x2x2<FMT>(kw[0][j], a0, a2);
         codes4_to_f16x2x2<FMT>(kw[1][j], a1, a3);
         if constexpr (MX) {
-          const bool hb = 4 * j >= p.gs;
+          const bool hb = 4 * j >= GS;
           const uint32_t f0 = hb ? fk0b : fk0a, f1 = hb ? fk1b : fk1a;
           a0 = hmul2_bits(a0, f0);
           a2 = hmul2_bits(a2, f0);
@@ -633,7 +626,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32)
       // 2^(e_block - e_max of the token); 2^e_max went into P above.
       uint32_t fv01 = 0u, fv23 = 0u;
       if constexpr (MX) {
-        const int vb = ((D == 128 ? 16 : 8) * g) / p.gs;
+        const int vb = ((D == 128 ? 16 : 8) * g) / GS;
         uint32_t f[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) f[u] = xt[(16 + 4 * c + ((u + c) & 3)) * XS + vb];
@@ -745,7 +738,7 @@ struct SplitKernel {
 template <int D, int BS, int FMT, int MODE>
 SplitKernel pick4() {
   constexpr int NST = stages_for<D>();
-  constexpr bool MX = MODE == FP8PA_SCALE_MX_BLOCK;
+  constexpr bool MX = MODE == FP8PA_SCALE_MX_BLOCK || MODE == kModeMx32;
   constexpr int SCB = MODE == FP8PA_SCALE_SEGMENT
                           ? 1
                           : (MODE == FP8PA_SCALE_TOKEN_HEAD ? 4 : (MX ? D / 16 : 0));
@@ -759,6 +752,9 @@ SplitKernel pick3(int mode) {
     case FP8PA_SCALE_TOKEN_HEAD: return pick4<D, BS, FMT, FP8PA_SCALE_TOKEN_HEAD>();
     case FP8PA_SCALE_MX_BLOCK:  // FP8 codes only (rejected for INT8 before launch)
       if constexpr (FMT != FP8PA_INT8) return pick4<D, BS, FMT, FP8PA_SCALE_MX_BLOCK>();
+      return pick4<D, BS, FMT, FP8PA_SCALE_TOKEN_HEAD>();
+    case kModeMx32:
+      if constexpr (FMT != FP8PA_INT8) return pick4<D, BS, FMT, kModeMx32>();
       return pick4<D, BS, FMT, FP8PA_SCALE_TOKEN_HEAD>();
     case kModeStaticPacked: return pick4<D, BS, FMT, kModeStaticPacked>();
     case FP8PA_SCALE_SEGMENT: return pick4<D, BS, FMT, FP8PA_SCALE_SEGMENT>();
@@ -788,9 +784,11 @@ SplitKernel pick(int d, int bs, int fmt, int mode) {
   return d == 128 ? pick1<128>(bs, fmt, mode) : pick1<64>(bs, fmt, mode);
 }
 
-// Kernel mode of a scale mode for G query heads per KV head.
-int kernel_mode(int mode, int G) {
+// Kernel mode of a scale mode for G query heads per KV head (gs: dims per
+// MX block).
+int kernel_mode(int mode, int G, int gs) {
   const bool pack = mode == FP8PA_SCALE_CHANNEL_STATIC && (G == 1 || G == 2 || G == 4);
+  if (mode == FP8PA_SCALE_MX_BLOCK && gs == 32) return kModeMx32;
   return pack ? kModeStaticPacked : mode;
 }
 
@@ -839,7 +837,7 @@ int decode_workers(const DecodeShape& s, int fmt, int mode, int device) {
   }
   if (g_decode_workers_override > 0) return g_decode_workers_override;
   if (s.gqa_tc) return gqa_tc_workers(s, device);
-  const SplitKernel k = pick(s.d, s.bs, fmt, kernel_mode(mode, s.hq / s.hkv));
+  const SplitKernel k = pick(s.d, s.bs, fmt, kernel_mode(mode, s.hq / s.hkv, s.gs));
   const int qw = gqa_qw(s);
   const int wpc = gqa_wpc(s.hkv, qw, k), hsets = s.hkv / (wpc / qw);
   const int per_sm = ctas_per_sm(reinterpret_cast<const void*>(k.fn), wpc * 32, k.smem(wpc));
@@ -866,7 +864,7 @@ size_t decode_workspace_bytes(const DecodeShape& s) {
 cudaError_t launch_decode_gqa(const DecodeShape& s, const DecodeArgs& a, cudaStream_t stream) {
   if (s.gqa_tc) return launch_decode_gqa_tc(s, a, stream);
   const int G = s.hq / s.hkv;
-  const SplitKernel k = pick(s.d, s.bs, a.fmt, kernel_mode(a.mode, G));
+  const SplitKernel k = pick(s.d, s.bs, a.fmt, kernel_mode(a.mode, G, a.gs));
   const int qw = gqa_qw(s);
   const int bp = s.batch / qw;  // planned requests
   const int wpc = gqa_wpc(s.hkv, qw, k), hsets = s.hkv / (wpc / qw);

@@ -99,6 +99,7 @@ struct DecodeShape {
   int mla_tc;         // 1 when the latent tensor-core kernel serves it (FP8, 64-head groups)
   int qlen;           // queries per request (batch counts request x query)
   int gqa_tc;         // 1 when a grouped-query chunk runs the tensor-core kernel
+  int gs;             // dims per scale group or MX block
 };
 
 // Query warps per KV head in the grouped-query split kernel: a causal chunk of
