@@ -226,3 +226,50 @@ def test_bulk_rows_every_finite_bf16_pattern(F, fmt, mode):
     _assert_codes_equal(vc.cpu().numpy(), ovc, "v codes")
     assert np.array_equal(ks.cpu().numpy().view(np.uint32), oks.view(np.uint32)), "k scales"
     assert np.array_equal(vs.cpu().numpy().view(np.uint32), ovs.view(np.uint32)), "v scales"
+
+
+@pytest.mark.parametrize("fmt", [W.E4M3, W.E5M2, W.INT8])
+@pytest.mark.parametrize("mode", [W.SCALE_TOKEN_HEAD, W.SCALE_TOKEN_GROUP])
+@pytest.mark.parametrize("n_tokens", [40, 2100])
+def test_dynamic_rows_with_infinities_and_nans(F, fmt, mode, n_tokens):
+    """Rows (or groups) holding +-inf get an infinite scale, and their codes
+    come from the exact division x / inf (0 of x's sign, NaN for an infinite
+    x); NaN entries leave the absmax alone.  Small calls (the one-step
+    kernel) and calls above 16K rows (the streaming kernel).  Codes and
+    scales match the oracle; where the quotient is NaN any NaN code is
+    accepted; INT8 codes a NaN quotient as 0 on both sides."""
+    from gpu_util import DEV, to_dev_bf16
+    d, hkv, bs, gs = 128, 4, 16, 32
+    rng = np.random.default_rng(11 + n_tokens)
+    xf = rng.standard_normal((2, n_tokens, hkv, d)).astype(np.float32)
+    x = W.f32_to_bf16_bits(xf).reshape(2, n_tokens, hkv, d)
+    flat = x.reshape(-1)
+    for pat in (0x7F80, 0xFF80, 0x7FC0):       # +inf, -inf, NaN
+        idx = rng.choice(flat.size, size=max(4, flat.size // 997), replace=False)
+        flat[idx] = pat
+    nb = n_tokens // bs + 2
+    slots = rng.permutation(nb * bs)[:n_tokens].astype(np.int32)
+    ng = d // gs if mode == W.SCALE_TOKEN_GROUP else 1
+    kc = torch.zeros((nb, hkv, bs, d), dtype=torch.uint8, device=DEV)
+    vc = torch.zeros_like(kc)
+    ks = torch.zeros((nb, hkv, bs, ng), dtype=torch.float32, device=DEV)
+    vs = torch.zeros_like(ks)
+    F.kv_append_quant(to_dev_bf16(x[0]), to_dev_bf16(x[1]), torch.from_numpy(slots).to(DEV), kc,
+                      vc, ks, vs, fmt=fmt, scale_mode=mode, group_size=gs)
+    assert F.get_device_error() == 0
+    okc = np.zeros((nb, hkv, bs, d), np.uint8)
+    ovc = okc.copy()
+    oks = np.zeros((nb, hkv, bs, ng), np.float32)
+    ovs = oks.copy()
+    assert oracle.kv_append_quant(x[0], x[1], slots, fmt, mode, gs, okc, ovc, oks, ovs, bs) == 0
+    for got, want, what in ((kc, okc, "k"), (vc, ovc, "v")):
+        got = got.cpu().numpy().reshape(-1)
+        want = want.reshape(-1)
+        nan_want = np.isnan(oracle.fp8_decode(want, fmt)) if fmt != W.INT8 else None
+        if nan_want is not None:
+            assert np.isnan(oracle.fp8_decode(got[nan_want], fmt)).all(), what
+            _assert_codes_equal(got[~nan_want], want[~nan_want], what)
+        else:
+            _assert_codes_equal(got, want, what)
+    assert np.array_equal(ks.cpu().numpy().view(np.uint32), oks.view(np.uint32)), "k scales"
+    assert np.array_equal(vs.cpu().numpy().view(np.uint32), ovs.view(np.uint32)), "v scales"
