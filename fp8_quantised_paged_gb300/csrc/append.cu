@@ -15,8 +15,9 @@
 // the nearest integer, ties to even, clamped to [-127, 127].
 //
 // A group of lanes per (token, kv head, K-or-V) row, several rows per warp.
-// Each lane owns 8 contiguous values per 16-byte chunk (one 16-byte load, one
-// 8-byte code store).  Every quotient is the IEEE fp32 round-to-nearest one
+// Each lane owns 8 contiguous values per 16-byte chunk (one 16-byte load and
+// 8 bytes of codes; a lane with consecutive chunks stores two chunks' codes
+// at once).  Every quotient is the IEEE fp32 round-to-nearest one
 // (__fdiv_rn for the scales and static channel scales; for per-token and
 // per-group scales a reciprocal per scale and a corrected product, see
 // quot_rn) and the FP8 cast is the hardware cvt.rn.satfinite (INT8:
