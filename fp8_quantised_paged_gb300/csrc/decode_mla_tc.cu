@@ -661,8 +661,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!dead) {
           int ntok[2];
           pair_tokens(j, ntok);
-          for (int n = 0; n < 16 && !dead; ++n)
-            if (!build_double(n, 1, t, ntok, fills_s)) dead = true;
+          // unrolled by 4: the double slot's index arithmetic folds into
+          // constants (by 8 or fully, the larger loop body costs more than
+          // that saves)
+#pragma unroll 4
+          for (int n = 0; n < 16; ++n)
+            if (!dead && !build_double(n, 1, t, ntok, fills_s)) dead = true;
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_stage);
@@ -716,7 +720,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         pair_tokens(j, ntok);
         if (!wait_warp(bar_full, pc & 1)) break;
         bool ok = true;
-        for (int n = 0; n < 16 && ok; ++n) ok = build_double(n, 0, bt, ntok, fills_b);
+#pragma unroll 4
+        for (int n = 0; n < 16; ++n)
+          if (ok) ok = build_double(n, 0, bt, ntok, fills_b);
         if (!ok) break;
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_stage);
