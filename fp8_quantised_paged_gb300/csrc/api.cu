@@ -500,17 +500,19 @@ size_t fp8pa_multiquery_workspace_bytes(int batch, int q_len, int n_q_heads, int
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
   // The largest need over the scale modes and formats of this layout (the
-  // split count follows each kernel's occupancy).
+  // split count follows each kernel's occupancy; MX blocks of 16 and of 32
+  // dims run different kernels).
   const bool mla = head_dim == 576;
-  const int modes[4] = {mla ? FP8PA_SCALE_TOKEN_GROUP : FP8PA_SCALE_TOKEN_HEAD,
+  const int modes[5] = {mla ? FP8PA_SCALE_TOKEN_GROUP : FP8PA_SCALE_TOKEN_HEAD,
                         mla ? FP8PA_SCALE_SEGMENT : FP8PA_SCALE_CHANNEL_STATIC,
-                        FP8PA_SCALE_MX_BLOCK, FP8PA_SCALE_SEGMENT};
+                        FP8PA_SCALE_MX_BLOCK, FP8PA_SCALE_MX_BLOCK, FP8PA_SCALE_SEGMENT};
+  const int sizes[5] = {mla ? 64 : 16, mla ? 64 : 16, 16, 32, 16};
   size_t need = 0;
-  for (int m = 0; m < (mla ? 2 : 4); ++m)
+  for (int m = 0; m < (mla ? 2 : 5); ++m)
     for (int fmt = FP8PA_E4M3; fmt <= FP8PA_INT8; ++fmt) {
       DecodePath path = decode_path(batch * q_len, q_len, n_q_heads, n_kv_heads, head_dim,
                                     head_dim_v, block_size, max_blocks_per_seq, fmt, modes[m],
-                                    mla ? 64 : 16, 1, FP8PA_OUT_BF16);
+                                    sizes[m], 1, FP8PA_OUT_BF16);
       if (path.status != FP8PA_OK) continue;
       path.shape.workers = decode_workers(path.shape, fmt, modes[m], dev);
       const size_t n = decode_workspace_bytes(path.shape);
