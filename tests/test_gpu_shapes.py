@@ -182,3 +182,39 @@ def test_blocks_beyond_4gib_of_cache(F, case):
     finally:
         g = None
         torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("gs", [16, 32])
+@pytest.mark.parametrize("fmt", [E4, E5])
+def test_mx_blocks_spanning_the_f16_factor_range(F, gs, fmt):
+    """Blocks of one token whose exponents lie up to 2^40 below the token's
+    largest (and all-zero blocks), so the decode's per-block factors
+    2^(e_k - e_max) take normal f16 values, f16 subnormals (2^-15 .. 2^-24)
+    and 0: exponents and codes bit-exact, attention (f32) within tolerance
+    of the oracle."""
+    from gpu_util import check_close, gpu_attention, gpu_cache, oracle_attention, oracle_cache
+    d, bs = 128, 16
+    w = W.make_shape_case(f"mx{gs}_factor_range", [1, bs - 1, 3 * bs + 5, 70], 16, 2, d, bs,
+                          fmt, MX, seed=3300 + gs + fmt, group_size=gs)
+    rng = np.random.default_rng(3300 + gs + fmt)
+    pw = np.array([0, -6, -12, -15, -18, -21, -24, -26, -40], np.float32)
+    kvs = []
+    for b in range(w.batch):
+        L = int(w.seq_lens[b])
+        pair = []
+        for _ in range(2):
+            x = rng.standard_normal((L, w.n_kv_heads, d)).astype(np.float32)
+            xb = x.reshape(L, w.n_kv_heads, d // gs, gs)
+            f = np.exp2(rng.choice(pw, size=(L, w.n_kv_heads, d // gs))).astype(np.float32)
+            f[rng.random(f.shape) < 0.1] = 0.0  # all-zero blocks
+            xb *= f[..., None]
+            pair.append(W.f32_to_bf16_bits(x))
+        kvs.append(tuple(pair))
+    g = gpu_cache(w, F, kvs)
+    o = oracle_cache(w, kvs)
+    for got, want, what in zip(g, o, ("K codes", "V codes", "K exponents", "V exponents")):
+        assert np.array_equal(got.cpu().numpy(), want), what
+    q = W.queries(w)
+    check_close(gpu_attention(w, F, q, g, out_dtype=torch.float32), oracle_attention(w, q, o),
+                bf16_out=False, what=f"mx{gs} factor range f32")
+    assert F.get_device_error() == 0
