@@ -122,11 +122,13 @@ __device__ __forceinline__ uint2 lds64(uint32_t addr) {
 }
 
 // ---------------------------------------------------------------- code conversions
-// INT8 codes b in [-128, 127] -> f16, exactly: the byte b + 128 becomes the
-// low mantissa byte of the f16 1024 (giving 1024 + b + 128), then 1152 is
-// subtracted.  `sel` picks the two bytes of `four_codes` (byte permute).
+// INT8 codes -> f16, exactly.  A code is stored as its integer b + 128
+// (excess-128, b in [-127, 127]), so the byte itself becomes the low
+// mantissa byte of the f16 1024 (giving 1024 + b + 128) and 1152 is
+// subtracted: one byte permute and one f16 subtract per pair.  `sel` picks
+// the two bytes of `four_codes`.
 __device__ __forceinline__ uint32_t int8x2_to_f16x2(uint32_t four_codes, uint32_t sel) {
-  const uint32_t biased = __byte_perm(four_codes ^ 0x80808080u, 0x64646464u, sel);
+  const uint32_t biased = __byte_perm(four_codes, 0x64646464u, sel);
   const __half2 r = __hsub2(*reinterpret_cast<const __half2*>(&biased),
                             __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480)));
   return *reinterpret_cast<const uint32_t*>(&r);
@@ -168,13 +170,13 @@ __device__ __forceinline__ void codes4_to_f16x2x2(uint32_t four_codes, uint32_t&
 
 // Two fp32 values -> two codes (lo -> low byte), round to nearest even.
 // FP8: finite overflow saturated to +-max, NaN to NaN.  INT8: clamped to
-// [-127, 127] (infinities too), NaN to 0.
+// [-127, 127] (infinities too), NaN to 0, stored + 128.
 template <int FMT>
 __device__ __forceinline__ uint32_t f32x2_to_codes2(float lo, float hi) {
   if constexpr (FMT == FP8PA_INT8) {
-    const int a = min(127, max(-127, __float2int_rn(lo)));
-    const int b = min(127, max(-127, __float2int_rn(hi)));
-    return (static_cast<uint32_t>(a) & 0xFFu) | ((static_cast<uint32_t>(b) & 0xFFu) << 8);
+    const int a = min(127, max(-127, __float2int_rn(lo))) + 128;
+    const int b = min(127, max(-127, __float2int_rn(hi))) + 128;
+    return static_cast<uint32_t>(a) | (static_cast<uint32_t>(b) << 8);
   }
   uint16_t r;
   if constexpr (FMT == FP8PA_E4M3) {

@@ -80,8 +80,9 @@ extern "C" {
 #define FP8PA_DEVERR_TIMEOUT 8u      /* decode: a bounded wait on an async copy ran out (work abandoned) */
 
 /* Code formats: FP8 E4M3 and E5M2, and symmetric INT8 (the alternate KV
- * codec; FMAX = 127, codes in [-127, 127] as two's complement bytes, value
- * = the integer; not with FP8PA_SCALE_MX_BLOCK). */
+ * codec; FMAX = 127, integer codes in [-127, 127] stored as the byte
+ * integer + 128 (bytes 1 .. 255, 128 for zero), value = byte - 128; not
+ * with FP8PA_SCALE_MX_BLOCK). */
 #define FP8PA_E4M3 0
 #define FP8PA_E5M2 1
 #define FP8PA_INT8 2
@@ -126,7 +127,7 @@ extern "C" {
  *               Blackwell; codes = fp8_rne_satfinite(x * 2^-e), exact scaling.
  * code          = fp8_rne_satfinite(x / s), IEEE fp32 division; INT8:
  *               x / s rounded to the nearest integer, ties to even, clamped
- *               to [-127, 127] (an INT8 KV cache is named only as a serving
+ *               to [-127, 127], stored + 128 (an INT8 KV cache is named only as a serving
  *               option, hotelren.com/news/5166672, inference-engine settings;
  *               the rest is this library's reading).  Codes are bit-exact
  *               with the definition above.  MX_BLOCK is FP8 only

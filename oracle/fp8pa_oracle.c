@@ -64,8 +64,9 @@
  * Reading: symmetric codes with FMAX = 127 in place of the FP8 maximum, so
  * the scale is fp32 absmax / 127 (IEEE division, clamped at 1e-12) and the
  * code is x / scale rounded to the nearest integer, ties to even, clamped
- * to [-127, 127], stored as a two's complement byte; a code's value is
- * its integer.  The power-of-two block mode is defined for FP8 only.
+ * to [-127, 127], stored as the byte integer + 128 (excess-128: bytes 1 ..
+ * 255, 128 for zero); a code's value is its integer, byte - 128.  The
+ * power-of-two block mode is defined for FP8 only.
  */
 #include <math.h>
 #include <stdint.h>
@@ -105,7 +106,7 @@ double or_fp8_max(int fmt) {
  * E5M2: 1 sign, 5 exponent (bias 15), 2 mantissa bits; exponent field 0 is
  *       subnormal (m/4)*2^-14; exponent field 31 is inf (m = 0) or NaN. */
 double or_fp8_decode(uint8_t code, int fmt) {
-  if (fmt == OR_INT8) return (double)(int8_t)code;
+  if (fmt == OR_INT8) return (double)((int)code - 128);
   int neg = (code >> 7) & 1;
   double mag;
   if (fmt == OR_E4M3) {
@@ -130,17 +131,17 @@ double or_fp8_decode(uint8_t code, int fmt) {
 }
 
 /* fp32 -> INT8 code: the nearest integer (from the floor and the remainder),
- * ties to the even one, clamped to [-127, 127]; NaN -> 0. */
+ * ties to the even one, clamped to [-127, 127], NaN -> 0; stored + 128. */
 static uint8_t or_int8_encode(float x) {
-  if (isnan(x)) return 0;
+  if (isnan(x)) return 128;
   const double xd = (double)x;
-  if (xd >= 127.0) return 127;
-  if (xd <= -127.0) return (uint8_t)(int8_t)-127;
+  if (xd >= 127.0) return 127 + 128;
+  if (xd <= -127.0) return -127 + 128;
   const double f = floor(xd);
   const double r = xd - f; /* exact: |xd| < 2^7 */
   long n = (long)f;
   if (r > 0.5 || (r == 0.5 && (n & 1l))) n += 1;
-  return (uint8_t)(int8_t)n;
+  return (uint8_t)(n + 128);
 }
 
 /* fp32 -> FP8 code by integer manipulation of the fp32 bit pattern:
@@ -196,9 +197,9 @@ uint8_t or_fp8_encode_bruteforce(float x, int fmt) {
   if (fmt == OR_INT8) {
     /* beyond the range it clamps; inside, scan every integer in
      * [-127, 127] for the nearest, ties to the even one */
-    if (isnan(x)) return 0;
-    if ((double)x >= 127.0) return 127;
-    if ((double)x <= -127.0) return (uint8_t)(int8_t)-127;
+    if (isnan(x)) return 128;
+    if ((double)x >= 127.0) return 127 + 128;
+    if ((double)x <= -127.0) return -127 + 128;
     int best = 0;
     double bestd = INFINITY;
     for (int c = -127; c <= 127; ++c) {
@@ -208,7 +209,7 @@ uint8_t or_fp8_encode_bruteforce(float x, int fmt) {
         best = c;
       }
     }
-    return (uint8_t)(int8_t)best;
+    return (uint8_t)(best + 128);
   }
   if (isnan(x)) return 0x7F;
   const double xd = (double)x;

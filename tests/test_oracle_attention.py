@@ -12,8 +12,7 @@ import torch
 import oracle
 from fp8_quantised_paged_gb300 import workloads as W
 
-TORCH_T = {oracle.E4M3: torch.float8_e4m3fn, oracle.E5M2: torch.float8_e5m2,
-           oracle.INT8: torch.int8}
+TORCH_T = {oracle.E4M3: torch.float8_e4m3fn, oracle.E5M2: torch.float8_e5m2}
 
 
 def build_cache(w):
@@ -41,14 +40,17 @@ def build_cache(w):
 
 
 def dequant_request(w, cache, scale, b):
-    """[L, Hkv, D] float64 through torch's float8 (or int8) decode, not the
-    oracle's."""
+    """[L, Hkv, D] float64 through torch's float8 decode (INT8: the byte less
+    128), not the oracle's."""
     L = int(w.seq_lens[b])
     t = np.arange(L)
     blk = w.block_tables[b, t // w.block_size]
     off = t % w.block_size
     codes = torch.from_numpy(cache[blk, :, off, :].copy())          # [L, Hkv, D]
-    vals = codes.view(TORCH_T[w.fmt]).to(torch.float64)
+    if w.fmt == oracle.INT8:
+        vals = codes.to(torch.float64) - 128.0
+    else:
+        vals = codes.view(TORCH_T[w.fmt]).to(torch.float64)
     if w.scale_mode == W.SCALE_TOKEN_HEAD:
         s = torch.from_numpy(scale[blk, :, off, 0].astype(np.float64))[..., None]
     elif w.scale_mode == W.SCALE_TOKEN_GROUP:
@@ -263,7 +265,9 @@ def test_int8_attention_matches_torch_sdpa(mode, hq, hkv, d, bs):
     w = W.make_shape_case("int8", [1, bs - 1, bs, bs + 1, 3 * bs + 5], hq, hkv, d, bs, W.INT8,
                           mode, seed=41)
     kc, vc, ks, vs = build_cache(w)
-    assert kc.view(np.int8).min() >= -127
+    for b in range(w.batch):  # written codes are bytes 1 .. 255 (integers -127 .. 127)
+        t = np.arange(int(w.seq_lens[b]))
+        assert kc[w.block_tables[b, t // bs], :, t % bs, :].min() >= 1
     q = W.queries(w)
     got = run_oracle(w, q, kc, vc, ks, vs)
     ref = sdpa_reference(w, q, kc, vc, ks, vs)

@@ -111,23 +111,24 @@ def test_encode_nan_and_inf():
     assert list(oracle.fp8_encode(x, oracle.E5M2)) == [0x7F, 0x7B, 0xFB]
 
 
-def test_int8_decode_is_the_twos_complement_integer():
+def test_int8_decode_is_the_excess_128_integer():
     codes = np.arange(256, dtype=np.uint8)
-    want = codes.view(np.int8).astype(np.float64)
+    want = codes.astype(np.float64) - 128.0
     assert np.array_equal(oracle.fp8_decode(codes, oracle.INT8), want)
 
 
 def test_int8_encode_matches_numpy_rint_and_bruteforce():
     """Symmetric INT8 codes: nearest integer, ties to even (numpy's rint),
-    clamped to [-127, 127]; every half-integer tie in range and random
-    values, against numpy and against the oracle's own scan of all codes."""
+    clamped to [-127, 127], stored + 128; every half-integer tie in range and
+    random values, against numpy and against the oracle's own scan of all
+    codes."""
     rng = np.random.default_rng(11)
     ties = np.arange(-130, 130).astype(np.float32) + np.float32(0.5)
     rand = rng.uniform(-300.0, 300.0, 20000).astype(np.float32)
     edges = np.array([0.0, -0.0, 126.5, -126.5, 127.0, -127.0, 127.49, -127.5, 1e30, -1e30,
                       np.inf, -np.inf], np.float32)
     x = np.concatenate([ties, rand, edges])
-    want = np.clip(np.rint(x.astype(np.float64)), -127, 127).astype(np.int8).view(np.uint8)
+    want = (np.clip(np.rint(x.astype(np.float64)), -127, 127) + 128).astype(np.uint8)
     assert np.array_equal(oracle.fp8_encode(x, oracle.INT8), want)
     fin = np.isfinite(x)
     assert np.array_equal(oracle.fp8_encode_bruteforce(x[fin], oracle.INT8), want[fin])
